@@ -1,0 +1,423 @@
+"""Throughput of the DP-SGD private-gradient step (norms -> clip -> clipped sum
+-> noise -> /L) on GB300, through the library's C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  A step is one pass of the whole path over one
+batch of synthetic records already resident in HBM: every
+dp_norm_accumulate (one batched call), dp_clip_factors and
+dp_clipped_noisy_grad.  The metric is clipped+noised examples per second over
+all ranks.  Under torchrun each rank processes its own batch (weak scaling,
+no collective on the data path of the timed step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "clipped+noised examples/sec per step; TFLOP/s & HBM GB/s as % of GB300 roofline"
+UNIT = "examples/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", type=int, default=2, help="workload index 1..5 (default: 2)")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-budget-s", type=float, default=12.0)
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_traffic(kernel: str):
+    """dram read+write bytes per launch from the committed ncu summary, or None
+    when the kernel's source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path)).get(kernel)
+    if not d:
+        return None
+    src = os.path.join(ROOT, d["source"])
+    if not os.path.exists(src):
+        return None
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != d["source_sha256"]:
+        return None
+    return d["bytes_per_launch"]
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------- work accounting
+def work_model(w):
+    """Algorithmic work of one step, per phase (one batch of w.B records).
+
+    Norm phase: ghost layers with T > 1 do the two symmetric Grams,
+    B T^2 (d_in + d_out) flops (tensor); T = 1 and materialized layers read
+    A and E once (HBM).  Gradient phase: ghost layers do the reweighted
+    GEMM, 2 B T d_in d_out flops (tensor); materialized layers read their
+    stored per-example gradients once and write G (HBM)."""
+    import differentially_private_gb300 as dp
+    esz = 4 if w.dtype == "f32" else 2
+    norm_flops = norm_bytes = grad_flops = grad_bytes = 0
+    for ly in w.layers:
+        ab = w.B * ly.T * (ly.d_in + ly.d_out) * esz
+        ncl = ly.d_out * ly.d_in + (ly.d_out if ly.has_bias else 0)
+        if dp.dp_choose_path(ly.T, ly.d_in, ly.d_out) == dp.DP_PATH_GHOST:
+            if ly.T == 1:
+                norm_bytes += ab
+            else:
+                norm_flops += w.B * ly.T * ly.T * (ly.d_in + ly.d_out)
+            grad_flops += 2 * w.B * ly.T * ly.d_in * ly.d_out
+            grad_bytes += ab + 4 * ncl
+        else:
+            norm_bytes += ab
+            grad_bytes += 4 * ncl * (w.B + 1)
+    return {"norm_flops": norm_flops, "norm_bytes": norm_bytes, "grad_flops": grad_flops, "grad_bytes": grad_bytes}
+
+
+# ------------------------------------------------------------ CPU oracle leg
+def oracle_sample_rate(w, A_host, E_host, budget_s: float):
+    """Oracle throughput (examples/s) on a bounded sample of the workload.
+
+    The oracle materializes every per-example gradient in float64.  Its
+    per-record work is timed on the first b records (b grows until the budget
+    is used or the batch is exhausted) and the noise of all P coordinates is
+    timed on a sample of coordinates; the full-batch step time is
+    t_records * B / b + t_noise * P / p."""
+    import numpy as np
+    from oracle import dpsgd, philox
+
+    layers = [dpsgd.Layer(ly.d_in, ly.d_out, ly.has_bias) for ly in w.layers]
+    t0 = time.perf_counter()
+    b = 0
+    while b < w.B and time.perf_counter() - t0 < budget_s * 0.8:
+        n2 = 0.0
+        for ly, A, E in zip(layers, A_host, E_host):
+            n2 += dpsgd.record_sqnorm(A[b], E[b], ly.has_bias)
+        c = dpsgd.clip_factors(np.array([n2]), w.C)[0]
+        for ly, A, E in zip(layers, A_host, E_host):
+            g, bb = dpsgd.per_example_grad(A[b], E[b], ly.has_bias)
+            _ = c * g
+        b += 1
+    t_rec = time.perf_counter() - t0
+    P = w.ncoords
+    p = min(P, 1 << 22)
+    t1 = time.perf_counter()
+    philox.normals(w.noise_seed, w.step, 0, p)
+    t_noise = (time.perf_counter() - t1) * P / p
+    t_full = t_rec * w.B / b + t_noise
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"oracle float64 on {b} of {w.B} records (materialize, clip, scale) timed, scaled to B; "
+              f"noise timed on {p} of {P} coordinates, scaled to P")
+    return w.B / t_full, cores, sample, t_full
+
+
+def host_inputs(w, device="cuda"):
+    import torch
+    from synthetic import generate_layer
+    A_host, E_host = [], []
+    for i in range(len(w.layers)):
+        a, e = generate_layer(w, i, device)
+        A_host.append(a.to("cpu", torch.float64).numpy())
+        E_host.append(e.to("cpu", torch.float64).numpy())
+        del a, e
+    return A_host, E_host
+
+
+# ------------------------------------------------------------------- arms
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import torch  # noqa: F401
+    A_host, E_host = host_inputs(w, "cpu")
+    per = max(2.0, args.cpu_budget_s / max(1, args.steps + args.warmup) * 4)
+    for _ in range(args.warmup):
+        oracle_sample_rate(w, A_host, E_host, min(per, 2.0))
+    times = []
+    rate, cores, sample = None, None, None
+    for _ in range(args.steps):
+        rate, cores, sample, t_full = oracle_sample_rate(w, A_host, E_host, per)
+        times.append(t_full)
+    t_step = statistics.mean(times)
+    value = w.B / t_step
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "layers": len(w.layers)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+    import differentially_private_gb300 as dp
+    from synthetic import generate_layer
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dp.load_library()
+
+    layers = [(ly.d_in, ly.d_out, ly.has_bias) for ly in w.layers]
+    A_dev, E_dev = [], []
+    for i in range(len(w.layers)):
+        a, e = generate_layer(w, i, device)
+        A_dev.append(a)
+        E_dev.append(e)
+    T_list = [ly.T for ly in w.layers]
+    stream = torch.cuda.current_stream(device)
+    pg = dp.PrivateGradient(layers, dtype=w.torch_dtype, device=local, stream=stream)
+    grads, clip, sq = pg.alloc_outputs(w.B)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    ctx = pg.ctx
+    ids = list(range(len(layers)))
+
+    def step(evs=None):
+        dp.dp_begin_step(ctx, w.B)
+        if evs:
+            evs[0].record(stream)
+        dp.dp_norm_accumulate_batch(ctx, ids, A_dev, E_dev, T_list, None)
+        if evs:
+            evs[1].record(stream)
+        dp.dp_clip_factors(ctx, w.C, clip, sq)
+        if evs:
+            evs[2].record(stream)
+        dp.dp_clipped_noisy_grad(ctx, w.sigma, w.noise_seed, w.step, grads)
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = dp.dp_step_status(ctx)
+    if st != dp.DP_OK:
+        raise dp.DPError(st, "dp_step_status", dp.dp_last_error(ctx))
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    n_launch0 = dp.dp_kernel_launches()
+    for k in range(K):
+        flush.zero_()
+        step(evs[k])
+    torch.cuda.synchronize()
+    n_launch = dp.dp_kernel_launches() - n_launch0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    st = dp.dp_step_status(ctx)
+    if st != dp.DP_OK:
+        raise dp.DPError(st, "dp_step_status", dp.dp_last_error(ctx))
+
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    norm_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    clip_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    grad_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * w.B * K / (total_ms / 1e3)
+
+    # roofline of the dominant phase
+    peaks = load_peaks()
+    wm = work_model(w)
+    mn, mg = statistics.mean(norm_ms), statistics.mean(grad_ms)
+    if mn >= mg:
+        phase, t_ms, flops, bytes_ = "norm", mn, wm["norm_flops"], wm["norm_bytes"]
+    else:
+        phase, t_ms, flops, bytes_ = "grad", mg, wm["grad_flops"], wm["grad_bytes"]
+    tc_time = flops / (peaks["bf16_tflops"] * 1e12)
+    hb_time = bytes_ / (peaks["hbm_gbs"] * 1e9)
+    if tc_time >= hb_time and flops > 0:
+        ach = flops / (t_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16_tflops"]}
+    else:
+        ach = bytes_ / (t_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"]}
+    kernel_name = {("norm", "hbm"): "norm_mat", ("norm", "tensor"): "norm_ghost",
+                   ("grad", "tensor"): "grad_gemm", ("grad", "hbm"): "grad_wsum"}[(phase, roof["bound"])]
+    roof["traffic"] = kernel_traffic(kernel_name)
+    roof["phase"] = phase
+    roof["peak_source"] = peaks["source"]
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        A_pin = [a.cpu().pin_memory() for a in A_dev]
+        E_pin = [e.cpu().pin_memory() for e in E_dev]
+        G_pin = [torch.empty(g.numel(), dtype=torch.float32).pin_memory() for g in grads]
+        h2d = sum(a.numel() * a.element_size() for a in A_pin) + sum(e.numel() * e.element_size() for e in E_pin)
+        d2h = sum(g.numel() * 4 for g in G_pin)
+
+        def e2e_step():
+            for a_d, a_h in zip(A_dev, A_pin):
+                a_d.copy_(a_h, non_blocking=True)
+            for e_d, e_h in zip(E_dev, E_pin):
+                e_d.copy_(e_h, non_blocking=True)
+            step()
+            for g_h, g_d in zip(G_pin, grads):
+                g_h.copy_(g_d, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        ke = max(3, min(K, 10))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ems], device=device, dtype=torch.float64)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * w.B * ke / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        A_host = [a.to("cpu", torch.float64).numpy() for a in A_dev]
+        E_host = [e.to("cpu", torch.float64).numpy() for e in E_dev]
+        rate, cores, sample, _ = oracle_sample_rate(w, A_host, E_host, args.cpu_budget_s)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "layers": len(w.layers),
+                       "T": sorted({ly.T for ly in w.layers}), "C": w.C, "sigma": w.sigma,
+                       "l2": f"flushed: {L2_FLUSH_BYTES >> 20} MB written before every timed step",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": n_launch,
+            "clocks": clk,
+            "phases_ms": {"norm": mn, "clip": statistics.mean(clip_ms), "grad": mg},
+        }
+        print(json.dumps(line), flush=True)
+    pg.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    from synthetic import by_index
+    w = by_index(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

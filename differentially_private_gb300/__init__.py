@@ -1,0 +1,45 @@
+"""GB300-native DP-SGD private-gradient hot path (clip + noise).
+
+The work is done by ``libdpclip.so`` (hand-written CUDA for sm_103a) behind
+the C ABI of ``include/dp_clip.h``; this package is its ctypes binding
+(``_binding``, same names as the C entry points), a convenience wrapper
+(``step.PrivateGradient``) and the in-tree build (``build``).
+"""
+
+from ._binding import (  # noqa: F401
+    DP_BF16,
+    DP_ERR_CUDA,
+    DP_ERR_INVALID_ARG,
+    DP_ERR_NONFINITE,
+    DP_ERR_OOM,
+    DP_ERR_SHAPE,
+    DP_ERR_STATE,
+    DP_ERR_UNSUPPORTED,
+    DP_F32,
+    DP_OK,
+    DP_PATH_GHOST,
+    DP_PATH_MATERIALIZE,
+    DPError,
+    EXPORTS,
+    LIB_PATH,
+    dp_begin_step,
+    dp_choose_path,
+    dp_clip_factors,
+    dp_clipped_noisy_grad,
+    dp_create,
+    dp_destroy,
+    dp_kernel_launches,
+    dp_last_error,
+    dp_layer_info,
+    dp_norm_accumulate,
+    dp_norm_accumulate_batch,
+    dp_num_coords,
+    dp_philox_normals,
+    dp_register_layer,
+    dp_set_normalizer,
+    dp_status_string,
+    dp_step_status,
+    dp_version,
+    load_library,
+)
+from .step import PrivateGradient, StepOutput  # noqa: F401

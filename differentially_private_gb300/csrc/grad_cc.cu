@@ -1,0 +1,238 @@
+// Clip factors, the reweighted clipped sum with its noise epilogue on the
+// CUDA cores, the weighted sum of stored per-example gradients, and the
+// standalone noise generator.
+//
+//   n2_i = sum over layers (registration order) of the layer's partials
+//   c_i  = 1 if sqrt(n2_i) <= C, else C / sqrt(n2_i) rounded toward zero
+//   G    = (sum_i c_i g_i + sigma C z) / L
+// ("Privacy-Preserving Machine Learning", section "Differentially private
+// stochastic gradient descent", phases 3-5; "Differential Privacy in
+// Fine-Tuning (DP-SGD)", "Per-Sample Gradient Clipping" and "Calibrated
+// Gaussian Noise Addition"; "Sensitivity Inflation from Cross-Record
+// Precision Routing in Private Quantized Fine-Tuning", Eq. 2 and Eq. 3.)
+#include "common.cuh"
+
+using namespace dpk;
+
+namespace {
+
+// --------------------------------------------------------------- clipping
+// One warp per record.  Lane l sums slots l, l+32, ... of every layer in
+// registration order, then the lanes are combined by a fixed butterfly, so
+// the result depends only on the record's partials and the slot counts.
+__global__ void __launch_bounds__(256) k_clip(const ClipParams p, float* __restrict__ n2_out,
+                                              float* __restrict__ c_out, float* __restrict__ n2_user,
+                                              float* __restrict__ c_user, unsigned* __restrict__ status) {
+    const int64_t rec = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (rec >= p.B) return;
+    float s = 0.f;
+    for (int l = 0; l < p.nlayers; ++l) {
+        const int ns = p.nslots[l];
+        const float* part = p.partial[l] + rec * ns;
+        for (int j = lane; j < ns; j += 32) s += part[j];
+    }
+    s = warp_sum(s);
+    if (lane == 0) {
+        float c;
+        if (!isfinite(s)) {
+            atomicOr(status, 1u);
+            c = 0.f;
+        } else {
+            const float n = sqrtf(s);
+            // C / n rounded toward zero keeps c * n <= C in float arithmetic
+            c = (n <= p.C) ? 1.0f : __fdiv_rz(p.C, n);
+        }
+        n2_out[rec] = s;
+        c_out[rec] = c;
+        if (n2_user) n2_user[rec] = s;
+        if (c_user) c_user[rec] = c;
+    }
+}
+
+// --------------------------------------------- stored-gradient weighted sum
+struct WsumParams {
+    int n;
+    GradTask t[kMaxGroup];
+};
+
+// blockIdx.y = layer of the group; each thread owns one Philox block of the
+// layer's coordinates (up to 4 coordinates) and sums c_i g_i[p] over records
+// in ascending order.
+__global__ void __launch_bounds__(256) k_grad_wsum(const WsumParams P, const float* __restrict__ c,
+                                                   const unsigned* __restrict__ status, StepScalars sc) {
+    if (status_bad(status)) return;
+    const GradTask& t = P.t[blockIdx.y];
+    const int64_t ncl = t.d_out * t.d_in + (t.has_bias ? t.d_out : 0);
+    const int64_t j0 = t.coord_off >> 2;
+    const int64_t j_last = (t.coord_off + ncl - 1) >> 2;
+    const float scale = sc.sigma * sc.C;
+    for (int64_t j = j0 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j <= j_last;
+         j += (int64_t)gridDim.x * blockDim.x) {
+        const float4 z4 = noise4(sc.seed, sc.step, (uint64_t)j);
+        const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int64_t p = 4 * j + q - t.coord_off;
+            if (p < 0 || p >= ncl) continue;
+            float acc = 0.f;
+            for (int64_t i = 0; i < sc.B; ++i) acc = fmaf(c[i], t.gstore[i * ncl + p], acc);
+            t.G[p] = (acc + scale * zz[q]) / sc.L;
+        }
+    }
+}
+
+// ---------------------------------------- reweighted E^T diag(c) A (CUDA core)
+constexpr int kBM = 64, kBN = 64, kBK = 16;
+
+template <int DT>
+__global__ void __launch_bounds__(256) k_grad_gemm_cc(const GradTask t, const float* __restrict__ c,
+                                                      const unsigned* __restrict__ status, StepScalars sc) {
+    using Tt = typename Elem<DT>::T;
+    if (status_bad(status)) return;
+    __shared__ float Es[kBK][kBM];
+    __shared__ float As[kBK][kBN];
+    const int tid = threadIdx.x;
+    const int tr = tid >> 4, tc = tid & 15;
+    const int64_t m0 = (int64_t)blockIdx.y * kBM, n0 = (int64_t)blockIdx.x * kBN;
+    const int64_t K = sc.B * t.T;
+    const Tt* E = (const Tt*)t.E;
+    const Tt* A = (const Tt*)t.A;
+    float acc[4][4] = {};
+    float bsum = 0.f;
+    const bool do_bias = t.has_bias && blockIdx.x == 0;
+    for (int64_t k0 = 0; k0 < K; k0 += kBK) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int idx = tid + 256 * r;
+            const int kk = idx >> 6, col = idx & 63;
+            const int64_t k = k0 + kk;
+            float e = 0.f, a = 0.f;
+            if (k < K) {
+                const float ck = c[k / t.T];
+                if (m0 + col < t.d_out) e = ck * Elem<DT>::ld(E + k * t.d_out + m0 + col);
+                if (n0 + col < t.d_in) a = Elem<DT>::ld(A + k * t.d_in + n0 + col);
+            }
+            Es[kk][col] = e;
+            As[kk][col] = a;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < kBK; ++kk) {
+            float ev[4], av[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ev[i] = Es[kk][tr * 4 + i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) av[j] = As[kk][tc * 4 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(ev[i], av[j], acc[i][j]);
+        }
+        if (do_bias && tid < kBM) {
+            for (int kk = 0; kk < kBK; ++kk) bsum += Es[kk][tid];
+        }
+        __syncthreads();
+    }
+    const float scale = sc.sigma * sc.C;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t m = m0 + tr * 4 + i;
+        if (m >= t.d_out) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t n = n0 + tc * 4 + j;
+            if (n >= t.d_in) continue;
+            const int64_t p = m * t.d_in + n;
+            const float z = noise_at(sc.seed, sc.step, (uint64_t)(t.coord_off + p));
+            t.G[p] = (acc[i][j] + scale * z) / sc.L;
+        }
+    }
+    if (do_bias && tid < kBM && m0 + tid < t.d_out) {
+        const int64_t p = t.d_out * t.d_in + m0 + tid;
+        const float z = noise_at(sc.seed, sc.step, (uint64_t)(t.coord_off + p));
+        t.G[p] = (bsum + scale * z) / sc.L;
+    }
+}
+
+// ------------------------------------------------------- noise test hook
+__global__ void k_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int64_t n,
+                                 uint32_t* __restrict__ raw, float* __restrict__ z) {
+    const int64_t jb = (int64_t)(k0 >> 2);
+    const int64_t nblocks = (int64_t)((k0 + n - 1) >> 2) - jb + 1;
+    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblocks;
+         b += (int64_t)gridDim.x * blockDim.x) {
+        const uint64_t j = (uint64_t)(jb + b);
+        const uint4 w = noise_block(seed, step, j);
+        if (raw) {
+            raw[4 * b + 0] = w.x;
+            raw[4 * b + 1] = w.y;
+            raw[4 * b + 2] = w.z;
+            raw[4 * b + 3] = w.w;
+        }
+        if (z) {
+            const float2 p0 = box_muller(w.x, w.y);
+            const float2 p1 = box_muller(w.z, w.w);
+            const float v[4] = {p0.x, p0.y, p1.x, p1.y};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int64_t k = (int64_t)(4 * j + q) - (int64_t)k0;
+                if (k >= 0 && k < n) z[k] = v[q];
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_clip(const ClipParams& p, float* n2, float* c, float* n2_user, float* c_user,
+                        unsigned* status, cudaStream_t s) {
+    const int threads = 256;
+    const int64_t blocks = (p.B * 32 + threads - 1) / threads;
+    k_clip<<<(unsigned)blocks, threads, 0, s>>>(p, n2, c, n2_user, c_user, status);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_grad_wsum(const GradTask* tasks, int n, const float* c, const unsigned* status,
+                             const StepScalars& sc, cudaStream_t s) {
+    for (int base = 0; base < n; base += kMaxGroup) {
+        WsumParams P;
+        P.n = n - base < kMaxGroup ? n - base : kMaxGroup;
+        int64_t maxblk = 1;
+        for (int i = 0; i < P.n; ++i) {
+            P.t[i] = tasks[base + i];
+            const GradTask& t = P.t[i];
+            const int64_t ncl = t.d_out * t.d_in + (t.has_bias ? t.d_out : 0);
+            const int64_t nb = ((t.coord_off + ncl - 1) >> 2) - (t.coord_off >> 2) + 1;
+            maxblk = nb > maxblk ? nb : maxblk;
+        }
+        int64_t gx = (maxblk + 255) / 256;
+        if (gx > 4096) gx = 4096;
+        k_grad_wsum<<<dim3((unsigned)gx, (unsigned)P.n), 256, 0, s>>>(P, c, status, sc);
+        count_launches(1);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_grad_gemm_cc(const GradTask& t, const float* c, const unsigned* status,
+                                const StepScalars& sc, cudaStream_t s) {
+    const dim3 grid((unsigned)((t.d_in + kBN - 1) / kBN), (unsigned)((t.d_out + kBM - 1) / kBM));
+    if (t.dtype == DT_F32) k_grad_gemm_cc<DT_F32><<<grid, 256, 0, s>>>(t, c, status, sc);
+    else k_grad_gemm_cc<DT_BF16><<<grid, 256, 0, s>>>(t, c, status, sc);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int64_t n,
+                                  uint32_t* raw, float* z, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const int64_t nblocks = (int64_t)((k0 + n - 1) >> 2) - (int64_t)(k0 >> 2) + 1;
+    int64_t grid = (nblocks + 255) / 256;
+    if (grid > 152 * 64) grid = 152 * 64;
+    k_philox_normals<<<(unsigned)grid, 256, 0, s>>>(seed, step, k0, n, raw, z);
+    count_launches(1);
+    return cudaGetLastError();
+}

@@ -1,0 +1,92 @@
+// Internal interface between the host runtime (runtime.cu) and the kernel
+// translation units.  Nothing here is part of the public C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+enum { DT_F32 = 0, DT_BF16 = 1 };
+
+// Largest number of registered layers a context accepts (the clip kernel
+// receives every layer's partial table as a kernel parameter).
+constexpr int kMaxLayers = 512;
+// Largest number of layers one grouped launch carries in its parameters.
+constexpr int kMaxGroup = 64;
+
+// Norm kernels.
+enum NormKernel {
+    NK_T1 = 0,        // ghost, T == 1: ||a||^2 ||e||^2 (+ ||e||^2)
+    NK_GHOST_CC = 1,  // ghost, CUDA-core tiled Gram
+    NK_MAT_CC = 2,    // materialize, CUDA-core tiled E^T A
+    NK_GHOST_TC = 3,  // ghost, tcgen05 Gram
+    NK_MAT_TC = 4,    // materialize, tcgen05 skinny E^T A
+};
+
+// Gradient kernels.
+enum GradKernel {
+    GK_WSUM = 0,      // from stored per-example gradients
+    GK_GEMM_CC = 1,   // CUDA-core reweighted E^T diag(c) A
+    GK_GEMM_TC = 2,   // tcgen05 reweighted E^T diag(c) A
+};
+
+// One layer's per-example norm work for one step.
+struct NormTask {
+    const void* A;      // [B, T, d_in]
+    const void* E;      // [B, T, d_out]
+    int64_t T, d_in, d_out;
+    int has_bias;
+    int dtype;
+    float* partial;     // [B][nslots] fp32 partial squared norms
+    int nslots;
+    float* gstore;      // [B][ncoords] per-example gradients, or nullptr
+};
+
+// One layer's gradient work.
+struct GradTask {
+    const void* A;
+    const void* E;
+    int64_t T, d_in, d_out;
+    int has_bias;
+    int dtype;
+    const float* gstore;   // stored per-example gradients (GK_WSUM)
+    float* G;              // output, d_out*d_in (+ d_out)
+    int64_t coord_off;     // first noise coordinate of the layer
+};
+
+struct StepScalars {
+    int64_t B;
+    float C;
+    float sigma;
+    float L;
+    uint64_t seed;
+    uint64_t step;
+};
+
+struct ClipParams {
+    int nlayers;
+    int64_t B;
+    float C;
+    const float* partial[kMaxLayers];
+    int nslots[kMaxLayers];
+};
+
+// ---- every kernel launch of the library is counted here (dp_kernel_launches)
+void count_launches(int n);
+
+// ---- slot counts (depend on the shapes only, never on B)
+int nslots_for(int kernel, int64_t T, int64_t d_in, int64_t d_out);
+int nslots_cc(int kernel, int64_t T, int64_t d_in, int64_t d_out);
+
+// ---- launchers; each returns the cudaGetLastError() of its launches
+cudaError_t launch_norm_t1(const NormTask& t, int64_t B, cudaStream_t s);
+cudaError_t launch_norm_ghost_cc(const NormTask& t, int64_t B, cudaStream_t s);
+cudaError_t launch_norm_mat_cc(const NormTask& t, int64_t B, cudaStream_t s);
+cudaError_t launch_layer_sqnorm(const float* partial, int nslots, int64_t B, float* out, cudaStream_t s);
+cudaError_t launch_clip(const ClipParams& p, float* n2, float* c, float* n2_user, float* c_user,
+                        unsigned* status, cudaStream_t s);
+cudaError_t launch_grad_wsum(const GradTask* tasks, int n, const float* c, const unsigned* status,
+                             const StepScalars& sc, cudaStream_t s);
+cudaError_t launch_grad_gemm_cc(const GradTask& t, const float* c, const unsigned* status,
+                                const StepScalars& sc, cudaStream_t s);
+cudaError_t launch_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int64_t n,
+                                  uint32_t* raw, float* z, cudaStream_t s);

@@ -1,0 +1,491 @@
+// Host runtime behind the C ABI of include/dp_clip.h: the context, the layer
+// registry and coordinate layout, the ghost / materialize chooser, the step
+// state machine, context-owned device scratch and kernel planning.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/dp_clip.h"
+#include "internal.h"
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+
+// Per-example gradients of a materialized layer are kept for the weighted sum
+// when they take at most this many bytes; otherwise the clipped sum re-reads
+// A and E.
+constexpr uint64_t kStoreBudgetBytes = 8ull << 30;
+
+enum Phase { IDLE = 0, OPEN = 1, CLIPPED = 2 };
+
+struct Layer {
+    int64_t d_in = 0, d_out = 0;
+    int has_bias = 0;
+    int dtype = DT_F32;
+    int64_t coord_off = 0, ncoords = 0;
+    // per step
+    bool accumulated = false;
+    int path = DP_PATH_GHOST;
+    int norm_kernel = NK_T1;
+    int grad_kernel = GK_GEMM_CC;
+    const void* A = nullptr;
+    const void* E = nullptr;
+    int64_t T = 0;
+    int nslots = 0;
+    bool stored = false;
+    // context-owned device buffers
+    float* partial = nullptr;
+    size_t partial_cap = 0;   // floats
+    float* gstore = nullptr;
+    size_t gstore_cap = 0;    // floats
+};
+
+}  // namespace
+
+struct dp_ctx {
+    int device = 0;
+    cudaStream_t stream = nullptr;
+    int sm_count = 0;
+    std::vector<Layer> layers;
+    int64_t P = 0;
+    Phase phase = IDLE;
+    int64_t B = 0;
+    double L = 1.0;
+    float C = 1.0f;
+    float* n2 = nullptr;
+    float* c = nullptr;
+    size_t bcap = 0;
+    size_t ccap = 0;
+    unsigned* status = nullptr;
+    std::string err;
+};
+
+namespace {
+
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) cudaSetDevice(dev);
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+dp_status fail(dp_ctx* ctx, dp_status s, const char* fmt, ...) {
+    if (ctx) {
+        char buf[512];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof buf, fmt, ap);
+        va_end(ap);
+        ctx->err = buf;
+    }
+    return s;
+}
+
+dp_status cuda_fail(dp_ctx* ctx, cudaError_t e, const char* what) {
+    return fail(ctx, DP_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Grow a context-owned float buffer to at least n floats.  Synchronizes the
+// stream before releasing the old buffer, which only happens when a step
+// needs more room than any earlier one.
+dp_status grow(dp_ctx* ctx, float** buf, size_t* cap, size_t n) {
+    if (n <= *cap && *buf) return DP_OK;
+    cudaError_t e;
+    if (*buf) {
+        e = cudaStreamSynchronize(ctx->stream);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamSynchronize");
+        cudaFree(*buf);
+        *buf = nullptr;
+        *cap = 0;
+    }
+    const size_t want = std::max<size_t>(n, 64);
+    e = cudaMalloc(reinterpret_cast<void**>(buf), want * sizeof(float));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *buf = nullptr;
+        return fail(ctx, DP_ERR_OOM, "cudaMalloc of %zu bytes failed: %s", want * sizeof(float),
+                    cudaGetErrorString(e));
+    }
+    *cap = want;
+    return DP_OK;
+}
+
+int choose(int64_t T, int64_t d_in, int64_t d_out) {
+    // exact T^2 < d_in * d_out on unsigned 128-bit products
+    const unsigned __int128 t2 = (unsigned __int128)(uint64_t)T * (uint64_t)T;
+    const unsigned __int128 dd = (unsigned __int128)(uint64_t)d_in * (uint64_t)d_out;
+    return t2 < dd ? DP_PATH_GHOST : DP_PATH_MATERIALIZE;
+}
+
+// Kernel choice depends on the shapes and dtype only, never on B, so that a
+// record's norm does not depend on the batch it is in.
+void plan_norm(Layer& ly, int64_t T) {
+    ly.path = choose(T, ly.d_in, ly.d_out);
+    if (ly.path == DP_PATH_GHOST) {
+        ly.norm_kernel = (T == 1) ? NK_T1 : NK_GHOST_CC;
+    } else {
+        ly.norm_kernel = NK_MAT_CC;
+    }
+    ly.nslots = nslots_for(ly.norm_kernel, T, ly.d_in, ly.d_out);
+}
+
+dp_status launch_norm(dp_ctx* ctx, Layer& ly) {
+    NormTask t;
+    t.A = ly.A;
+    t.E = ly.E;
+    t.T = ly.T;
+    t.d_in = ly.d_in;
+    t.d_out = ly.d_out;
+    t.has_bias = ly.has_bias;
+    t.dtype = ly.dtype;
+    t.partial = ly.partial;
+    t.nslots = ly.nslots;
+    t.gstore = ly.stored ? ly.gstore : nullptr;
+    cudaError_t e = cudaSuccess;
+    switch (ly.norm_kernel) {
+        case NK_T1: e = launch_norm_t1(t, ctx->B, ctx->stream); break;
+        case NK_GHOST_CC: e = launch_norm_ghost_cc(t, ctx->B, ctx->stream); break;
+        case NK_MAT_CC: e = launch_norm_mat_cc(t, ctx->B, ctx->stream); break;
+        default: return fail(ctx, DP_ERR_UNSUPPORTED, "no norm kernel %d", ly.norm_kernel);
+    }
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "norm kernel launch");
+    return DP_OK;
+}
+
+// Validate one accumulate request without changing any state.
+dp_status check_accumulate(dp_ctx* ctx, int id, const void* A, const void* E, int64_t T) {
+    if (ctx->phase != OPEN)
+        return fail(ctx, DP_ERR_STATE, "dp_norm_accumulate needs an open step before dp_clip_factors");
+    if (id < 0 || id >= (int)ctx->layers.size()) return fail(ctx, DP_ERR_INVALID_ARG, "unknown layer id %d", id);
+    if (ctx->layers[id].accumulated)
+        return fail(ctx, DP_ERR_STATE, "layer %d was already accumulated in this step", id);
+    if (T < 1) return fail(ctx, DP_ERR_SHAPE, "T must be >= 1 (got %lld)", (long long)T);
+    if (!A || !E) return fail(ctx, DP_ERR_INVALID_ARG, "A and E must not be NULL");
+    if (!aligned16(A) || !aligned16(E)) return fail(ctx, DP_ERR_INVALID_ARG, "A and E must be 16-byte aligned");
+    const Layer& ly = ctx->layers[id];
+    const unsigned __int128 rows = (unsigned __int128)(uint64_t)ctx->B * (uint64_t)T;
+    if (rows * (uint64_t)std::max(ly.d_in, ly.d_out) >= ((unsigned __int128)1 << 62))
+        return fail(ctx, DP_ERR_SHAPE, "B*T*d overflows");
+    return DP_OK;
+}
+
+// Record the request, size the layer's scratch and launch its norm kernel.
+dp_status do_accumulate(dp_ctx* ctx, int id, const void* A, const void* E, int64_t T, float* sq) {
+    Layer& ly = ctx->layers[id];
+    Layer plan = ly;
+    plan.A = A;
+    plan.E = E;
+    plan.T = T;
+    plan_norm(plan, T);
+    if (plan.nslots <= 0) return fail(ctx, DP_ERR_UNSUPPORTED, "no norm plan for layer %d", id);
+    dp_status st = grow(ctx, &ly.partial, &ly.partial_cap, (size_t)ctx->B * plan.nslots);
+    if (st != DP_OK) return st;
+    plan.partial = ly.partial;
+    plan.partial_cap = ly.partial_cap;
+    plan.stored = false;
+    if (plan.path == DP_PATH_MATERIALIZE &&
+        (uint64_t)ctx->B * (uint64_t)ly.ncoords * 4u <= kStoreBudgetBytes) {
+        st = grow(ctx, &ly.gstore, &ly.gstore_cap, (size_t)ctx->B * ly.ncoords);
+        if (st != DP_OK) return st;
+        plan.gstore = ly.gstore;
+        plan.gstore_cap = ly.gstore_cap;
+        plan.stored = true;
+    }
+    plan.grad_kernel = plan.stored ? GK_WSUM : GK_GEMM_CC;
+    st = launch_norm(ctx, plan);
+    if (st != DP_OK) return st;
+    if (sq) {
+        const cudaError_t e = launch_layer_sqnorm(plan.partial, plan.nslots, ctx->B, sq, ctx->stream);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "layer norm launch");
+    }
+    plan.accumulated = true;
+    ly = plan;
+    return DP_OK;
+}
+
+}  // namespace
+
+static std::atomic<int64_t> g_launches{0};
+
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+int nslots_for(int kernel, int64_t T, int64_t d_in, int64_t d_out) {
+    return nslots_cc(kernel, T, d_in, d_out);
+}
+
+extern "C" {
+
+int dp_version(void) { return kVersion; }
+
+int64_t dp_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* dp_status_string(dp_status s) {
+    switch (s) {
+        case DP_OK: return "ok";
+        case DP_ERR_INVALID_ARG: return "invalid argument";
+        case DP_ERR_SHAPE: return "invalid shape";
+        case DP_ERR_STATE: return "call out of order";
+        case DP_ERR_NONFINITE: return "non-finite per-example norm";
+        case DP_ERR_CUDA: return "CUDA error";
+        case DP_ERR_OOM: return "out of device memory";
+        case DP_ERR_UNSUPPORTED: return "unsupported";
+    }
+    return "unknown status";
+}
+
+int dp_choose_path(int64_t T, int64_t d_in, int64_t d_out) {
+    if (T < 1 || d_in < 1 || d_out < 1) return -1;
+    return choose(T, d_in, d_out);
+}
+
+dp_status dp_create(dp_ctx** out, int device, void* cuda_stream) {
+    if (!out) return DP_ERR_INVALID_ARG;
+    *out = nullptr;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+        cudaGetLastError();
+        return DP_ERR_CUDA;
+    }
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return DP_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return DP_ERR_UNSUPPORTED;
+    dp_ctx* ctx = new (std::nothrow) dp_ctx();
+    if (!ctx) return DP_ERR_OOM;
+    ctx->device = device;
+    ctx->stream = static_cast<cudaStream_t>(cuda_stream);
+    ctx->sm_count = prop.multiProcessorCount;
+    DeviceGuard g(device);
+    if (cudaMalloc(reinterpret_cast<void**>(&ctx->status), sizeof(unsigned)) != cudaSuccess) {
+        cudaGetLastError();
+        delete ctx;
+        return DP_ERR_OOM;
+    }
+    if (cudaMemsetAsync(ctx->status, 0, sizeof(unsigned), ctx->stream) != cudaSuccess) {
+        cudaFree(ctx->status);
+        delete ctx;
+        return DP_ERR_CUDA;
+    }
+    *out = ctx;
+    return DP_OK;
+}
+
+dp_status dp_destroy(dp_ctx* ctx) {
+    if (!ctx) return DP_OK;
+    DeviceGuard g(ctx->device);
+    cudaStreamSynchronize(ctx->stream);
+    for (Layer& ly : ctx->layers) {
+        cudaFree(ly.partial);
+        cudaFree(ly.gstore);
+    }
+    cudaFree(ctx->n2);
+    cudaFree(ctx->c);
+    cudaFree(ctx->status);
+    delete ctx;
+    return DP_OK;
+}
+
+dp_status dp_register_layer(dp_ctx* ctx, int64_t d_in, int64_t d_out, int has_bias, dp_dtype dtype,
+                            int* layer_id) {
+    if (!ctx || !layer_id) return fail(ctx, DP_ERR_INVALID_ARG, "NULL argument");
+    if (ctx->phase != IDLE) return fail(ctx, DP_ERR_STATE, "layers are registered between steps only");
+    if (d_in < 1 || d_out < 1) return fail(ctx, DP_ERR_SHAPE, "d_in and d_out must be >= 1");
+    if (dtype != DP_F32 && dtype != DP_BF16) return fail(ctx, DP_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if ((int)ctx->layers.size() >= kMaxLayers) return fail(ctx, DP_ERR_UNSUPPORTED, "at most %d layers", kMaxLayers);
+    const unsigned __int128 nc = (unsigned __int128)(uint64_t)d_out * (uint64_t)d_in + (has_bias ? (uint64_t)d_out : 0);
+    if (nc + (uint64_t)ctx->P >= ((unsigned __int128)1 << 62)) return fail(ctx, DP_ERR_SHAPE, "too many coordinates");
+    Layer ly;
+    ly.d_in = d_in;
+    ly.d_out = d_out;
+    ly.has_bias = has_bias ? 1 : 0;
+    ly.dtype = dtype == DP_F32 ? DT_F32 : DT_BF16;
+    ly.coord_off = ctx->P;
+    ly.ncoords = (int64_t)nc;
+    ctx->P += ly.ncoords;
+    ctx->layers.push_back(ly);
+    *layer_id = (int)ctx->layers.size() - 1;
+    return DP_OK;
+}
+
+dp_status dp_layer_info(const dp_ctx* ctx, int layer_id, int64_t* coord_offset, int64_t* ncoords) {
+    if (!ctx) return DP_ERR_INVALID_ARG;
+    if (layer_id < 0 || layer_id >= (int)ctx->layers.size()) return DP_ERR_INVALID_ARG;
+    if (coord_offset) *coord_offset = ctx->layers[layer_id].coord_off;
+    if (ncoords) *ncoords = ctx->layers[layer_id].ncoords;
+    return DP_OK;
+}
+
+int64_t dp_num_coords(const dp_ctx* ctx) { return ctx ? ctx->P : 0; }
+
+dp_status dp_begin_step(dp_ctx* ctx, int64_t B) {
+    if (!ctx) return DP_ERR_INVALID_ARG;
+    if (B < 1) return fail(ctx, DP_ERR_SHAPE, "B must be >= 1");
+    if (ctx->layers.empty()) return fail(ctx, DP_ERR_STATE, "no layer registered");
+    DeviceGuard g(ctx->device);
+    dp_status st = grow(ctx, &ctx->n2, &ctx->bcap, (size_t)B);
+    if (st != DP_OK) return st;
+    st = grow(ctx, &ctx->c, &ctx->ccap, (size_t)B);
+    if (st != DP_OK) return st;
+    const cudaError_t e = cudaMemsetAsync(ctx->status, 0, sizeof(unsigned), ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMemsetAsync");
+    for (Layer& ly : ctx->layers) {
+        ly.accumulated = false;
+        ly.A = ly.E = nullptr;
+        ly.T = 0;
+    }
+    ctx->B = B;
+    ctx->L = (double)B;
+    ctx->phase = OPEN;
+    ctx->err.clear();
+    return DP_OK;
+}
+
+dp_status dp_set_normalizer(dp_ctx* ctx, double L) {
+    if (!ctx) return DP_ERR_INVALID_ARG;
+    if (ctx->phase == IDLE) return fail(ctx, DP_ERR_STATE, "dp_set_normalizer needs an open step");
+    if (!std::isfinite(L) || L <= 0.0 || !std::isfinite((float)L))
+        return fail(ctx, DP_ERR_INVALID_ARG, "normalizer L must be finite and > 0");
+    ctx->L = L;
+    return DP_OK;
+}
+
+dp_status dp_norm_accumulate(dp_ctx* ctx, int layer_id, const void* A, const void* E, int64_t T,
+                             float* sqnorm_out) {
+    if (!ctx) return DP_ERR_INVALID_ARG;
+    dp_status st = check_accumulate(ctx, layer_id, A, E, T);
+    if (st != DP_OK) return st;
+    if (sqnorm_out && !aligned16(sqnorm_out) && (reinterpret_cast<uintptr_t>(sqnorm_out) & 3u))
+        return fail(ctx, DP_ERR_INVALID_ARG, "sqnorm_out must be 4-byte aligned");
+    DeviceGuard g(ctx->device);
+    return do_accumulate(ctx, layer_id, A, E, T, sqnorm_out);
+}
+
+dp_status dp_norm_accumulate_batch(dp_ctx* ctx, int n, const int* layer_ids, const void* const* A,
+                                   const void* const* E, const int64_t* T, float* const* sqnorm_out) {
+    if (!ctx) return DP_ERR_INVALID_ARG;
+    if (n < 0 || (n > 0 && (!layer_ids || !A || !E || !T))) return fail(ctx, DP_ERR_INVALID_ARG, "bad batch arrays");
+    for (int i = 0; i < n; ++i) {
+        dp_status st = check_accumulate(ctx, layer_ids[i], A[i], E[i], T[i]);
+        if (st != DP_OK) return st;
+        for (int j = 0; j < i; ++j)
+            if (layer_ids[j] == layer_ids[i])
+                return fail(ctx, DP_ERR_STATE, "layer %d appears twice in one batch", layer_ids[i]);
+    }
+    DeviceGuard g(ctx->device);
+    for (int i = 0; i < n; ++i) {
+        dp_status st = do_accumulate(ctx, layer_ids[i], A[i], E[i], T[i], sqnorm_out ? sqnorm_out[i] : nullptr);
+        if (st != DP_OK) return st;
+    }
+    return DP_OK;
+}
+
+dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnorm_out) {
+    if (!ctx) return DP_ERR_INVALID_ARG;
+    if (ctx->phase != OPEN) return fail(ctx, DP_ERR_STATE, "dp_clip_factors needs an open, unclipped step");
+    if (!std::isfinite(C) || !(C > 0.0f)) return fail(ctx, DP_ERR_INVALID_ARG, "clip bound C must be finite and > 0");
+    for (size_t l = 0; l < ctx->layers.size(); ++l)
+        if (!ctx->layers[l].accumulated)
+            return fail(ctx, DP_ERR_STATE, "layer %zu was not accumulated in this step", l);
+    DeviceGuard g(ctx->device);
+    ClipParams* p = new (std::nothrow) ClipParams();
+    if (!p) return fail(ctx, DP_ERR_OOM, "host allocation failed");
+    p->nlayers = (int)ctx->layers.size();
+    p->B = ctx->B;
+    p->C = C;
+    for (int l = 0; l < p->nlayers; ++l) {
+        p->partial[l] = ctx->layers[l].partial;
+        p->nslots[l] = ctx->layers[l].nslots;
+    }
+    const cudaError_t e = launch_clip(*p, ctx->n2, ctx->c, total_sqnorm_out, c_out, ctx->status, ctx->stream);
+    delete p;
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "clip kernel launch");
+    ctx->C = C;
+    ctx->phase = CLIPPED;
+    return DP_OK;
+}
+
+dp_status dp_clipped_noisy_grad(dp_ctx* ctx, float sigma, uint64_t seed, uint64_t step, float* const* G) {
+    if (!ctx) return DP_ERR_INVALID_ARG;
+    if (ctx->phase != CLIPPED) return fail(ctx, DP_ERR_STATE, "dp_clipped_noisy_grad needs dp_clip_factors first");
+    if (!std::isfinite(sigma) || sigma < 0.0f) return fail(ctx, DP_ERR_INVALID_ARG, "sigma must be finite and >= 0");
+    if (!G) return fail(ctx, DP_ERR_INVALID_ARG, "G must not be NULL");
+    for (size_t l = 0; l < ctx->layers.size(); ++l)
+        if (!G[l] || !aligned16(G[l])) return fail(ctx, DP_ERR_INVALID_ARG, "G[%zu] is NULL or not 16-byte aligned", l);
+    DeviceGuard g(ctx->device);
+    StepScalars sc;
+    sc.B = ctx->B;
+    sc.C = ctx->C;
+    sc.sigma = sigma;
+    sc.L = (float)ctx->L;
+    sc.seed = seed;
+    sc.step = step;
+    std::vector<GradTask> wsum;
+    for (size_t l = 0; l < ctx->layers.size(); ++l) {
+        const Layer& ly = ctx->layers[l];
+        GradTask t;
+        t.A = ly.A;
+        t.E = ly.E;
+        t.T = ly.T;
+        t.d_in = ly.d_in;
+        t.d_out = ly.d_out;
+        t.has_bias = ly.has_bias;
+        t.dtype = ly.dtype;
+        t.gstore = ly.gstore;
+        t.G = G[l];
+        t.coord_off = ly.coord_off;
+        if (ly.grad_kernel == GK_WSUM) {
+            wsum.push_back(t);
+            continue;
+        }
+        const cudaError_t e = launch_grad_gemm_cc(t, ctx->c, ctx->status, sc, ctx->stream);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "clipped-sum kernel launch");
+    }
+    if (!wsum.empty()) {
+        const cudaError_t e = launch_grad_wsum(wsum.data(), (int)wsum.size(), ctx->c, ctx->status, sc, ctx->stream);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "weighted-sum kernel launch");
+    }
+    ctx->phase = IDLE;
+    return DP_OK;
+}
+
+dp_status dp_step_status(dp_ctx* ctx) {
+    if (!ctx) return DP_ERR_INVALID_ARG;
+    DeviceGuard g(ctx->device);
+    cudaError_t e = cudaStreamSynchronize(ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamSynchronize");
+    unsigned word = 0;
+    e = cudaMemcpy(&word, ctx->status, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "status read");
+    if (word & 1u) return fail(ctx, DP_ERR_NONFINITE, "a per-example gradient norm was not finite");
+    return DP_OK;
+}
+
+const char* dp_last_error(const dp_ctx* ctx) { return ctx ? ctx->err.c_str() : ""; }
+
+dp_status dp_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int64_t n, uint32_t* raw_out,
+                            float* z_out, void* stream) {
+    if (n < 0) return DP_ERR_SHAPE;
+    if (n == 0) return DP_OK;
+    if ((raw_out && (reinterpret_cast<uintptr_t>(raw_out) & 3u)) || (z_out && (reinterpret_cast<uintptr_t>(z_out) & 3u)))
+        return DP_ERR_INVALID_ARG;
+    if (k0 + (uint64_t)n < k0) return DP_ERR_SHAPE;
+    const cudaError_t e = launch_philox_normals(seed, step, k0, n, raw_out, z_out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DP_OK : DP_ERR_CUDA;
+}
+
+}  // extern "C"
