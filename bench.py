@@ -103,9 +103,21 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
-    def stop(self):
+    def wait_samples(self, n: int, timeout_s: float = 3.0):
+        t0 = time.time()
+        while self.proc is not None and len(self.lines) < n and time.time() - t0 < timeout_s:
+            time.sleep(0.02)
+
+    def mark(self) -> int:
+        """Index of the last sample taken before the timed region starts."""
+        self.wait_samples(1)
+        return max(0, len(self.lines) - 1)
+
+    def stop(self, since: int = 0):
+        """Stop after one more sample arrives; summarise samples from `since` on."""
         if self.proc is None:
             return None
+        self.wait_samples(len(self.lines) + 1, 1.0)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -114,7 +126,7 @@ class ClockSampler:
         self.t.join(timeout=5)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in self.lines[since:]:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -253,15 +265,36 @@ def run_ours(args, w):
     dp.load_library()
 
     layers = [(ly.d_in, ly.d_out, ly.has_bias) for ly in w.layers]
+    # all inputs in one device arena (256-byte aligned segments), so that the
+    # end-to-end leg moves them with one host->device copy per step
+    esz = 4 if w.dtype == "f32" else 2
+    seg = lambda n: (n * esz + 255) // 256 * 256  # noqa: E731
+    sizes = []
+    for ly in w.layers:
+        sizes += [w.B * ly.T * ly.d_in, w.B * ly.T * ly.d_out]
+    arena = torch.empty(sum(seg(n) for n in sizes), dtype=torch.uint8, device=device)
+    views, off = [], 0
+    for n in sizes:
+        views.append(arena[off:off + n * esz].view(w.torch_dtype))
+        off += seg(n)
     A_dev, E_dev = [], []
-    for i in range(len(w.layers)):
+    for i, ly in enumerate(w.layers):
         a, e = generate_layer(w, i, device)
-        A_dev.append(a)
-        E_dev.append(e)
+        A_dev.append(views[2 * i].view(a.shape))
+        E_dev.append(views[2 * i + 1].view(e.shape))
+        A_dev[-1].copy_(a)
+        E_dev[-1].copy_(e)
+        del a, e
     T_list = [ly.T for ly in w.layers]
     stream = torch.cuda.current_stream(device)
     pg = dp.PrivateGradient(layers, dtype=w.torch_dtype, device=local, stream=stream)
-    grads, clip, sq = pg.alloc_outputs(w.B)
+    _, clip, sq = pg.alloc_outputs(w.B)
+    gsizes = [(n + 63) // 64 * 64 for (_, _, _, _, n) in pg.layers]
+    garena = torch.empty(sum(gsizes), dtype=torch.float32, device=device)
+    grads, off = [], 0
+    for (_, _, _, _, n), gs in zip(pg.layers, gsizes):
+        grads.append(garena[off:off + n])
+        off += gs
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     ctx = pg.ctx
     ids = list(range(len(layers)))
@@ -280,6 +313,8 @@ def run_ours(args, w):
         if evs:
             evs[3].record(stream)
 
+    clocks = ClockSampler(local)
+    clocks.start()
     for _ in range(max(3, args.warmup)):
         flush.zero_()
         step()
@@ -290,8 +325,7 @@ def run_ours(args, w):
 
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    clocks = ClockSampler(local)
-    clocks.start()
+    since = clocks.mark()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -303,7 +337,7 @@ def run_ours(args, w):
     n_launch = dp.dp_kernel_launches() - n_launch0
     if world > 1:
         torch.distributed.barrier()
-    clk = clocks.stop()
+    clk = clocks.stop(since)
     st = dp.dp_step_status(ctx)
     if st != dp.DP_OK:
         raise dp.DPError(st, "dp_step_status", dp.dp_last_error(ctx))
@@ -346,20 +380,15 @@ def run_ours(args, w):
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        A_pin = [a.cpu().pin_memory() for a in A_dev]
-        E_pin = [e.cpu().pin_memory() for e in E_dev]
-        G_pin = [torch.empty(g.numel(), dtype=torch.float32).pin_memory() for g in grads]
-        h2d = sum(a.numel() * a.element_size() for a in A_pin) + sum(e.numel() * e.element_size() for e in E_pin)
-        d2h = sum(g.numel() * 4 for g in G_pin)
+        arena_pin = arena.cpu().pin_memory()
+        garena_pin = torch.empty(garena.numel(), dtype=torch.float32).pin_memory()
+        h2d = arena.numel()
+        d2h = garena.numel() * 4
 
         def e2e_step():
-            for a_d, a_h in zip(A_dev, A_pin):
-                a_d.copy_(a_h, non_blocking=True)
-            for e_d, e_h in zip(E_dev, E_pin):
-                e_d.copy_(e_h, non_blocking=True)
+            arena.copy_(arena_pin, non_blocking=True)
             step()
-            for g_h, g_d in zip(G_pin, grads):
-                g_h.copy_(g_d, non_blocking=True)
+            garena_pin.copy_(garena, non_blocking=True)
 
         for _ in range(2):
             e2e_step()

@@ -155,6 +155,24 @@ __global__ void __launch_bounds__(256) k_grad_gemm_cc(const GradTask t, const fl
     }
 }
 
+// --------------------------------------------- bias part of the clipped sum
+// sb[m] = sum_k c[k / T] E[k, m] (ascending k), then G = (sb + sigma C z) / L
+// at the layer's bias coordinates.  Used beside the tensor-core weight sum.
+template <int DT>
+__global__ void __launch_bounds__(256) k_bias_sum(const GradTask t, const float* __restrict__ c,
+                                                  const unsigned* __restrict__ status, StepScalars sc) {
+    using Tt = typename Elem<DT>::T;
+    if (status_bad(status)) return;
+    const int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (m >= t.d_out) return;
+    const Tt* E = (const Tt*)t.E;
+    const int64_t K = sc.B * t.T;
+    float acc = 0.f;
+    for (int64_t k = 0; k < K; ++k) acc = fmaf(c[k / t.T], Elem<DT>::ld(E + k * t.d_out + m), acc);
+    const int64_t p = t.d_out * t.d_in + m;
+    t.G[p] = (acc + sc.sigma * sc.C * noise_at(sc.seed, sc.step, (uint64_t)(t.coord_off + p))) / sc.L;
+}
+
 // ------------------------------------------------------- noise test hook
 __global__ void k_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int64_t n,
                                  uint32_t* __restrict__ raw, float* __restrict__ z) {
@@ -222,6 +240,15 @@ cudaError_t launch_grad_gemm_cc(const GradTask& t, const float* c, const unsigne
     const dim3 grid((unsigned)((t.d_in + kBN - 1) / kBN), (unsigned)((t.d_out + kBM - 1) / kBM));
     if (t.dtype == DT_F32) k_grad_gemm_cc<DT_F32><<<grid, 256, 0, s>>>(t, c, status, sc);
     else k_grad_gemm_cc<DT_BF16><<<grid, 256, 0, s>>>(t, c, status, sc);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bias_sum(const GradTask& t, const float* c, const unsigned* status, const StepScalars& sc,
+                            cudaStream_t s) {
+    const unsigned grid = (unsigned)((t.d_out + 255) / 256);
+    if (t.dtype == DT_F32) k_bias_sum<DT_F32><<<grid, 256, 0, s>>>(t, c, status, sc);
+    else k_bias_sum<DT_BF16><<<grid, 256, 0, s>>>(t, c, status, sc);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -12,6 +12,9 @@ enum { DT_F32 = 0, DT_BF16 = 1 };
 constexpr int kMaxLayers = 512;
 // Largest number of layers one grouped launch carries in its parameters.
 constexpr int kMaxGroup = 64;
+// Largest number of layers one skinny-materialize launch carries (each
+// brings two 128-byte TMA descriptors in the kernel parameters).
+constexpr int kMaxSkinnyGroup = 48;
 
 // Norm kernels.
 enum NormKernel {
@@ -90,3 +93,13 @@ cudaError_t launch_grad_gemm_cc(const GradTask& t, const float* c, const unsigne
                                 const StepScalars& sc, cudaStream_t s);
 cudaError_t launch_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int64_t n,
                                   uint32_t* raw, float* z, cudaStream_t s);
+cudaError_t launch_bias_sum(const GradTask& t, const float* c, const unsigned* status,
+                            const StepScalars& sc, cudaStream_t s);
+
+// ---- tcgen05 kernels (tc_gemm.cu)
+bool tc_sum_supported(int dtype, int64_t d_in, int64_t d_out, int has_bias);
+bool tc_skinny_supported(int dtype, int64_t d_in, int64_t d_out, int has_bias);
+int nslots_skinny(int64_t d_in, int64_t d_out);
+cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* status,
+                                  const StepScalars& sc, cudaStream_t s);
+cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsigned* status, cudaStream_t s);

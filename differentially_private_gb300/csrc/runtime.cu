@@ -140,12 +140,12 @@ void plan_norm(Layer& ly, int64_t T) {
     if (ly.path == DP_PATH_GHOST) {
         ly.norm_kernel = (T == 1) ? NK_T1 : NK_GHOST_CC;
     } else {
-        ly.norm_kernel = NK_MAT_CC;
+        ly.norm_kernel = tc_skinny_supported(ly.dtype, ly.d_in, ly.d_out, ly.has_bias) ? NK_MAT_TC : NK_MAT_CC;
     }
     ly.nslots = nslots_for(ly.norm_kernel, T, ly.d_in, ly.d_out);
 }
 
-dp_status launch_norm(dp_ctx* ctx, Layer& ly) {
+NormTask make_norm_task(const Layer& ly) {
     NormTask t;
     t.A = ly.A;
     t.E = ly.E;
@@ -157,11 +157,17 @@ dp_status launch_norm(dp_ctx* ctx, Layer& ly) {
     t.partial = ly.partial;
     t.nslots = ly.nslots;
     t.gstore = ly.stored ? ly.gstore : nullptr;
+    return t;
+}
+
+dp_status launch_norm(dp_ctx* ctx, const Layer& ly) {
+    const NormTask t = make_norm_task(ly);
     cudaError_t e = cudaSuccess;
     switch (ly.norm_kernel) {
         case NK_T1: e = launch_norm_t1(t, ctx->B, ctx->stream); break;
         case NK_GHOST_CC: e = launch_norm_ghost_cc(t, ctx->B, ctx->stream); break;
         case NK_MAT_CC: e = launch_norm_mat_cc(t, ctx->B, ctx->stream); break;
+        case NK_MAT_TC: e = launch_mat_skinny_tc(&t, 1, ctx->B, ctx->status, ctx->stream); break;
         default: return fail(ctx, DP_ERR_UNSUPPORTED, "no norm kernel %d", ly.norm_kernel);
     }
     if (e != cudaSuccess) return cuda_fail(ctx, e, "norm kernel launch");
@@ -182,13 +188,14 @@ dp_status check_accumulate(dp_ctx* ctx, int id, const void* A, const void* E, in
     const unsigned __int128 rows = (unsigned __int128)(uint64_t)ctx->B * (uint64_t)T;
     if (rows * (uint64_t)std::max(ly.d_in, ly.d_out) >= ((unsigned __int128)1 << 62))
         return fail(ctx, DP_ERR_SHAPE, "B*T*d overflows");
+    if (rows >= ((unsigned __int128)1 << 31)) return fail(ctx, DP_ERR_SHAPE, "B*T must be below 2^31");
     return DP_OK;
 }
 
-// Record the request, size the layer's scratch and launch its norm kernel.
-dp_status do_accumulate(dp_ctx* ctx, int id, const void* A, const void* E, int64_t T, float* sq) {
+// Plan one layer's step work and size its context scratch; no launch.
+dp_status prepare(dp_ctx* ctx, int id, const void* A, const void* E, int64_t T, Layer& plan) {
     Layer& ly = ctx->layers[id];
-    Layer plan = ly;
+    plan = ly;
     plan.A = A;
     plan.E = E;
     plan.T = T;
@@ -207,15 +214,19 @@ dp_status do_accumulate(dp_ctx* ctx, int id, const void* A, const void* E, int64
         plan.gstore_cap = ly.gstore_cap;
         plan.stored = true;
     }
-    plan.grad_kernel = plan.stored ? GK_WSUM : GK_GEMM_CC;
-    st = launch_norm(ctx, plan);
-    if (st != DP_OK) return st;
+    if (plan.stored) plan.grad_kernel = GK_WSUM;
+    else if (tc_sum_supported(plan.dtype, plan.d_in, plan.d_out, plan.has_bias)) plan.grad_kernel = GK_GEMM_TC;
+    else plan.grad_kernel = GK_GEMM_CC;
+    return DP_OK;
+}
+
+dp_status finish(dp_ctx* ctx, int id, Layer& plan, float* sq) {
     if (sq) {
         const cudaError_t e = launch_layer_sqnorm(plan.partial, plan.nslots, ctx->B, sq, ctx->stream);
         if (e != cudaSuccess) return cuda_fail(ctx, e, "layer norm launch");
     }
     plan.accumulated = true;
-    ly = plan;
+    ctx->layers[id] = plan;
     return DP_OK;
 }
 
@@ -226,6 +237,7 @@ static std::atomic<int64_t> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 int nslots_for(int kernel, int64_t T, int64_t d_in, int64_t d_out) {
+    if (kernel == NK_MAT_TC) return nslots_skinny(d_in, d_out);
     return nslots_cc(kernel, T, d_in, d_out);
 }
 
@@ -372,7 +384,12 @@ dp_status dp_norm_accumulate(dp_ctx* ctx, int layer_id, const void* A, const voi
     if (sqnorm_out && !aligned16(sqnorm_out) && (reinterpret_cast<uintptr_t>(sqnorm_out) & 3u))
         return fail(ctx, DP_ERR_INVALID_ARG, "sqnorm_out must be 4-byte aligned");
     DeviceGuard g(ctx->device);
-    return do_accumulate(ctx, layer_id, A, E, T, sqnorm_out);
+    Layer plan;
+    st = prepare(ctx, layer_id, A, E, T, plan);
+    if (st != DP_OK) return st;
+    st = launch_norm(ctx, plan);
+    if (st != DP_OK) return st;
+    return finish(ctx, layer_id, plan, sqnorm_out);
 }
 
 dp_status dp_norm_accumulate_batch(dp_ctx* ctx, int n, const int* layer_ids, const void* const* A,
@@ -387,8 +404,27 @@ dp_status dp_norm_accumulate_batch(dp_ctx* ctx, int n, const int* layer_ids, con
                 return fail(ctx, DP_ERR_STATE, "layer %d appears twice in one batch", layer_ids[i]);
     }
     DeviceGuard g(ctx->device);
+    std::vector<Layer> plans((size_t)n);
     for (int i = 0; i < n; ++i) {
-        dp_status st = do_accumulate(ctx, layer_ids[i], A[i], E[i], T[i], sqnorm_out ? sqnorm_out[i] : nullptr);
+        dp_status st = prepare(ctx, layer_ids[i], A[i], E[i], T[i], plans[i]);
+        if (st != DP_OK) return st;
+    }
+    // one grouped launch for every skinny materialized layer, one launch each for the rest
+    std::vector<NormTask> skinny;
+    for (int i = 0; i < n; ++i) {
+        if (plans[i].norm_kernel == NK_MAT_TC) {
+            skinny.push_back(make_norm_task(plans[i]));
+        } else {
+            dp_status st = launch_norm(ctx, plans[i]);
+            if (st != DP_OK) return st;
+        }
+    }
+    if (!skinny.empty()) {
+        const cudaError_t e = launch_mat_skinny_tc(skinny.data(), (int)skinny.size(), ctx->B, ctx->status, ctx->stream);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "grouped norm kernel launch");
+    }
+    for (int i = 0; i < n; ++i) {
+        dp_status st = finish(ctx, layer_ids[i], plans[i], sqnorm_out ? sqnorm_out[i] : nullptr);
         if (st != DP_OK) return st;
     }
     return DP_OK;
@@ -452,7 +488,13 @@ dp_status dp_clipped_noisy_grad(dp_ctx* ctx, float sigma, uint64_t seed, uint64_
             wsum.push_back(t);
             continue;
         }
-        const cudaError_t e = launch_grad_gemm_cc(t, ctx->c, ctx->status, sc, ctx->stream);
+        cudaError_t e;
+        if (ly.grad_kernel == GK_GEMM_TC) {
+            e = launch_clipped_sum_tc(t, ctx->c, ctx->status, sc, ctx->stream);
+            if (e == cudaSuccess && ly.has_bias) e = launch_bias_sum(t, ctx->c, ctx->status, sc, ctx->stream);
+        } else {
+            e = launch_grad_gemm_cc(t, ctx->c, ctx->status, sc, ctx->stream);
+        }
         if (e != cudaSuccess) return cuda_fail(ctx, e, "clipped-sum kernel launch");
     }
     if (!wsum.empty()) {

@@ -1,0 +1,627 @@
+// tcgen05 / TMA kernels whose operands are both "row = contraction index"
+// (MN-major) arrays:
+//
+//  * k_clipped_sum_tc: the reweighted clipped sum of one layer,
+//        S = E^T diag(c) A = sum_i c_i E_i^T A_i     (K = B*T rows),
+//    with the clip factor of every row applied to the TMA-staged E tile in
+//    shared memory before the tensor cores read it, and the noise epilogue
+//        G = (S + sigma C z) / L
+//    computed from TMEM ("Privacy-Preserving Machine Learning", section
+//    "Differentially private stochastic gradient descent", phases 3-5;
+//    "Sensitivity Inflation from Cross-Record Precision Routing in Private
+//    Quantized Fine-Tuning", Eq. 3).
+//
+//  * k_mat_skinny_tc: materialized per-example gradients of low-rank
+//    (LoRA) factors, g_i = E_i^T A_i, one record and one 128-wide block of
+//    the large dimension per work item, with ||g_i||_F^2 partials and the
+//    stored g_i for the weighted sum.  One launch serves many layers.
+//
+// Warp roles (one CTA per SM, persistent over work items):
+//   warp 0      TMA producer (one lane)
+//   warp 1      TMEM owner and MMA issuer (one lane)
+//   warps 2-5   clip-factor rescale of staged E tiles (clipped sum only)
+//   warps 6-9   epilogue: TMEM -> registers -> global
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "tc_common.cuh"
+
+using namespace dpk;
+
+namespace {
+
+// ============================================================ clipped sum
+constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
+constexpr int kAStage = kBM * kBK * 2;  // E tile: 2 boxes of 64 columns x 64 rows
+constexpr int kBStage = kBN * kBK * 2;  // A tile: 4 boxes
+constexpr int kStageBytes = kAStage + kBStage;
+constexpr int kThreads = 320;
+constexpr int kAccCols = kBN;           // fp32 accumulator columns per buffer
+constexpr uint32_t kIdescSum = tc::idesc_bf16_f32(kBM, kBN, 1, 1);
+constexpr size_t kSumSmem = 1024 + (size_t)kStages * kStageBytes + 256;
+
+struct SumParams {
+    CUtensorMap tmE;   // {d_out, K} bf16, box {64, 64}, 128B swizzle
+    CUtensorMap tmA;   // {d_in,  K} bf16, box {64, 64}, 128B swizzle
+    int64_t K, T, d_in, d_out;
+    int m_blocks, n_blocks;
+    const float* c;
+    unsigned* status;
+    float* G;
+    int64_t coord_off;
+    float scale;       // sigma * C
+    float L;
+    uint64_t seed, step;
+};
+
+struct SumSmem {
+    uint64_t full[kStages];
+    uint64_t scaled[kStages];
+    uint64_t empty[kStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks, int& mb, int& nb) {
+    // groups of 8 row blocks, column blocks fastest inside a group: the tiles
+    // running together share their E and A column blocks in L2
+    constexpr int GM = 8;
+    const int per_group = GM * n_blocks;
+    const int g = tile / per_group;
+    const int first = g * GM;
+    const int gm = min(GM, m_blocks - first);
+    const int r = tile - g * per_group;
+    mb = first + r % gm;
+    nb = r / gm;
+}
+
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float c) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&v);
+    const float2 f = __bfloat1622float2(h);
+    h = __floats2bfloat162_rn(f.x * c, f.y * c);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// z for 32 consecutive coordinates starting at kb
+__device__ __forceinline__ void noise32(uint64_t seed, uint64_t step, uint64_t kb, float (&z)[32]) {
+    if ((kb & 3u) == 0) {
+        const uint64_t j0 = kb >> 2;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 v = noise4(seed, step, j0 + q);
+            z[4 * q] = v.x;
+            z[4 * q + 1] = v.y;
+            z[4 * q + 2] = v.z;
+            z[4 * q + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z[j] = noise_at(seed, step, kb + j);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_clipped_sum_tc(const __grid_constant__ SumParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    SumSmem* sh = reinterpret_cast<SumSmem*>(tiles + (size_t)kStages * kStageBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntiles = p.m_blocks * p.n_blocks;
+    const int nk = (int)((p.K + kBK - 1) / kBK);
+    volatile int* abort_flag = &sh->abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            tc::mbar_init(&sh->full[s], 1);
+            tc::mbar_init(&sh->scaled[s], 128);
+            tc::mbar_init(&sh->empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&sh->acc_full[a], 1);
+            tc::mbar_init(&sh->acc_empty[a], 128);
+        }
+        tc::mbar_init(&sh->drain, 1);
+        sh->abort_flag = 0;
+        tc::fence_barrier_init();
+        tc::tma_prefetch_desc(&p.tmE);
+        tc::tma_prefetch_desc(&p.tmA);
+    }
+    if (warp == 1) tc::tmem_alloc(&sh->tmem_base, 2 * kAccCols);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+    // a step that saw a non-finite norm writes nothing
+    const bool skip = status_bad(p.status);
+
+    if (!skip && warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+                int mb, nb;
+                tile_coords(tile, p.m_blocks, p.n_blocks, mb, nb);
+                for (int kt = 0; kt < nk; ++kt, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort_flag, p.status)) goto producer_done;
+                    uint8_t* st = tiles + (size_t)s * kStageBytes;
+                    tc::mbar_arrive_expect_tx(&sh->full[s], kStageBytes);
+                    const int k0 = kt * kBK;
+                    tc::tma_load_2d(st, &p.tmE, &sh->full[s], mb * kBM, k0);
+                    tc::tma_load_2d(st + 8192, &p.tmE, &sh->full[s], mb * kBM + 64, k0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        tc::tma_load_2d(st + kAStage + q * 8192, &p.tmA, &sh->full[s], nb * kBN + 64 * q, k0);
+                }
+            }
+        producer_done:
+            for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j)
+                tc::mbar_wait_drain(&sh->full[j % kStages], (j / kStages) & 1u);
+        }
+    } else if (!skip && warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, lt = 0;
+            for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++lt) {
+                const uint32_t a = lt & 1u, aph = (lt >> 1) & 1u;
+                if (!tc::mbar_wait(&sh->acc_empty[a], aph ^ 1u, abort_flag, p.status)) break;
+                tc::tc_fence_after();
+                const uint32_t d_tmem = tmem + a * kAccCols;
+                bool ok = true;
+                for (int kt = 0; kt < nk; ++kt, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (!tc::mbar_wait(&sh->scaled[s], ph, abort_flag, p.status)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    const uint32_t sa = tc::smem_u32(tiles + (size_t)s * kStageBytes);
+                    const uint32_t sb = sa + kAStage;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        // 16 contraction rows = two 8-row groups of 1024 bytes
+                        const uint64_t ad = tc::smem_desc(sa + kk * 2048, 8192, 1024, tc::SW_128B);
+                        const uint64_t bd = tc::smem_desc(sb + kk * 2048, 8192, 1024, tc::SW_128B);
+                        tc::mma_bf16(d_tmem, ad, bd, kIdescSum, (kt | kk) != 0);
+                    }
+                    tc::mma_commit(&sh->empty[s]);
+                }
+                if (!ok) break;
+                tc::mma_commit(&sh->acc_full[a]);
+            }
+        }
+    } else if (!skip && warp >= 2 && warp < 6) {
+        // ------------------------------------------------ clip-factor rescale
+        const int t = threadIdx.x - 64;
+        uint32_t it = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            for (int kt = 0; kt < nk; ++kt, ++it) {
+                const int s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1u;
+                if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) goto scale_done;
+                uint8_t* st = tiles + (size_t)s * kStageBytes;
+                const int64_t k0 = (int64_t)kt * kBK;
+                // 1024 chunks of 16 bytes; chunk q = t + 128 r holds 8 columns of
+                // row (q / 8) % 64 = t / 8 + 16 (r % 4) of the stage
+                float crow[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int64_t k = k0 + (t >> 3) + 16 * i;
+                    crow[i] = (k < p.K) ? __ldg(p.c + k / p.T) : 0.f;
+                }
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int q = t + 128 * r;
+                    const float cr = crow[r & 3];
+                    if (cr != 1.0f) {
+                        uint4* ptr = reinterpret_cast<uint4*>(st + (size_t)q * 16);
+                        uint4 v = *ptr;
+                        v.x = scale_bf16x2(v.x, cr);
+                        v.y = scale_bf16x2(v.y, cr);
+                        v.z = scale_bf16x2(v.z, cr);
+                        v.w = scale_bf16x2(v.w, cr);
+                        *ptr = v;
+                    }
+                }
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(&sh->scaled[s]);
+            }
+        }
+    scale_done:;
+    } else if (!skip && warp >= 6) {
+        // ------------------------------------------------ epilogue
+        const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
+        const int row = quarter * 32 + lane;
+        uint32_t lt = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++lt) {
+            int mb, nb;
+            tile_coords(tile, p.m_blocks, p.n_blocks, mb, nb);
+            const uint32_t a = lt & 1u, aph = (lt >> 1) & 1u;
+            if (!tc::mbar_wait(&sh->acc_full[a], aph, abort_flag, p.status)) break;
+            tc::tc_fence_after();
+            const int64_t m = (int64_t)mb * kBM + row;
+            const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + a * kAccCols;
+            for (int ch = 0; ch < kBN / 32; ++ch) {
+                float v[32];
+                float h[16];
+                tc::tmem_ld16(tbase + ch * 32, h);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = h[j];
+                tc::tmem_ld16(tbase + ch * 32 + 16, h);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[16 + j] = h[j];
+                const int64_t n = (int64_t)nb * kBN + ch * 32;
+                if (m >= p.d_out || n >= p.d_in) continue;
+                float z[32];
+                noise32(p.seed, p.step, (uint64_t)(p.coord_off + m * p.d_in + n), z);
+                float* out = p.G + m * p.d_in + n;
+                if (n + 32 <= p.d_in) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        float4 o;
+                        o.x = (v[j] + p.scale * z[j]) / p.L;
+                        o.y = (v[j + 1] + p.scale * z[j + 1]) / p.L;
+                        o.z = (v[j + 2] + p.scale * z[j + 2]) / p.L;
+                        o.w = (v[j + 3] + p.scale * z[j + 3]) / p.L;
+                        *reinterpret_cast<float4*>(out + j) = o;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (n + j < p.d_in) out[j] = (v[j] + p.scale * z[j]) / p.L;
+                }
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&sh->acc_empty[a]);
+        }
+    }
+
+    if (!skip && warp == 1 && lane == 0) {
+        tc::mma_commit(&sh->drain);
+        tc::mbar_wait_drain(&sh->drain, 0);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 2 * kAccCols);
+    }
+}
+
+// ============================================================ skinny materialize
+constexpr int kSkBM = 128, kSkBN = 16, kSkStages = 8;
+constexpr int kSkXStage = kSkBM * kBK * 2;   // 16 KB: 2 boxes of 64 columns x 64 rows
+constexpr int kSkYStage = kSkBN * kBK * 2;   //  2 KB: 16 columns x 64 rows, 32B swizzle
+constexpr int kSkStageBytes = kSkXStage + kSkYStage;
+constexpr int kSkAcc = 4;                    // accumulator buffers of 16 columns
+constexpr int kSkThreads = 192;              // producer, MMA, 4 epilogue warps
+constexpr uint32_t kIdescSk = tc::idesc_bf16_f32(kSkBM, kSkBN, 1, 1);
+constexpr size_t kSkSmem = 1024 + (size_t)kSkStages * kSkStageBytes + 512;
+
+struct SkinnyLayer {
+    CUtensorMap tmX;   // large operand {D, T, B}, box {64, 64, 1}, 128B swizzle
+    CUtensorMap tmY;   // rank-r operand {r, T, B}, box {16, 64, 1}, 32B swizzle
+    int64_t T, D, r;
+    int x_is_A;        // 1: X = A (d_in = D, d_out = r); 0: X = E (d_out = D, d_in = r)
+    int mblocks;
+    int item_begin;
+    float* partial;    // [B][mblocks]
+    float* gstore;     // [B][r*D] or nullptr
+};
+
+struct SkinnyParams {
+    int nlayers;
+    int total_items;
+    unsigned* status;
+    SkinnyLayer L[kMaxSkinnyGroup];
+};
+
+struct SkSmem {
+    uint64_t full[kSkStages];
+    uint64_t empty[kSkStages];
+    uint64_t acc_full[kSkAcc];
+    uint64_t acc_empty[kSkAcc];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ int find_layer(const SkinnyParams& p, int item) {
+    int l = 0;
+    while (l + 1 < p.nlayers && p.L[l + 1].item_begin <= item) ++l;
+    return l;
+}
+
+__global__ void __launch_bounds__(kSkThreads, 1) k_mat_skinny_tc(const __grid_constant__ SkinnyParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    SkSmem* sh = reinterpret_cast<SkSmem*>(tiles + (size_t)kSkStages * kSkStageBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int* abort_flag = &sh->abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSkStages; ++s) {
+            tc::mbar_init(&sh->full[s], 1);
+            tc::mbar_init(&sh->empty[s], 1);
+        }
+        for (int a = 0; a < kSkAcc; ++a) {
+            tc::mbar_init(&sh->acc_full[a], 1);
+            tc::mbar_init(&sh->acc_empty[a], 128);
+        }
+        tc::mbar_init(&sh->drain, 1);
+        sh->abort_flag = 0;
+        tc::fence_barrier_init();
+    }
+    if (warp == 1) tc::tmem_alloc(&sh->tmem_base, 64);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int item = blockIdx.x; item < p.total_items; item += gridDim.x) {
+                const SkinnyLayer& ly = p.L[find_layer(p, item)];
+                const int local = item - ly.item_begin;
+                const int rec = local / ly.mblocks, mb = local % ly.mblocks;
+                const int nk = (int)((ly.T + kBK - 1) / kBK);
+                for (int kt = 0; kt < nk; ++kt, ++it) {
+                    const int s = it % kSkStages;
+                    const uint32_t ph = (it / kSkStages) & 1u;
+                    if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort_flag, p.status)) goto sk_producer_done;
+                    uint8_t* st = tiles + (size_t)s * kSkStageBytes;
+                    tc::mbar_arrive_expect_tx(&sh->full[s], kSkStageBytes);
+                    tc::tma_load_3d(st, &ly.tmX, &sh->full[s], mb * kSkBM, kt * kBK, rec);
+                    tc::tma_load_3d(st + 8192, &ly.tmX, &sh->full[s], mb * kSkBM + 64, kt * kBK, rec);
+                    tc::tma_load_3d(st + kSkXStage, &ly.tmY, &sh->full[s], 0, kt * kBK, rec);
+                }
+            }
+        sk_producer_done:
+            // every copy this thread issued lands before the CTA may exit
+            for (uint32_t j = it > kSkStages ? it - kSkStages : 0; j < it; ++j)
+                tc::mbar_wait_drain(&sh->full[j % kSkStages], (j / kSkStages) & 1u);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t it = 0, lt = 0;
+            for (int item = blockIdx.x; item < p.total_items; item += gridDim.x, ++lt) {
+                const SkinnyLayer& ly = p.L[find_layer(p, item)];
+                const int nk = (int)((ly.T + kBK - 1) / kBK);
+                const uint32_t a = lt % kSkAcc, aph = (lt / kSkAcc) & 1u;
+                if (!tc::mbar_wait(&sh->acc_empty[a], aph ^ 1u, abort_flag, p.status)) break;
+                tc::tc_fence_after();
+                const uint32_t d_tmem = tmem + a * kSkBN;
+                bool ok = true;
+                for (int kt = 0; kt < nk; ++kt, ++it) {
+                    const int s = it % kSkStages;
+                    const uint32_t ph = (it / kSkStages) & 1u;
+                    if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    const uint32_t sx = tc::smem_u32(tiles + (size_t)s * kSkStageBytes);
+                    const uint32_t sy = sx + kSkXStage;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t ad = tc::smem_desc(sx + kk * 2048, 8192, 1024, tc::SW_128B);
+                        // 32-byte rows: an 8-row group is 256 bytes, 16 rows advance 512
+                        const uint64_t bd = tc::smem_desc(sy + kk * 512, 2048, 256, tc::SW_32B);
+                        tc::mma_bf16(d_tmem, ad, bd, kIdescSk, (kt | kk) != 0);
+                    }
+                    tc::mma_commit(&sh->empty[s]);
+                }
+                if (!ok) break;
+                tc::mma_commit(&sh->acc_full[a]);
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2-5)
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const int ew = warp - 2;
+        uint32_t lt = 0;
+        for (int item = blockIdx.x; item < p.total_items; item += gridDim.x, ++lt) {
+            const SkinnyLayer& ly = p.L[find_layer(p, item)];
+            const int local = item - ly.item_begin;
+            const int rec = local / ly.mblocks, mb = local % ly.mblocks;
+            const uint32_t a = lt % kSkAcc, aph = (lt / kSkAcc) & 1u;
+            if (!tc::mbar_wait(&sh->acc_full[a], aph, abort_flag, p.status)) break;
+            tc::tc_fence_after();
+            float v[16];
+            tc::tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + a * kSkBN, v);
+            tc::tc_fence_before();
+            tc::mbar_arrive(&sh->acc_empty[a]);
+            const int64_t d = (int64_t)mb * kSkBM + row;
+            float ss = 0.f;
+            if (d < ly.D) {
+                const int64_t ncl = ly.r * ly.D;
+                float* g = ly.gstore ? ly.gstore + (int64_t)rec * ncl : nullptr;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    if (j < ly.r) {
+                        ss = fmaf(v[j], v[j], ss);
+                        if (g) {
+                            // X = A: entry (j, d) of g [r x D]; X = E: entry (d, j) of g [D x r]
+                            const int64_t idx = ly.x_is_A ? (int64_t)j * ly.D + d : d * ly.r + j;
+                            g[idx] = v[j];
+                        }
+                    }
+                }
+            }
+            // one partial per epilogue warp (32 rows); the clip kernel adds
+            // the four in a fixed order, so no barrier is needed here
+            ss = warp_sum(ss);
+            if (lane == 0) ly.partial[((int64_t)rec * ly.mblocks + mb) * 4 + ew] = ss;
+        }
+    }
+
+    if (warp == 1 && lane == 0) {
+        // make sure no MMA is still writing TMEM before it is released
+        tc::mma_commit(&sh->drain);
+        tc::mbar_wait_drain(&sh->drain, 0);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 64);
+    }
+}
+
+// ============================================================ host side
+// driver entry point cuTensorMapEncodeTiled, fetched through the runtime so
+// that the library does not link libcuda directly
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+            const uint32_t* box, CUtensorMapSwizzle swz) {
+    auto fn = get_encode();
+    if (!fn) return false;
+    cuuint64_t gd[3], gs[2];
+    cuuint32_t bd[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i];
+        bd[i] = box[i];
+    }
+    for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bd,
+                          es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int sm_count_cached() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 1;
+    }
+    return n;
+}
+
+}  // namespace
+
+bool tc_sum_supported(int dtype, int64_t d_in, int64_t d_out, int has_bias) {
+    (void)has_bias;
+    return dtype == DT_BF16 && d_in % 8 == 0 && d_out % 8 == 0 && d_in >= 64 && d_out >= 64;
+}
+
+bool tc_skinny_supported(int dtype, int64_t d_in, int64_t d_out, int has_bias) {
+    if (dtype != DT_BF16 || has_bias) return false;
+    const int64_t r = d_in < d_out ? d_in : d_out;
+    const int64_t D = d_in < d_out ? d_out : d_in;
+    return (r == 8 || r == 16) && D % 8 == 0 && D >= 64;
+}
+
+int nslots_skinny(int64_t d_in, int64_t d_out) {
+    const int64_t D = d_in < d_out ? d_out : d_in;
+    return (int)((D + kSkBM - 1) / kSkBM) * 4;   // one partial per epilogue warp
+}
+
+cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* status, const StepScalars& sc,
+                                  cudaStream_t s) {
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_clipped_sum_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSumSmem);
+        attr = true;
+    }
+    SumParams p;
+    const int64_t K = sc.B * t.T;
+    {
+        const uint64_t dims[2] = {(uint64_t)t.d_out, (uint64_t)K};
+        const uint64_t str[1] = {(uint64_t)t.d_out * 2};
+        const uint32_t box[2] = {64, (uint32_t)kBK};
+        if (!encode(&p.tmE, t.E, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    }
+    {
+        const uint64_t dims[2] = {(uint64_t)t.d_in, (uint64_t)K};
+        const uint64_t str[1] = {(uint64_t)t.d_in * 2};
+        const uint32_t box[2] = {64, (uint32_t)kBK};
+        if (!encode(&p.tmA, t.A, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    }
+    p.K = K;
+    p.T = t.T;
+    p.d_in = t.d_in;
+    p.d_out = t.d_out;
+    p.m_blocks = (int)((t.d_out + kBM - 1) / kBM);
+    p.n_blocks = (int)((t.d_in + kBN - 1) / kBN);
+    p.c = c;
+    p.status = status;
+    p.G = t.G;
+    p.coord_off = t.coord_off;
+    p.scale = sc.sigma * sc.C;
+    p.L = sc.L;
+    p.seed = sc.seed;
+    p.step = sc.step;
+    const int ntiles = p.m_blocks * p.n_blocks;
+    const int grid = ntiles < sm_count_cached() ? ntiles : sm_count_cached();
+    k_clipped_sum_tc<<<grid, kThreads, kSumSmem, s>>>(p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsigned* status, cudaStream_t s) {
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_mat_skinny_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSkSmem);
+        attr = true;
+    }
+    for (int base = 0; base < n; base += kMaxSkinnyGroup) {
+        SkinnyParams* p = new SkinnyParams();
+        p->nlayers = n - base < kMaxSkinnyGroup ? n - base : kMaxSkinnyGroup;
+        p->status = status;
+        int items = 0;
+        for (int i = 0; i < p->nlayers; ++i) {
+            const NormTask& t = tasks[base + i];
+            SkinnyLayer& L = p->L[i];
+            const bool x_is_A = t.d_in > t.d_out;
+            L.x_is_A = x_is_A ? 1 : 0;
+            L.D = x_is_A ? t.d_in : t.d_out;
+            L.r = x_is_A ? t.d_out : t.d_in;
+            L.T = t.T;
+            L.mblocks = (int)((L.D + kSkBM - 1) / kSkBM);
+            L.item_begin = items;
+            L.partial = t.partial;
+            L.gstore = t.gstore;
+            items += (int)(B * L.mblocks);
+            const void* X = x_is_A ? t.A : t.E;
+            const void* Y = x_is_A ? t.E : t.A;
+            const uint64_t xd[3] = {(uint64_t)L.D, (uint64_t)t.T, (uint64_t)B};
+            const uint64_t xs[2] = {(uint64_t)L.D * 2, (uint64_t)(L.D * t.T * 2)};
+            const uint32_t xb[3] = {64, (uint32_t)kBK, 1};
+            const uint64_t yd[3] = {(uint64_t)L.r, (uint64_t)t.T, (uint64_t)B};
+            const uint64_t ys[2] = {(uint64_t)L.r * 2, (uint64_t)(L.r * t.T * 2)};
+            const uint32_t yb[3] = {16, (uint32_t)kBK, 1};
+            if (!encode(&L.tmX, X, 3, xd, xs, xb, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                !encode(&L.tmY, Y, 3, yd, ys, yb, CU_TENSOR_MAP_SWIZZLE_32B)) {
+                delete p;
+                return cudaErrorInvalidValue;
+            }
+        }
+        p->total_items = items;
+        const int grid = items < sm_count_cached() ? items : sm_count_cached();
+        k_mat_skinny_tc<<<grid, kSkThreads, kSkSmem, s>>>(*p);
+        count_launches(1);
+        delete p;
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}

@@ -84,7 +84,8 @@ def test_workload2_lora_opt125m_full_size():
 
 
 def test_workload3_dense_reduced():
-    w = by_index(3).scaled(B=5, layers=(by_index(3).layers[0].__class__("linear", 320, 448, 200),))
+    from synthetic.workloads import LayerSpec
+    w = by_index(3).scaled(B=5, layers=(LayerSpec("linear", 320, 448, 200),))
     layers, A, E, T = _wl_inputs(w)
     _, _, ref = assert_step_parity(layers, A, E, T, w.C, w.sigma, 3, 0)
     assert ref.paths == [dpsgd.GHOST]
@@ -99,7 +100,7 @@ def test_workload4_mlp_t1_reduced():
 
 def test_workload5_llama_layer_reduced():
     from synthetic.workloads import LayerSpec
-    T = 160
+    T = 176          # 176^2 >= 16 * 1792: every LoRA factor materializes, as at full size
     layers = []
     for t in ("q", "k", "v", "o"):
         layers += [LayerSpec(f"{t}.A", 512, 16, T), LayerSpec(f"{t}.B", 16, 512, T)]
