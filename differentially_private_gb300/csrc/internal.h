@@ -103,3 +103,8 @@ int nslots_skinny(int64_t d_in, int64_t d_out);
 cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* status,
                                   const StepScalars& sc, cudaStream_t s);
 cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsigned* status, cudaStream_t s);
+
+// ---- tcgen05 ghost Gram (tc_gram.cu)
+bool tc_gram_supported(int dtype, int64_t T, int64_t d_in, int64_t d_out);
+int nslots_gram(int64_t T);
+cudaError_t launch_ghost_gram_tc(const NormTask& t, int64_t B, unsigned* status, cudaStream_t s);

@@ -138,7 +138,9 @@ int choose(int64_t T, int64_t d_in, int64_t d_out) {
 void plan_norm(Layer& ly, int64_t T) {
     ly.path = choose(T, ly.d_in, ly.d_out);
     if (ly.path == DP_PATH_GHOST) {
-        ly.norm_kernel = (T == 1) ? NK_T1 : NK_GHOST_CC;
+        if (T == 1) ly.norm_kernel = NK_T1;
+        else if (tc_gram_supported(ly.dtype, T, ly.d_in, ly.d_out)) ly.norm_kernel = NK_GHOST_TC;
+        else ly.norm_kernel = NK_GHOST_CC;
     } else {
         ly.norm_kernel = tc_skinny_supported(ly.dtype, ly.d_in, ly.d_out, ly.has_bias) ? NK_MAT_TC : NK_MAT_CC;
     }
@@ -168,6 +170,7 @@ dp_status launch_norm(dp_ctx* ctx, const Layer& ly) {
         case NK_GHOST_CC: e = launch_norm_ghost_cc(t, ctx->B, ctx->stream); break;
         case NK_MAT_CC: e = launch_norm_mat_cc(t, ctx->B, ctx->stream); break;
         case NK_MAT_TC: e = launch_mat_skinny_tc(&t, 1, ctx->B, ctx->status, ctx->stream); break;
+        case NK_GHOST_TC: e = launch_ghost_gram_tc(t, ctx->B, ctx->status, ctx->stream); break;
         default: return fail(ctx, DP_ERR_UNSUPPORTED, "no norm kernel %d", ly.norm_kernel);
     }
     if (e != cudaSuccess) return cuda_fail(ctx, e, "norm kernel launch");
@@ -238,6 +241,7 @@ void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed);
 
 int nslots_for(int kernel, int64_t T, int64_t d_in, int64_t d_out) {
     if (kernel == NK_MAT_TC) return nslots_skinny(d_in, d_out);
+    if (kernel == NK_GHOST_TC) return nslots_gram(T);
     return nslots_cc(kernel, T, d_in, d_out);
 }
 

@@ -289,6 +289,201 @@ __global__ void __launch_bounds__(kThreads, 1) k_clipped_sum_tc(const __grid_con
     }
 }
 
+// ============================================== clipped sum, per-record fold
+// When every record spans whole 64-row K tiles (T % 64 == 0), the tensor
+// cores accumulate each record's unscaled partial P_i = E_i^T A_i in TMEM
+// (two buffers) and the epilogue warps fold S += c_i * P_i in fp32
+// registers: the clip factor is applied exactly, without rounding the
+// scaled operand back to bf16 and without a shared-memory rescale pass.
+// Warps 2-9: two per TMEM lane quarter, each owning 128 of the 256 columns.
+constexpr int kFoldThreads = 320;
+
+struct FoldSmem {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t p_full[2];
+    uint64_t p_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// z for 16 consecutive coordinates starting at kb
+__device__ __forceinline__ void noise16(uint64_t seed, uint64_t step, uint64_t kb, float (&z)[16]) {
+    if ((kb & 3u) == 0) {
+        const uint64_t j0 = kb >> 2;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 v = noise4(seed, step, j0 + q);
+            z[4 * q] = v.x;
+            z[4 * q + 1] = v.y;
+            z[4 * q + 2] = v.z;
+            z[4 * q + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) z[j] = noise_at(seed, step, kb + j);
+    }
+}
+
+__global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const __grid_constant__ SumParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    FoldSmem* sh = reinterpret_cast<FoldSmem*>(tiles + (size_t)kStages * kStageBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntiles = p.m_blocks * p.n_blocks;
+    const int kpr = (int)(p.T / kBK);              // K tiles per record
+    const int64_t B = p.K / p.T;
+    volatile int* abort_flag = &sh->abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            tc::mbar_init(&sh->full[s], 1);
+            tc::mbar_init(&sh->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&sh->p_full[b], 1);
+            tc::mbar_init(&sh->p_empty[b], 256);
+        }
+        tc::mbar_init(&sh->drain, 1);
+        sh->abort_flag = 0;
+        tc::fence_barrier_init();
+        tc::tma_prefetch_desc(&p.tmE);
+        tc::tma_prefetch_desc(&p.tmA);
+    }
+    if (warp == 1) tc::tmem_alloc(&sh->tmem_base, 2 * kAccCols);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+    const bool skip = status_bad(p.status);
+
+    if (!skip && warp == 0) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            const int nk = (int)(B * kpr);
+            for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+                int mb, nb;
+                tile_coords(tile, p.m_blocks, p.n_blocks, mb, nb);
+                for (int kt = 0; kt < nk; ++kt, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort_flag, p.status)) goto fold_producer_done;
+                    uint8_t* st = tiles + (size_t)s * kStageBytes;
+                    tc::mbar_arrive_expect_tx(&sh->full[s], kStageBytes);
+                    const int k0 = kt * kBK;
+                    tc::tma_load_2d(st, &p.tmE, &sh->full[s], mb * kBM, k0);
+                    tc::tma_load_2d(st + 8192, &p.tmE, &sh->full[s], mb * kBM + 64, k0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        tc::tma_load_2d(st + kAStage + q * 8192, &p.tmA, &sh->full[s], nb * kBN + 64 * q, k0);
+                }
+            }
+        fold_producer_done:
+            for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j)
+                tc::mbar_wait_drain(&sh->full[j % kStages], (j / kStages) & 1u);
+        }
+    } else if (!skip && warp == 1) {
+        if (lane == 0) {
+            uint32_t it = 0, rc = 0;
+            for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+                bool ok = true;
+                for (int64_t i = 0; i < B && ok; ++i, ++rc) {
+                    const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
+                    if (!tc::mbar_wait(&sh->p_empty[b], bph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    const uint32_t d_tmem = tmem + b * kAccCols;
+                    for (int kt = 0; kt < kpr; ++kt, ++it) {
+                        const int s = it % kStages;
+                        const uint32_t ph = (it / kStages) & 1u;
+                        if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) { ok = false; break; }
+                        tc::tc_fence_after();
+                        const uint32_t sa = tc::smem_u32(tiles + (size_t)s * kStageBytes);
+                        const uint32_t sb = sa + kAStage;
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            const uint64_t ad = tc::smem_desc(sa + kk * 2048, 8192, 1024, tc::SW_128B);
+                            const uint64_t bd = tc::smem_desc(sb + kk * 2048, 8192, 1024, tc::SW_128B);
+                            tc::mma_bf16(d_tmem, ad, bd, kIdescSum, (kt | kk) != 0);
+                        }
+                        tc::mma_commit(&sh->empty[s]);
+                    }
+                    if (!ok) break;
+                    tc::mma_commit(&sh->p_full[b]);
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (!skip && warp >= 2) {
+        const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;          // columns half*128 .. +127
+        const int row = quarter * 32 + lane;
+        uint32_t rc = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, p.m_blocks, p.n_blocks, mb, nb);
+            float S[128];
+#pragma unroll
+            for (int j = 0; j < 128; ++j) S[j] = 0.f;
+            bool ok = true;
+            for (int64_t i = 0; i < B; ++i, ++rc) {
+                const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
+                if (!tc::mbar_wait(&sh->p_full[b], bph, abort_flag, p.status)) { ok = false; break; }
+                tc::tc_fence_after();
+                const float ci = __ldg(p.c + i);
+                const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + half * 128;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    float v[16];
+                    tc::tmem_ld16(tb + ch * 16, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) S[ch * 16 + j] = fmaf(ci, v[j], S[ch * 16 + j]);
+                }
+                tc::tc_fence_before();
+                tc::mbar_arrive(&sh->p_empty[b]);
+            }
+            if (!ok) break;
+            const int64_t m = (int64_t)mb * kBM + row;
+            if (m < p.d_out) {
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const int64_t n = (int64_t)nb * kBN + half * 128 + ch * 16;
+                    if (n >= p.d_in) continue;
+                    float z[16];
+                    noise16(p.seed, p.step, (uint64_t)(p.coord_off + m * p.d_in + n), z);
+                    float* out = p.G + m * p.d_in + n;
+                    if (n + 16 <= p.d_in) {
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4) {
+                            float4 o;
+                            o.x = (S[ch * 16 + j] + p.scale * z[j]) / p.L;
+                            o.y = (S[ch * 16 + j + 1] + p.scale * z[j + 1]) / p.L;
+                            o.z = (S[ch * 16 + j + 2] + p.scale * z[j + 2]) / p.L;
+                            o.w = (S[ch * 16 + j + 3] + p.scale * z[j + 3]) / p.L;
+                            *reinterpret_cast<float4*>(out + j) = o;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (n + j < p.d_in) out[j] = (S[ch * 16 + j] + p.scale * z[j]) / p.L;
+                    }
+                }
+            }
+        }
+    }
+
+    if (!skip && warp == 1 && lane == 0) {
+        tc::mma_commit(&sh->drain);
+        tc::mbar_wait_drain(&sh->drain, 0);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 2 * kAccCols);
+    }
+}
+
 // ============================================================ skinny materialize
 constexpr int kSkBM = 128, kSkBN = 16, kSkStages = 8;
 constexpr int kSkXStage = kSkBM * kBK * 2;   // 16 KB: 2 boxes of 64 columns x 64 rows
@@ -540,6 +735,7 @@ cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* s
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(k_clipped_sum_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSumSmem);
+        cudaFuncSetAttribute(k_clipped_sum_fold_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSumSmem);
         attr = true;
     }
     SumParams p;
@@ -572,7 +768,10 @@ cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* s
     p.step = sc.step;
     const int ntiles = p.m_blocks * p.n_blocks;
     const int grid = ntiles < sm_count_cached() ? ntiles : sm_count_cached();
-    k_clipped_sum_tc<<<grid, kThreads, kSumSmem, s>>>(p);
+    if (t.T % kBK == 0)
+        k_clipped_sum_fold_tc<<<grid, kFoldThreads, kSumSmem, s>>>(p);
+    else
+        k_clipped_sum_tc<<<grid, kThreads, kSumSmem, s>>>(p);
     count_launches(1);
     return cudaGetLastError();
 }
