@@ -17,23 +17,30 @@ using namespace dpk;
 namespace {
 
 // --------------------------------------------------------------- clipping
-// One warp per record.  Lane l sums slots l, l+32, ... of every layer in
-// registration order, then the lanes are combined by a fixed butterfly, so
-// the result depends only on the record's partials and the slot counts.
-__global__ void __launch_bounds__(256) k_clip(const ClipParams p, float* __restrict__ n2_out,
-                                              float* __restrict__ c_out, float* __restrict__ n2_user,
-                                              float* __restrict__ c_user, unsigned* __restrict__ status) {
-    const int64_t rec = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (rec >= p.B) return;
-    float s = 0.f;
-    for (int l = 0; l < p.nlayers; ++l) {
-        const int ns = p.nslots[l];
-        const float* part = p.partial[l] + rec * ns;
-        for (int j = lane; j < ns; j += 32) s += part[j];
+// One block per record.  Warp w reduces layers w, w + 8, ... : lane l sums
+// the layer's slots l, l + 32, ... and a fixed butterfly combines the lanes;
+// then one thread adds the layer totals in registration order.  The order
+// depends only on the slot counts, never on B or on other records.
+constexpr int kClipThreads = 256;
+
+__global__ void __launch_bounds__(kClipThreads) k_clip(const ClipParams p, float* __restrict__ n2_out,
+                                                       float* __restrict__ c_out, float* __restrict__ n2_user,
+                                                       float* __restrict__ c_user, unsigned* __restrict__ status) {
+    extern __shared__ float layer_tot[];   // [nlayers]
+    const int64_t rec = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int l = warp; l < p.nlayers; l += kClipThreads / 32) {
+        const LayerSlots ls = p.table[l];
+        const float* part = ls.partial + rec * ls.nslots;
+        float s = 0.f;
+        for (int64_t j = lane; j < ls.nslots; j += 32) s += part[j];
+        s = warp_sum(s);
+        if (lane == 0) layer_tot[l] = s;
     }
-    s = warp_sum(s);
-    if (lane == 0) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float s = 0.f;
+        for (int l = 0; l < p.nlayers; ++l) s += layer_tot[l];
         float c;
         if (!isfinite(s)) {
             atomicOr(status, 1u);
@@ -67,17 +74,54 @@ __global__ void __launch_bounds__(256) k_grad_wsum(const WsumParams P, const flo
     const int64_t j0 = t.coord_off >> 2;
     const int64_t j_last = (t.coord_off + ncl - 1) >> 2;
     const float scale = sc.sigma * sc.C;
+    const bool vec = ((t.coord_off | ncl) & 3) == 0;   // Philox blocks = aligned float4 of G and g_i
     for (int64_t j = j0 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j <= j_last;
          j += (int64_t)gridDim.x * blockDim.x) {
         const float4 z4 = noise4(sc.seed, sc.step, (uint64_t)j);
-        const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
+        if (vec) {
+            const int64_t p = 4 * j - t.coord_off;
+            const float4* g4 = reinterpret_cast<const float4*>(t.gstore + p);
+            const int64_t stride4 = ncl / 4;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            int64_t i = 0;
+            // records in ascending order; four loads in flight per thread
+            for (; i + 4 <= sc.B; i += 4) {
+                float4 v[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int64_t p = 4 * j + q - t.coord_off;
-            if (p < 0 || p >= ncl) continue;
-            float acc = 0.f;
-            for (int64_t i = 0; i < sc.B; ++i) acc = fmaf(c[i], t.gstore[i * ncl + p], acc);
-            t.G[p] = (acc + scale * zz[q]) / sc.L;
+                for (int u = 0; u < 4; ++u) v[u] = __ldg(g4 + (i + u) * stride4);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float ci = __ldg(c + i + u);
+                    acc.x = fmaf(ci, v[u].x, acc.x);
+                    acc.y = fmaf(ci, v[u].y, acc.y);
+                    acc.z = fmaf(ci, v[u].z, acc.z);
+                    acc.w = fmaf(ci, v[u].w, acc.w);
+                }
+            }
+            for (; i < sc.B; ++i) {
+                const float4 v = __ldg(g4 + i * stride4);
+                const float ci = __ldg(c + i);
+                acc.x = fmaf(ci, v.x, acc.x);
+                acc.y = fmaf(ci, v.y, acc.y);
+                acc.z = fmaf(ci, v.z, acc.z);
+                acc.w = fmaf(ci, v.w, acc.w);
+            }
+            float4 o;
+            o.x = (acc.x + scale * z4.x) / sc.L;
+            o.y = (acc.y + scale * z4.y) / sc.L;
+            o.z = (acc.z + scale * z4.z) / sc.L;
+            o.w = (acc.w + scale * z4.w) / sc.L;
+            *reinterpret_cast<float4*>(t.G + p) = o;
+        } else {
+            const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int64_t p = 4 * j + q - t.coord_off;
+                if (p < 0 || p >= ncl) continue;
+                float acc = 0.f;
+                for (int64_t i = 0; i < sc.B; ++i) acc = fmaf(c[i], t.gstore[i * ncl + p], acc);
+                t.G[p] = (acc + scale * zz[q]) / sc.L;
+            }
         }
     }
 }
@@ -206,8 +250,11 @@ __global__ void k_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int6
 cudaError_t launch_clip(const ClipParams& p, float* n2, float* c, float* n2_user, float* c_user,
                         unsigned* status, cudaStream_t s) {
     const int threads = 256;
-    const int64_t blocks = (p.B * 32 + threads - 1) / threads;
-    k_clip<<<(unsigned)blocks, threads, 0, s>>>(p, n2, c, n2_user, c_user, status);
+    (void)threads;
+    const size_t smem = (size_t)p.nlayers * sizeof(float);
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(k_clip, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    k_clip<<<(unsigned)p.B, kClipThreads, smem, s>>>(p, n2, c, n2_user, c_user, status);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -2,14 +2,14 @@
 // translation units.  Nothing here is part of the public C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 enum { DT_F32 = 0, DT_BF16 = 1 };
 
-// Largest number of registered layers a context accepts (the clip kernel
-// receives every layer's partial table as a kernel parameter).
-constexpr int kMaxLayers = 512;
+// Largest number of registered layers a context accepts.
+constexpr int kMaxLayers = 4096;
 // Largest number of layers one grouped launch carries in its parameters.
 constexpr int kMaxGroup = 64;
 // Largest number of layers one skinny-materialize launch carries (each
@@ -42,6 +42,7 @@ struct NormTask {
     float* partial;     // [B][nslots] fp32 partial squared norms
     int nslots;
     float* gstore;      // [B][ncoords] per-example gradients, or nullptr
+    const CUtensorMap* maps;  // two pre-encoded TMA descriptors (tensor-core kernels), or nullptr
 };
 
 // One layer's gradient work.
@@ -54,6 +55,7 @@ struct GradTask {
     const float* gstore;   // stored per-example gradients (GK_WSUM)
     float* G;              // output, d_out*d_in (+ d_out)
     int64_t coord_off;     // first noise coordinate of the layer
+    const CUtensorMap* maps;  // two pre-encoded TMA descriptors (tensor-core kernels), or nullptr
 };
 
 struct StepScalars {
@@ -65,12 +67,17 @@ struct StepScalars {
     uint64_t step;
 };
 
+// Where a layer's per-record partial squared norms live ([B][nslots]).
+struct LayerSlots {
+    const float* partial;
+    int64_t nslots;
+};
+
 struct ClipParams {
     int nlayers;
     int64_t B;
     float C;
-    const float* partial[kMaxLayers];
-    int nslots[kMaxLayers];
+    const LayerSlots* table;   // device array of nlayers entries, registration order
 };
 
 // ---- every kernel launch of the library is counted here (dp_kernel_launches)
@@ -103,6 +110,10 @@ int nslots_skinny(int64_t d_in, int64_t d_out);
 cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* status,
                                   const StepScalars& sc, cudaStream_t s);
 cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsigned* status, cudaStream_t s);
+// TMA descriptors of a layer, encoded once per (pointers, T, B) and cached by the runtime
+bool tc_encode_skinny(const NormTask& t, int64_t B, CUtensorMap* maps2);
+bool tc_encode_sum(const GradTask& t, int64_t B, CUtensorMap* maps2);
+bool tc_encode_gram(const NormTask& t, int64_t B, CUtensorMap* maps2);
 
 // ---- tcgen05 ghost Gram (tc_gram.cu)
 bool tc_gram_supported(int dtype, int64_t T, int64_t d_in, int64_t d_out);

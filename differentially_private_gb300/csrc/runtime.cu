@@ -47,6 +47,19 @@ struct Layer {
     size_t partial_cap = 0;   // floats
     float* gstore = nullptr;
     size_t gstore_cap = 0;    // floats
+    // TMA descriptors of the tensor-core kernels, encoded once per request
+    // shape: reused while (A, E, T, B) stay the same from step to step
+    struct MapKey {
+        const void* A = nullptr;
+        const void* E = nullptr;
+        int64_t T = 0, B = 0;
+        int kind = -1;
+        bool operator==(const MapKey& o) const {
+            return A == o.A && E == o.E && T == o.T && B == o.B && kind == o.kind;
+        }
+    } nkey, gkey;
+    alignas(64) CUtensorMap nmaps[2];
+    alignas(64) CUtensorMap gmaps[2];
 };
 
 }  // namespace
@@ -66,6 +79,9 @@ struct dp_ctx {
     size_t bcap = 0;
     size_t ccap = 0;
     unsigned* status = nullptr;
+    LayerSlots* d_table = nullptr;     // clip kernel's view of every layer's partials
+    size_t d_table_cap = 0;
+    std::vector<LayerSlots> h_table;   // what d_table holds
     std::string err;
 };
 
@@ -159,6 +175,7 @@ NormTask make_norm_task(const Layer& ly) {
     t.partial = ly.partial;
     t.nslots = ly.nslots;
     t.gstore = ly.stored ? ly.gstore : nullptr;
+    t.maps = (ly.norm_kernel == NK_MAT_TC || ly.norm_kernel == NK_GHOST_TC) ? ly.nmaps : nullptr;
     return t;
 }
 
@@ -220,6 +237,44 @@ dp_status prepare(dp_ctx* ctx, int id, const void* A, const void* E, int64_t T, 
     if (plan.stored) plan.grad_kernel = GK_WSUM;
     else if (tc_sum_supported(plan.dtype, plan.d_in, plan.d_out, plan.has_bias)) plan.grad_kernel = GK_GEMM_TC;
     else plan.grad_kernel = GK_GEMM_CC;
+    // descriptors of the tensor-core kernels, re-encoded only when the request changed
+    if (plan.norm_kernel == NK_MAT_TC || plan.norm_kernel == NK_GHOST_TC) {
+        Layer::MapKey key;
+        key.A = A;
+        key.E = E;
+        key.T = T;
+        key.B = ctx->B;
+        key.kind = plan.norm_kernel;
+        if (!(key == plan.nkey)) {
+            plan.nkey = Layer::MapKey();
+            NormTask t = make_norm_task(plan);
+            t.maps = nullptr;
+            const bool ok = plan.norm_kernel == NK_MAT_TC ? tc_encode_skinny(t, ctx->B, plan.nmaps)
+                                                           : tc_encode_gram(t, ctx->B, plan.nmaps);
+            if (!ok) return fail(ctx, DP_ERR_CUDA, "TMA descriptor encoding failed for layer %d", id);
+            plan.nkey = key;
+        }
+    }
+    if (plan.grad_kernel == GK_GEMM_TC) {
+        Layer::MapKey key;
+        key.A = A;
+        key.E = E;
+        key.T = T;
+        key.B = ctx->B;
+        key.kind = GK_GEMM_TC;
+        if (!(key == plan.gkey)) {
+            plan.gkey = Layer::MapKey();
+            GradTask g{};
+            g.A = A;
+            g.E = E;
+            g.T = T;
+            g.d_in = plan.d_in;
+            g.d_out = plan.d_out;
+            if (!tc_encode_sum(g, ctx->B, plan.gmaps))
+                return fail(ctx, DP_ERR_CUDA, "TMA descriptor encoding failed for layer %d", id);
+            plan.gkey = key;
+        }
+    }
     return DP_OK;
 }
 
@@ -312,6 +367,7 @@ dp_status dp_destroy(dp_ctx* ctx) {
     cudaFree(ctx->n2);
     cudaFree(ctx->c);
     cudaFree(ctx->status);
+    cudaFree(ctx->d_table);
     delete ctx;
     return DP_OK;
 }
@@ -442,17 +498,36 @@ dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnor
         if (!ctx->layers[l].accumulated)
             return fail(ctx, DP_ERR_STATE, "layer %zu was not accumulated in this step", l);
     DeviceGuard g(ctx->device);
-    ClipParams* p = new (std::nothrow) ClipParams();
-    if (!p) return fail(ctx, DP_ERR_OOM, "host allocation failed");
-    p->nlayers = (int)ctx->layers.size();
-    p->B = ctx->B;
-    p->C = C;
-    for (int l = 0; l < p->nlayers; ++l) {
-        p->partial[l] = ctx->layers[l].partial;
-        p->nslots[l] = ctx->layers[l].nslots;
+    std::vector<LayerSlots> cur(ctx->layers.size());
+    for (size_t l = 0; l < ctx->layers.size(); ++l) {
+        cur[l].partial = ctx->layers[l].partial;
+        cur[l].nslots = ctx->layers[l].nslots;
     }
-    const cudaError_t e = launch_clip(*p, ctx->n2, ctx->c, total_sqnorm_out, c_out, ctx->status, ctx->stream);
-    delete p;
+    bool same = cur.size() == ctx->h_table.size();
+    for (size_t l = 0; same && l < cur.size(); ++l)
+        same = cur[l].partial == ctx->h_table[l].partial && cur[l].nslots == ctx->h_table[l].nslots;
+    if (!same) {
+        if (ctx->d_table_cap < cur.size()) {
+            cudaError_t e = cudaStreamSynchronize(ctx->stream);
+            if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamSynchronize");
+            cudaFree(ctx->d_table);
+            ctx->d_table = nullptr;
+            ctx->d_table_cap = 0;
+            e = cudaMalloc(reinterpret_cast<void**>(&ctx->d_table), cur.size() * sizeof(LayerSlots));
+            if (e != cudaSuccess) return fail(ctx, DP_ERR_OOM, "cudaMalloc of the layer table failed");
+            ctx->d_table_cap = cur.size();
+        }
+        ctx->h_table = cur;
+        const cudaError_t e = cudaMemcpyAsync(ctx->d_table, ctx->h_table.data(), cur.size() * sizeof(LayerSlots),
+                                              cudaMemcpyHostToDevice, ctx->stream);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "layer table upload");
+    }
+    ClipParams p;
+    p.nlayers = (int)ctx->layers.size();
+    p.B = ctx->B;
+    p.C = C;
+    p.table = ctx->d_table;
+    const cudaError_t e = launch_clip(p, ctx->n2, ctx->c, total_sqnorm_out, c_out, ctx->status, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "clip kernel launch");
     ctx->C = C;
     ctx->phase = CLIPPED;
@@ -488,6 +563,7 @@ dp_status dp_clipped_noisy_grad(dp_ctx* ctx, float sigma, uint64_t seed, uint64_
         t.gstore = ly.gstore;
         t.G = G[l];
         t.coord_off = ly.coord_off;
+        t.maps = ly.grad_kernel == GK_GEMM_TC ? ly.gmaps : nullptr;
         if (ly.grad_kernel == GK_WSUM) {
             wsum.push_back(t);
             continue;

@@ -207,23 +207,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_clipped_sum_tc(const __grid_con
                 float crow[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int64_t k = k0 + (t >> 3) + 16 * i;
-                    crow[i] = (k < p.K) ? __ldg(p.c + k / p.T) : 0.f;
+                    // K < 2^31 rows, so the record index fits 32-bit arithmetic
+                    const uint32_t k = (uint32_t)k0 + (uint32_t)(t >> 3) + 16u * i;
+                    crow[i] = (k < (uint32_t)p.K) ? __ldg(p.c + k / (uint32_t)p.T) : 0.f;
                 }
+                uint4 v[8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) v[r] = *reinterpret_cast<const uint4*>(st + (size_t)(t + 128 * r) * 16);
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
-                    const int q = t + 128 * r;
                     const float cr = crow[r & 3];
-                    if (cr != 1.0f) {
-                        uint4* ptr = reinterpret_cast<uint4*>(st + (size_t)q * 16);
-                        uint4 v = *ptr;
-                        v.x = scale_bf16x2(v.x, cr);
-                        v.y = scale_bf16x2(v.y, cr);
-                        v.z = scale_bf16x2(v.z, cr);
-                        v.w = scale_bf16x2(v.w, cr);
-                        *ptr = v;
-                    }
+                    v[r].x = scale_bf16x2(v[r].x, cr);
+                    v[r].y = scale_bf16x2(v[r].y, cr);
+                    v[r].z = scale_bf16x2(v[r].z, cr);
+                    v[r].w = scale_bf16x2(v[r].w, cr);
                 }
+#pragma unroll
+                for (int r = 0; r < 8; ++r) *reinterpret_cast<uint4*>(st + (size_t)(t + 128 * r) * 16) = v[r];
                 tc::fence_proxy_async_smem();
                 tc::mbar_arrive(&sh->scaled[s]);
             }
@@ -528,12 +528,22 @@ __device__ __forceinline__ int find_layer(const SkinnyParams& p, int item) {
     return l;
 }
 
+// Layer of the current work item; items of a CTA increase, so the cursor only
+// moves forward (one parameter read per layer boundary, not a scan per item).
+__device__ __forceinline__ void advance_layer(const SkinnyParams& p, int item, int& l) {
+    while (l + 1 < p.nlayers && p.L[l + 1].item_begin <= item) ++l;
+}
+
 __global__ void __launch_bounds__(kSkThreads, 1) k_mat_skinny_tc(const __grid_constant__ SkinnyParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     SkSmem* sh = reinterpret_cast<SkSmem*>(tiles + (size_t)kSkStages * kSkStageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int* abort_flag = &sh->abort_flag;
+    // each CTA takes one contiguous range of work items, so consecutive items
+    // share a layer and its TMA descriptors
+    const int item_lo = (int)((int64_t)blockIdx.x * p.total_items / gridDim.x);
+    const int item_hi = (int)((int64_t)(blockIdx.x + 1) * p.total_items / gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kSkStages; ++s) {
@@ -557,8 +567,16 @@ __global__ void __launch_bounds__(kSkThreads, 1) k_mat_skinny_tc(const __grid_co
     if (warp == 0) {
         if (lane == 0) {
             uint32_t it = 0;
-            for (int item = blockIdx.x; item < p.total_items; item += gridDim.x) {
-                const SkinnyLayer& ly = p.L[find_layer(p, item)];
+            // the descriptors of the (usually one or two) layers of this CTA's range
+            if (item_lo < item_hi)
+                for (int l = find_layer(p, item_lo); l <= find_layer(p, item_hi - 1); ++l) {
+                    tc::tma_prefetch_desc(&p.L[l].tmX);
+                    tc::tma_prefetch_desc(&p.L[l].tmY);
+                }
+            int cur = find_layer(p, item_lo);
+            for (int item = item_lo; item < item_hi; ++item) {
+                advance_layer(p, item, cur);
+                const SkinnyLayer& ly = p.L[cur];
                 const int local = item - ly.item_begin;
                 const int rec = local / ly.mblocks, mb = local % ly.mblocks;
                 const int nk = (int)((ly.T + kBK - 1) / kBK);
@@ -581,8 +599,10 @@ __global__ void __launch_bounds__(kSkThreads, 1) k_mat_skinny_tc(const __grid_co
     } else if (warp == 1) {
         if (lane == 0) {
             uint32_t it = 0, lt = 0;
-            for (int item = blockIdx.x; item < p.total_items; item += gridDim.x, ++lt) {
-                const SkinnyLayer& ly = p.L[find_layer(p, item)];
+            int cur = find_layer(p, item_lo);
+            for (int item = item_lo; item < item_hi; ++item, ++lt) {
+                advance_layer(p, item, cur);
+                const SkinnyLayer& ly = p.L[cur];
                 const int nk = (int)((ly.T + kBK - 1) / kBK);
                 const uint32_t a = lt % kSkAcc, aph = (lt / kSkAcc) & 1u;
                 if (!tc::mbar_wait(&sh->acc_empty[a], aph ^ 1u, abort_flag, p.status)) break;
@@ -615,8 +635,10 @@ __global__ void __launch_bounds__(kSkThreads, 1) k_mat_skinny_tc(const __grid_co
         const int row = quarter * 32 + lane;
         const int ew = warp - 2;
         uint32_t lt = 0;
-        for (int item = blockIdx.x; item < p.total_items; item += gridDim.x, ++lt) {
-            const SkinnyLayer& ly = p.L[find_layer(p, item)];
+        int cur = find_layer(p, item_lo);
+        for (int item = item_lo; item < item_hi; ++item, ++lt) {
+            advance_layer(p, item, cur);
+            const SkinnyLayer& ly = p.L[cur];
             const int local = item - ly.item_begin;
             const int rec = local / ly.mblocks, mb = local % ly.mblocks;
             const uint32_t a = lt % kSkAcc, aph = (lt / kSkAcc) & 1u;
@@ -730,6 +752,33 @@ int nslots_skinny(int64_t d_in, int64_t d_out) {
     return (int)((D + kSkBM - 1) / kSkBM) * 4;   // one partial per epilogue warp
 }
 
+bool tc_encode_sum(const GradTask& t, int64_t B, CUtensorMap* maps2) {
+    const int64_t K = B * t.T;
+    const uint32_t box[2] = {64, (uint32_t)kBK};
+    const uint64_t de[2] = {(uint64_t)t.d_out, (uint64_t)K};
+    const uint64_t se[1] = {(uint64_t)t.d_out * 2};
+    const uint64_t da[2] = {(uint64_t)t.d_in, (uint64_t)K};
+    const uint64_t sa[1] = {(uint64_t)t.d_in * 2};
+    return encode(&maps2[0], t.E, 2, de, se, box, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           encode(&maps2[1], t.A, 2, da, sa, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool tc_encode_skinny(const NormTask& t, int64_t B, CUtensorMap* maps2) {
+    const bool x_is_A = t.d_in > t.d_out;
+    const int64_t D = x_is_A ? t.d_in : t.d_out;
+    const int64_t r = x_is_A ? t.d_out : t.d_in;
+    const void* X = x_is_A ? t.A : t.E;
+    const void* Y = x_is_A ? t.E : t.A;
+    const uint64_t xd[3] = {(uint64_t)D, (uint64_t)t.T, (uint64_t)B};
+    const uint64_t xs[2] = {(uint64_t)D * 2, (uint64_t)(D * t.T * 2)};
+    const uint32_t xb[3] = {64, (uint32_t)kBK, 1};
+    const uint64_t yd[3] = {(uint64_t)r, (uint64_t)t.T, (uint64_t)B};
+    const uint64_t ys[2] = {(uint64_t)r * 2, (uint64_t)(r * t.T * 2)};
+    const uint32_t yb[3] = {16, (uint32_t)kBK, 1};
+    return encode(&maps2[0], X, 3, xd, xs, xb, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           encode(&maps2[1], Y, 3, yd, ys, yb, CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
 cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* status, const StepScalars& sc,
                                   cudaStream_t s) {
     static bool attr = false;
@@ -739,20 +788,16 @@ cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* s
         attr = true;
     }
     SumParams p;
-    const int64_t K = sc.B * t.T;
-    {
-        const uint64_t dims[2] = {(uint64_t)t.d_out, (uint64_t)K};
-        const uint64_t str[1] = {(uint64_t)t.d_out * 2};
-        const uint32_t box[2] = {64, (uint32_t)kBK};
-        if (!encode(&p.tmE, t.E, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    if (t.maps) {
+        p.tmE = t.maps[0];
+        p.tmA = t.maps[1];
+    } else {
+        CUtensorMap m[2];
+        if (!tc_encode_sum(t, sc.B, m)) return cudaErrorInvalidValue;
+        p.tmE = m[0];
+        p.tmA = m[1];
     }
-    {
-        const uint64_t dims[2] = {(uint64_t)t.d_in, (uint64_t)K};
-        const uint64_t str[1] = {(uint64_t)t.d_in * 2};
-        const uint32_t box[2] = {64, (uint32_t)kBK};
-        if (!encode(&p.tmA, t.A, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-    }
-    p.K = K;
+    p.K = sc.B * t.T;
     p.T = t.T;
     p.d_in = t.d_in;
     p.d_out = t.d_out;
@@ -782,14 +827,14 @@ cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsign
         cudaFuncSetAttribute(k_mat_skinny_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSkSmem);
         attr = true;
     }
+    thread_local SkinnyParams p;   // host staging of the (large) parameter block; each launch copies it
     for (int base = 0; base < n; base += kMaxSkinnyGroup) {
-        SkinnyParams* p = new SkinnyParams();
-        p->nlayers = n - base < kMaxSkinnyGroup ? n - base : kMaxSkinnyGroup;
-        p->status = status;
+        p.nlayers = n - base < kMaxSkinnyGroup ? n - base : kMaxSkinnyGroup;
+        p.status = status;
         int items = 0;
-        for (int i = 0; i < p->nlayers; ++i) {
+        for (int i = 0; i < p.nlayers; ++i) {
             const NormTask& t = tasks[base + i];
-            SkinnyLayer& L = p->L[i];
+            SkinnyLayer& L = p.L[i];
             const bool x_is_A = t.d_in > t.d_out;
             L.x_is_A = x_is_A ? 1 : 0;
             L.D = x_is_A ? t.d_in : t.d_out;
@@ -800,25 +845,20 @@ cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsign
             L.partial = t.partial;
             L.gstore = t.gstore;
             items += (int)(B * L.mblocks);
-            const void* X = x_is_A ? t.A : t.E;
-            const void* Y = x_is_A ? t.E : t.A;
-            const uint64_t xd[3] = {(uint64_t)L.D, (uint64_t)t.T, (uint64_t)B};
-            const uint64_t xs[2] = {(uint64_t)L.D * 2, (uint64_t)(L.D * t.T * 2)};
-            const uint32_t xb[3] = {64, (uint32_t)kBK, 1};
-            const uint64_t yd[3] = {(uint64_t)L.r, (uint64_t)t.T, (uint64_t)B};
-            const uint64_t ys[2] = {(uint64_t)L.r * 2, (uint64_t)(L.r * t.T * 2)};
-            const uint32_t yb[3] = {16, (uint32_t)kBK, 1};
-            if (!encode(&L.tmX, X, 3, xd, xs, xb, CU_TENSOR_MAP_SWIZZLE_128B) ||
-                !encode(&L.tmY, Y, 3, yd, ys, yb, CU_TENSOR_MAP_SWIZZLE_32B)) {
-                delete p;
-                return cudaErrorInvalidValue;
+            if (t.maps) {
+                L.tmX = t.maps[0];
+                L.tmY = t.maps[1];
+            } else {
+                CUtensorMap m[2];
+                if (!tc_encode_skinny(t, B, m)) return cudaErrorInvalidValue;
+                L.tmX = m[0];
+                L.tmY = m[1];
             }
         }
-        p->total_items = items;
+        p.total_items = items;
         const int grid = items < sm_count_cached() ? items : sm_count_cached();
-        k_mat_skinny_tc<<<grid, kSkThreads, kSkSmem, s>>>(*p);
+        k_mat_skinny_tc<<<grid, kSkThreads, kSkSmem, s>>>(p);
         count_launches(1);
-        delete p;
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

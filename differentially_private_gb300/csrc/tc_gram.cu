@@ -232,6 +232,15 @@ int gram_tiles_per_rec(int64_t T) {
 
 }  // namespace
 
+bool tc_encode_gram(const NormTask& t, int64_t B, CUtensorMap* maps2) {
+    const uint32_t box[3] = {64, (uint32_t)kGM, 1};
+    const uint64_t da[3] = {(uint64_t)t.d_in, (uint64_t)t.T, (uint64_t)B};
+    const uint64_t sa[2] = {(uint64_t)t.d_in * 2, (uint64_t)(t.d_in * t.T * 2)};
+    const uint64_t de[3] = {(uint64_t)t.d_out, (uint64_t)t.T, (uint64_t)B};
+    const uint64_t se[2] = {(uint64_t)t.d_out * 2, (uint64_t)(t.d_out * t.T * 2)};
+    return encode_bf16(&maps2[0], t.A, da, sa, box) && encode_bf16(&maps2[1], t.E, de, se, box);
+}
+
 bool tc_gram_supported(int dtype, int64_t T, int64_t d_in, int64_t d_out) {
     return dtype == DT_BF16 && T > 1 && d_in % 8 == 0 && d_out % 8 == 0 && d_in >= 64 && d_out >= 64;
 }
@@ -245,16 +254,14 @@ cudaError_t launch_ghost_gram_tc(const NormTask& t, int64_t B, unsigned* status,
         attr = true;
     }
     GramParams p;
-    const uint32_t box[3] = {64, (uint32_t)kGM, 1};
-    {
-        const uint64_t dims[3] = {(uint64_t)t.d_in, (uint64_t)t.T, (uint64_t)B};
-        const uint64_t str[2] = {(uint64_t)t.d_in * 2, (uint64_t)(t.d_in * t.T * 2)};
-        if (!encode_bf16(&p.tmA, t.A, dims, str, box)) return cudaErrorInvalidValue;
-    }
-    {
-        const uint64_t dims[3] = {(uint64_t)t.d_out, (uint64_t)t.T, (uint64_t)B};
-        const uint64_t str[2] = {(uint64_t)t.d_out * 2, (uint64_t)(t.d_out * t.T * 2)};
-        if (!encode_bf16(&p.tmE, t.E, dims, str, box)) return cudaErrorInvalidValue;
+    if (t.maps) {
+        p.tmA = t.maps[0];
+        p.tmE = t.maps[1];
+    } else {
+        CUtensorMap m[2];
+        if (!tc_encode_gram(t, B, m)) return cudaErrorInvalidValue;
+        p.tmA = m[0];
+        p.tmE = m[1];
     }
     p.T = t.T;
     p.d_in = t.d_in;
