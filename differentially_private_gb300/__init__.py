@@ -31,6 +31,7 @@ from ._binding import (  # noqa: F401
     dp_kernel_launches,
     dp_last_error,
     dp_layer_info,
+    dp_layer_sqnorms_static,
     dp_norm_accumulate,
     dp_norm_accumulate_batch,
     dp_num_coords,

@@ -35,7 +35,7 @@ EXPORTS = (
     "dp_version", "dp_kernel_launches", "dp_status_string", "dp_create", "dp_destroy", "dp_register_layer",
     "dp_layer_info", "dp_num_coords", "dp_choose_path", "dp_begin_step", "dp_set_normalizer",
     "dp_norm_accumulate", "dp_norm_accumulate_batch", "dp_clip_factors", "dp_clipped_noisy_grad",
-    "dp_step_status", "dp_last_error", "dp_philox_normals",
+    "dp_step_status", "dp_last_error", "dp_philox_normals", "dp_layer_sqnorms_static",
 )
 
 
@@ -85,6 +85,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "dp_step_status": (i32, [vp]),
         "dp_last_error": (c.c_char_p, [vp]),
         "dp_philox_normals": (i32, [u64, u64, u64, i64, vp, vp, vp]),
+        "dp_layer_sqnorms_static": (i32, [vp, vp, i64, i64, i64, i64, i32, i32, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -215,3 +216,11 @@ def dp_last_error(ctx) -> str:
 def dp_philox_normals(seed: int, step: int, k0: int, n: int, raw_out=None, z_out=None, stream=None) -> None:
     _check(load_library().dp_philox_normals(int(seed) & (2 ** 64 - 1), int(step) & (2 ** 64 - 1), int(k0), int(n),
                                             _ptr(raw_out), _ptr(z_out), _stream(stream)), "dp_philox_normals")
+
+
+def dp_layer_sqnorms_static(A, E, B: int, T: int, d_in: int, d_out: int, has_bias: bool, dtype: int,
+                            sqnorm_out, stream=None) -> None:
+    """One layer's per-example squared norms through the entry point that allocates nothing."""
+    _check(load_library().dp_layer_sqnorms_static(_ptr(A), _ptr(E), int(B), int(T), int(d_in), int(d_out),
+                                                  int(bool(has_bias)), int(dtype), _ptr(sqnorm_out),
+                                                  _stream(stream)), "dp_layer_sqnorms_static")

@@ -85,6 +85,8 @@ void count_launches(int n);
 
 // ---- slot counts (depend on the shapes only, never on B)
 int nslots_for(int kernel, int64_t T, int64_t d_in, int64_t d_out);
+// norm kernel the runtime picks for these shapes (NormKernel), and its slot count
+int plan_norm_kernel(int dtype, int64_t T, int64_t d_in, int64_t d_out, int has_bias, int* nslots);
 int nslots_cc(int kernel, int64_t T, int64_t d_in, int64_t d_out);
 
 // ---- launchers; each returns the cudaGetLastError() of its launches

@@ -294,6 +294,17 @@ static std::atomic<int64_t> g_launches{0};
 
 void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+int plan_norm_kernel(int dtype, int64_t T, int64_t d_in, int64_t d_out, int has_bias, int* nslots) {
+    Layer ly;
+    ly.d_in = d_in;
+    ly.d_out = d_out;
+    ly.has_bias = has_bias;
+    ly.dtype = dtype;
+    plan_norm(ly, T);
+    *nslots = ly.nslots;
+    return ly.norm_kernel;
+}
+
 int nslots_for(int kernel, int64_t T, int64_t d_in, int64_t d_out) {
     if (kernel == NK_MAT_TC) return nslots_skinny(d_in, d_out);
     if (kernel == NK_GHOST_TC) return nslots_gram(T);

@@ -222,6 +222,37 @@ const char* dp_last_error(const dp_ctx* ctx);
 dp_status dp_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int64_t n,
                             uint32_t* raw_out, float* z_out, void* stream);
 
+/*
+ * dp_layer_sqnorms_static -- per-example squared gradient norms of ONE layer
+ * without allocating anything.  The pages have no counterpart of this entry
+ * point: it exists for callers that cannot call cudaMalloc -- a process that
+ * reserved all device memory for its own pool at start-up, a program whose
+ * device memory is owned by another framework's allocator, or a
+ * latency-bound loop that cannot afford the device-wide synchronization
+ * cudaMalloc / cudaFree may perform.
+ *
+ * It computes what dp_norm_accumulate writes to sqnorm_out (same kernels,
+ * same shape rule, no context): sqnorm_out[i] = ||E_i^T A_i||_F^2
+ * (+ ||sum_t E_i[t]||^2 when has_bias).  A [B, T, d_in], E [B, T, d_out]
+ * (device, dtype, 16-byte aligned), sqnorm_out device float [B]; work is
+ * enqueued on `stream` (cudaStream_t, NULL = legacy default) of the CURRENT
+ * device.  The kernels' partial sums go to a fixed file-scope device array
+ * of 2^20 floats (4 MiB) that every GPU loading the library keeps until the
+ * process exits; a request needing more than 2^20 partial slots
+ * (B times the slots per record, which depend on T, d_in and d_out) fails
+ * with DP_ERR_SHAPE before anything is launched.  The first call on a
+ * device resolves the array's device address (cudaGetSymbolAddress); make
+ * that first call before any stream capture.  All calls share the one
+ * array and it keeps the last call's contents: calls whose work overlaps on
+ * the GPU (other streams, other host threads) race and give wrong results;
+ * serialize them.  Returns DP_ERR_INVALID_ARG / DP_ERR_SHAPE for bad
+ * arguments, DP_ERR_CUDA when a CUDA call or launch fails.  No cudaMalloc,
+ * cudaFree or allocating library routine is called.
+ */
+dp_status dp_layer_sqnorms_static(const void* A, const void* E, int64_t B, int64_t T, int64_t d_in,
+                                  int64_t d_out, int has_bias, dp_dtype dtype, float* sqnorm_out,
+                                  void* stream);
+
 #ifdef __cplusplus
 }
 #endif
