@@ -17,30 +17,41 @@ using namespace dpk;
 namespace {
 
 // --------------------------------------------------------------- clipping
-// One block per record.  Warp w reduces layers w, w + 8, ... : lane l sums
-// the layer's slots l, l + 32, ... and a fixed butterfly combines the lanes;
-// then one thread adds the layer totals in registration order.  The order
+// One block per record.  The record's partial slots of all layers, in
+// registration order, form one flat index space; thread t sums flat slots
+// t, t + blockDim, ... (so every load of the record is in flight at once),
+// then a fixed-order block reduction combines the threads.  The order
 // depends only on the slot counts, never on B or on other records.
-constexpr int kClipThreads = 256;
+constexpr int kClipThreads = 512;
 
 __global__ void __launch_bounds__(kClipThreads) k_clip(const ClipParams p, float* __restrict__ n2_out,
                                                        float* __restrict__ c_out, float* __restrict__ n2_user,
                                                        float* __restrict__ c_user, unsigned* __restrict__ status) {
-    extern __shared__ float layer_tot[];   // [nlayers]
+    extern __shared__ int64_t clip_smem[];
+    int64_t* pref = clip_smem;                                            // [nlayers + 1] first flat slot
+    const float** base = reinterpret_cast<const float**>(clip_smem + p.nlayers + 1);  // [nlayers]
+    __shared__ float red[32];
     const int64_t rec = blockIdx.x;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int l = warp; l < p.nlayers; l += kClipThreads / 32) {
+    for (int l = threadIdx.x; l < p.nlayers; l += blockDim.x) {
         const LayerSlots ls = p.table[l];
-        const float* part = ls.partial + rec * ls.nslots;
-        float s = 0.f;
-        for (int64_t j = lane; j < ls.nslots; j += 32) s += part[j];
-        s = warp_sum(s);
-        if (lane == 0) layer_tot[l] = s;
+        base[l] = ls.partial + rec * ls.nslots;
+        pref[l + 1] = ls.nslots;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        float s = 0.f;
-        for (int l = 0; l < p.nlayers; ++l) s += layer_tot[l];
+        pref[0] = 0;
+        for (int l = 0; l < p.nlayers; ++l) pref[l + 1] += pref[l];
+    }
+    __syncthreads();
+    const int64_t total = pref[p.nlayers];
+    float s = 0.f;
+    int l = 0;
+    for (int64_t j = threadIdx.x; j < total; j += blockDim.x) {
+        while (pref[l + 1] <= j) ++l;
+        s += base[l][j - pref[l]];
+    }
+    s = block_sum(s, red);
+    if (threadIdx.x == 0) {
         float c;
         if (!isfinite(s)) {
             atomicOr(status, 1u);
@@ -84,18 +95,21 @@ __global__ void __launch_bounds__(256) k_grad_wsum(const WsumParams P, const flo
             const int64_t stride4 = ncl / 4;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             int64_t i = 0;
-            // records in ascending order; four loads in flight per thread
-            for (; i + 4 <= sc.B; i += 4) {
-                float4 v[4];
+            // records in ascending order; eight records' loads in flight per thread
+            for (; i + 8 <= sc.B; i += 8) {
+                float4 v[8];
+                float cv[8];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) v[u] = __ldg(g4 + (i + u) * stride4);
+                for (int u = 0; u < 8; ++u) {
+                    v[u] = __ldg(g4 + (i + u) * stride4);
+                    cv[u] = __ldg(c + i + u);
+                }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float ci = __ldg(c + i + u);
-                    acc.x = fmaf(ci, v[u].x, acc.x);
-                    acc.y = fmaf(ci, v[u].y, acc.y);
-                    acc.z = fmaf(ci, v[u].z, acc.z);
-                    acc.w = fmaf(ci, v[u].w, acc.w);
+                for (int u = 0; u < 8; ++u) {
+                    acc.x = fmaf(cv[u], v[u].x, acc.x);
+                    acc.y = fmaf(cv[u], v[u].y, acc.y);
+                    acc.z = fmaf(cv[u], v[u].z, acc.z);
+                    acc.w = fmaf(cv[u], v[u].w, acc.w);
                 }
             }
             for (; i < sc.B; ++i) {
@@ -251,7 +265,7 @@ cudaError_t launch_clip(const ClipParams& p, float* n2, float* c, float* n2_user
                         unsigned* status, cudaStream_t s) {
     const int threads = 256;
     (void)threads;
-    const size_t smem = (size_t)p.nlayers * sizeof(float);
+    const size_t smem = (size_t)(2 * p.nlayers + 1) * sizeof(int64_t);
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(k_clip, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     k_clip<<<(unsigned)p.B, kClipThreads, smem, s>>>(p, n2, c, n2_user, c_user, status);

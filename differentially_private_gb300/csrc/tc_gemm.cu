@@ -1,5 +1,5 @@
-// tcgen05 / TMA kernels whose operands are both "row = contraction index"
-// (MN-major) arrays:
+// tcgen05 / TMA kernels for the reweighted clipped sum, whose operands are
+// both "row = contraction index" (MN-major) arrays:
 //
 //  * k_clipped_sum_tc: the reweighted clipped sum of one layer,
 //        S = E^T diag(c) A = sum_i c_i E_i^T A_i     (K = B*T rows),
@@ -10,11 +10,6 @@
 //    "Differentially private stochastic gradient descent", phases 3-5;
 //    "Sensitivity Inflation from Cross-Record Precision Routing in Private
 //    Quantized Fine-Tuning", Eq. 3).
-//
-//  * k_mat_skinny_tc: materialized per-example gradients of low-rank
-//    (LoRA) factors, g_i = E_i^T A_i, one record and one 128-wide block of
-//    the large dimension per work item, with ||g_i||_F^2 partials and the
-//    stored g_i for the weighted sum.  One launch serves many layers.
 //
 // Warp roles (one CTA per SM, persistent over work items):
 //   warp 0      TMA producer (one lane)
@@ -484,207 +479,6 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
     }
 }
 
-// ============================================================ skinny materialize
-constexpr int kSkBM = 128, kSkBN = 16, kSkStages = 8;
-constexpr int kSkXStage = kSkBM * kBK * 2;   // 16 KB: 2 boxes of 64 columns x 64 rows
-constexpr int kSkYStage = kSkBN * kBK * 2;   //  2 KB: 16 columns x 64 rows, 32B swizzle
-constexpr int kSkStageBytes = kSkXStage + kSkYStage;
-constexpr int kSkAcc = 4;                    // accumulator buffers of 16 columns
-constexpr int kSkThreads = 192;              // producer, MMA, 4 epilogue warps
-constexpr uint32_t kIdescSk = tc::idesc_bf16_f32(kSkBM, kSkBN, 1, 1);
-constexpr size_t kSkSmem = 1024 + (size_t)kSkStages * kSkStageBytes + 512;
-
-struct SkinnyLayer {
-    CUtensorMap tmX;   // large operand {D, T, B}, box {64, 64, 1}, 128B swizzle
-    CUtensorMap tmY;   // rank-r operand {r, T, B}, box {16, 64, 1}, 32B swizzle
-    int64_t T, D, r;
-    int x_is_A;        // 1: X = A (d_in = D, d_out = r); 0: X = E (d_out = D, d_in = r)
-    int mblocks;
-    int item_begin;
-    float* partial;    // [B][mblocks]
-    float* gstore;     // [B][r*D] or nullptr
-};
-
-struct SkinnyParams {
-    int nlayers;
-    int total_items;
-    unsigned* status;
-    SkinnyLayer L[kMaxSkinnyGroup];
-};
-
-struct SkSmem {
-    uint64_t full[kSkStages];
-    uint64_t empty[kSkStages];
-    uint64_t acc_full[kSkAcc];
-    uint64_t acc_empty[kSkAcc];
-    uint64_t drain;
-    uint32_t tmem_base;
-    int abort_flag;
-};
-
-__device__ __forceinline__ int find_layer(const SkinnyParams& p, int item) {
-    int l = 0;
-    while (l + 1 < p.nlayers && p.L[l + 1].item_begin <= item) ++l;
-    return l;
-}
-
-// Layer of the current work item; items of a CTA increase, so the cursor only
-// moves forward (one parameter read per layer boundary, not a scan per item).
-__device__ __forceinline__ void advance_layer(const SkinnyParams& p, int item, int& l) {
-    while (l + 1 < p.nlayers && p.L[l + 1].item_begin <= item) ++l;
-}
-
-__global__ void __launch_bounds__(kSkThreads, 1) k_mat_skinny_tc(const __grid_constant__ SkinnyParams p) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    SkSmem* sh = reinterpret_cast<SkSmem*>(tiles + (size_t)kSkStages * kSkStageBytes);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    volatile int* abort_flag = &sh->abort_flag;
-    // each CTA takes one contiguous range of work items, so consecutive items
-    // share a layer and its TMA descriptors
-    const int item_lo = (int)((int64_t)blockIdx.x * p.total_items / gridDim.x);
-    const int item_hi = (int)((int64_t)(blockIdx.x + 1) * p.total_items / gridDim.x);
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kSkStages; ++s) {
-            tc::mbar_init(&sh->full[s], 1);
-            tc::mbar_init(&sh->empty[s], 1);
-        }
-        for (int a = 0; a < kSkAcc; ++a) {
-            tc::mbar_init(&sh->acc_full[a], 1);
-            tc::mbar_init(&sh->acc_empty[a], 128);
-        }
-        tc::mbar_init(&sh->drain, 1);
-        sh->abort_flag = 0;
-        tc::fence_barrier_init();
-    }
-    if (warp == 1) tc::tmem_alloc(&sh->tmem_base, 64);
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
-    const uint32_t tmem = sh->tmem_base;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            uint32_t it = 0;
-            // the descriptors of the (usually one or two) layers of this CTA's range
-            if (item_lo < item_hi)
-                for (int l = find_layer(p, item_lo); l <= find_layer(p, item_hi - 1); ++l) {
-                    tc::tma_prefetch_desc(&p.L[l].tmX);
-                    tc::tma_prefetch_desc(&p.L[l].tmY);
-                }
-            int cur = find_layer(p, item_lo);
-            for (int item = item_lo; item < item_hi; ++item) {
-                advance_layer(p, item, cur);
-                const SkinnyLayer& ly = p.L[cur];
-                const int local = item - ly.item_begin;
-                const int rec = local / ly.mblocks, mb = local % ly.mblocks;
-                const int nk = (int)((ly.T + kBK - 1) / kBK);
-                for (int kt = 0; kt < nk; ++kt, ++it) {
-                    const int s = it % kSkStages;
-                    const uint32_t ph = (it / kSkStages) & 1u;
-                    if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort_flag, p.status)) goto sk_producer_done;
-                    uint8_t* st = tiles + (size_t)s * kSkStageBytes;
-                    tc::mbar_arrive_expect_tx(&sh->full[s], kSkStageBytes);
-                    tc::tma_load_3d(st, &ly.tmX, &sh->full[s], mb * kSkBM, kt * kBK, rec);
-                    tc::tma_load_3d(st + 8192, &ly.tmX, &sh->full[s], mb * kSkBM + 64, kt * kBK, rec);
-                    tc::tma_load_3d(st + kSkXStage, &ly.tmY, &sh->full[s], 0, kt * kBK, rec);
-                }
-            }
-        sk_producer_done:
-            // every copy this thread issued lands before the CTA may exit
-            for (uint32_t j = it > kSkStages ? it - kSkStages : 0; j < it; ++j)
-                tc::mbar_wait_drain(&sh->full[j % kSkStages], (j / kSkStages) & 1u);
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            uint32_t it = 0, lt = 0;
-            int cur = find_layer(p, item_lo);
-            for (int item = item_lo; item < item_hi; ++item, ++lt) {
-                advance_layer(p, item, cur);
-                const SkinnyLayer& ly = p.L[cur];
-                const int nk = (int)((ly.T + kBK - 1) / kBK);
-                const uint32_t a = lt % kSkAcc, aph = (lt / kSkAcc) & 1u;
-                if (!tc::mbar_wait(&sh->acc_empty[a], aph ^ 1u, abort_flag, p.status)) break;
-                tc::tc_fence_after();
-                const uint32_t d_tmem = tmem + a * kSkBN;
-                bool ok = true;
-                for (int kt = 0; kt < nk; ++kt, ++it) {
-                    const int s = it % kSkStages;
-                    const uint32_t ph = (it / kSkStages) & 1u;
-                    if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) { ok = false; break; }
-                    tc::tc_fence_after();
-                    const uint32_t sx = tc::smem_u32(tiles + (size_t)s * kSkStageBytes);
-                    const uint32_t sy = sx + kSkXStage;
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t ad = tc::smem_desc(sx + kk * 2048, 8192, 1024, tc::SW_128B);
-                        // 32-byte rows: an 8-row group is 256 bytes, 16 rows advance 512
-                        const uint64_t bd = tc::smem_desc(sy + kk * 512, 2048, 256, tc::SW_32B);
-                        tc::mma_bf16(d_tmem, ad, bd, kIdescSk, (kt | kk) != 0);
-                    }
-                    tc::mma_commit(&sh->empty[s]);
-                }
-                if (!ok) break;
-                tc::mma_commit(&sh->acc_full[a]);
-            }
-        }
-    } else {
-        // ------------------------------------------------ epilogue (warps 2-5)
-        const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;
-        const int ew = warp - 2;
-        uint32_t lt = 0;
-        int cur = find_layer(p, item_lo);
-        for (int item = item_lo; item < item_hi; ++item, ++lt) {
-            advance_layer(p, item, cur);
-            const SkinnyLayer& ly = p.L[cur];
-            const int local = item - ly.item_begin;
-            const int rec = local / ly.mblocks, mb = local % ly.mblocks;
-            const uint32_t a = lt % kSkAcc, aph = (lt / kSkAcc) & 1u;
-            if (!tc::mbar_wait(&sh->acc_full[a], aph, abort_flag, p.status)) break;
-            tc::tc_fence_after();
-            float v[16];
-            tc::tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + a * kSkBN, v);
-            tc::tc_fence_before();
-            tc::mbar_arrive(&sh->acc_empty[a]);
-            const int64_t d = (int64_t)mb * kSkBM + row;
-            float ss = 0.f;
-            if (d < ly.D) {
-                const int64_t ncl = ly.r * ly.D;
-                float* g = ly.gstore ? ly.gstore + (int64_t)rec * ncl : nullptr;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    if (j < ly.r) {
-                        ss = fmaf(v[j], v[j], ss);
-                        if (g) {
-                            // X = A: entry (j, d) of g [r x D]; X = E: entry (d, j) of g [D x r]
-                            const int64_t idx = ly.x_is_A ? (int64_t)j * ly.D + d : d * ly.r + j;
-                            g[idx] = v[j];
-                        }
-                    }
-                }
-            }
-            // one partial per epilogue warp (32 rows); the clip kernel adds
-            // the four in a fixed order, so no barrier is needed here
-            ss = warp_sum(ss);
-            if (lane == 0) ly.partial[((int64_t)rec * ly.mblocks + mb) * 4 + ew] = ss;
-        }
-    }
-
-    if (warp == 1 && lane == 0) {
-        // make sure no MMA is still writing TMEM before it is released
-        tc::mma_commit(&sh->drain);
-        tc::mbar_wait_drain(&sh->drain, 0);
-    }
-    tc::tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, 64);
-    }
-}
-
 // ============================================================ host side
 // driver entry point cuTensorMapEncodeTiled, fetched through the runtime so
 // that the library does not link libcuda directly
@@ -740,18 +534,6 @@ bool tc_sum_supported(int dtype, int64_t d_in, int64_t d_out, int has_bias) {
     return dtype == DT_BF16 && d_in % 8 == 0 && d_out % 8 == 0 && d_in >= 64 && d_out >= 64;
 }
 
-bool tc_skinny_supported(int dtype, int64_t d_in, int64_t d_out, int has_bias) {
-    if (dtype != DT_BF16 || has_bias) return false;
-    const int64_t r = d_in < d_out ? d_in : d_out;
-    const int64_t D = d_in < d_out ? d_out : d_in;
-    return (r == 8 || r == 16) && D % 8 == 0 && D >= 64;
-}
-
-int nslots_skinny(int64_t d_in, int64_t d_out) {
-    const int64_t D = d_in < d_out ? d_out : d_in;
-    return (int)((D + kSkBM - 1) / kSkBM) * 4;   // one partial per epilogue warp
-}
-
 bool tc_encode_sum(const GradTask& t, int64_t B, CUtensorMap* maps2) {
     const int64_t K = B * t.T;
     const uint32_t box[2] = {64, (uint32_t)kBK};
@@ -761,22 +543,6 @@ bool tc_encode_sum(const GradTask& t, int64_t B, CUtensorMap* maps2) {
     const uint64_t sa[1] = {(uint64_t)t.d_in * 2};
     return encode(&maps2[0], t.E, 2, de, se, box, CU_TENSOR_MAP_SWIZZLE_128B) &&
            encode(&maps2[1], t.A, 2, da, sa, box, CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
-bool tc_encode_skinny(const NormTask& t, int64_t B, CUtensorMap* maps2) {
-    const bool x_is_A = t.d_in > t.d_out;
-    const int64_t D = x_is_A ? t.d_in : t.d_out;
-    const int64_t r = x_is_A ? t.d_out : t.d_in;
-    const void* X = x_is_A ? t.A : t.E;
-    const void* Y = x_is_A ? t.E : t.A;
-    const uint64_t xd[3] = {(uint64_t)D, (uint64_t)t.T, (uint64_t)B};
-    const uint64_t xs[2] = {(uint64_t)D * 2, (uint64_t)(D * t.T * 2)};
-    const uint32_t xb[3] = {64, (uint32_t)kBK, 1};
-    const uint64_t yd[3] = {(uint64_t)r, (uint64_t)t.T, (uint64_t)B};
-    const uint64_t ys[2] = {(uint64_t)r * 2, (uint64_t)(r * t.T * 2)};
-    const uint32_t yb[3] = {16, (uint32_t)kBK, 1};
-    return encode(&maps2[0], X, 3, xd, xs, xb, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           encode(&maps2[1], Y, 3, yd, ys, yb, CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
 cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* status, const StepScalars& sc,
@@ -819,48 +585,4 @@ cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* s
         k_clipped_sum_tc<<<grid, kThreads, kSumSmem, s>>>(p);
     count_launches(1);
     return cudaGetLastError();
-}
-
-cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsigned* status, cudaStream_t s) {
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_mat_skinny_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSkSmem);
-        attr = true;
-    }
-    thread_local SkinnyParams p;   // host staging of the (large) parameter block; each launch copies it
-    for (int base = 0; base < n; base += kMaxSkinnyGroup) {
-        p.nlayers = n - base < kMaxSkinnyGroup ? n - base : kMaxSkinnyGroup;
-        p.status = status;
-        int items = 0;
-        for (int i = 0; i < p.nlayers; ++i) {
-            const NormTask& t = tasks[base + i];
-            SkinnyLayer& L = p.L[i];
-            const bool x_is_A = t.d_in > t.d_out;
-            L.x_is_A = x_is_A ? 1 : 0;
-            L.D = x_is_A ? t.d_in : t.d_out;
-            L.r = x_is_A ? t.d_out : t.d_in;
-            L.T = t.T;
-            L.mblocks = (int)((L.D + kSkBM - 1) / kSkBM);
-            L.item_begin = items;
-            L.partial = t.partial;
-            L.gstore = t.gstore;
-            items += (int)(B * L.mblocks);
-            if (t.maps) {
-                L.tmX = t.maps[0];
-                L.tmY = t.maps[1];
-            } else {
-                CUtensorMap m[2];
-                if (!tc_encode_skinny(t, B, m)) return cudaErrorInvalidValue;
-                L.tmX = m[0];
-                L.tmY = m[1];
-            }
-        }
-        p.total_items = items;
-        const int grid = items < sm_count_cached() ? items : sm_count_cached();
-        k_mat_skinny_tc<<<grid, kSkThreads, kSkSmem, s>>>(p);
-        count_launches(1);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
 }

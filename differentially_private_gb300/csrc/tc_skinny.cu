@@ -1,0 +1,400 @@
+// Materialized per-example gradients of low-rank (LoRA) factors on the
+// tensor cores (tcgen05 + TMA), for layers where the chooser materializes
+// (T^2 >= d_in * d_out) and one side is a rank r of 8 or 16:
+//
+//   g_i = E_i^T A_i,   ||g_i||_F^2,   and g_i kept for the weighted sum
+//
+// ("Privacy-Preserving Machine Learning", section "Differentially private
+// stochastic gradient descent", phase 2: per-sample gradients).  With D the
+// large side, X the [T, D] operand (A for LoRA-A, E for LoRA-B) and Y the
+// [T, r] operand, the kernel computes g_i^T or g_i as X_i^T Y_i: M = 128
+// columns of X per MMA, N = 16 (r padded with the TMA's zero fill), K = T.
+//
+// Work item = (layer, record, chunk of up to 8 128-column blocks of D).
+// Stages walk the item k-tile by k-tile and, inside a k-tile, block by
+// block, so the blocks of one 64-row slab are read back to back (whole rows
+// of X in DRAM order).  Y has its own small ring and is loaded once per
+// k-tile for all blocks.  Each block accumulates into its own 16 TMEM
+// columns; items alternate between two accumulator sets.  One launch serves
+// up to kMaxSkinnyGroup layers; each CTA takes a contiguous range of items.
+//
+// The epilogue writes one partial squared norm per (record, block, epilogue
+// warp) -- no barrier, no atomics: a record's norm depends only on its own
+// rows ("Sensitivity Inflation from Cross-Record Precision Routing in
+// Private Quantized Fine-Tuning", Proposition 2).
+//
+// Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
+// warps 2-5 epilogue.
+#include "common.cuh"
+#include "tc_common.cuh"
+
+using namespace dpk;
+
+namespace {
+
+constexpr int kBM = 128, kBN = 16, kBK = 64;
+constexpr int kXStages = 8;                 // 16 KB: 128 columns x 64 rows (two 64-column boxes)
+constexpr int kYStages = 4;                 //  2 KB: 16 columns x 64 rows, 32-byte swizzle
+constexpr int kXStage = kBM * kBK * 2;
+constexpr int kYStage = kBN * kBK * 2;
+constexpr int kMaxMb = 8;                   // column blocks per work item
+constexpr int kAccSets = 2;
+constexpr uint32_t kTmemCols = 256;         // kAccSets * kMaxMb * kBN
+constexpr int kThreads = 192;
+constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kBM, kBN, 1, 1);
+constexpr size_t kSmem = 1024 + (size_t)kXStages * kXStage + (size_t)kYStages * kYStage + 8192 + 512;
+
+struct SkinnyLayer {
+    CUtensorMap tmX;   // {D, T, B}, box {64, 64, 1}, 128-byte swizzle
+    CUtensorMap tmY;   // {r, T, B}, box {16, 64, 1}, 32-byte swizzle
+    int64_t T, D, r;
+    int x_is_A;        // 1: X = A (d_in = D, d_out = r); 0: X = E (d_out = D, d_in = r)
+    int mblocks;       // 128-column blocks of D
+    int nchunks;       // items per record
+    int chunk_mb;      // blocks per item (the last item of a record may have fewer)
+    int item_begin;
+    float* partial;    // [B][mblocks * 4]
+    float* gstore;     // [B][r * D] or nullptr
+};
+
+struct SkinnyParams {
+    int nlayers;
+    int total_items;
+    unsigned* status;
+    SkinnyLayer L[kMaxSkinnyGroup];
+};
+
+struct Smem {
+    alignas(16) float gstage[4][32 * kBN];   // per epilogue warp: 32 rows x r of g before a coalesced store
+    uint64_t full[kXStages];
+    uint64_t empty[kXStages];
+    uint64_t yfull[kYStages];
+    uint64_t yempty[kYStages];
+    uint64_t acc_full[kAccSets];
+    uint64_t acc_empty[kAccSets];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ int find_layer(const SkinnyParams& p, int item) {
+    int l = 0;
+    while (l + 1 < p.nlayers && p.L[l + 1].item_begin <= item) ++l;
+    return l;
+}
+
+// items of a CTA increase, so the layer cursor only moves forward
+__device__ __forceinline__ void advance_layer(const SkinnyParams& p, int item, int& l) {
+    while (l + 1 < p.nlayers && p.L[l + 1].item_begin <= item) ++l;
+}
+
+struct ItemInfo {
+    int rec, mb0, nmb, nk;
+};
+
+__device__ __forceinline__ ItemInfo item_info(const SkinnyLayer& ly, int item) {
+    const int local = item - ly.item_begin;
+    ItemInfo r;
+    r.rec = local / ly.nchunks;
+    const int chunk = local % ly.nchunks;
+    r.mb0 = chunk * ly.chunk_mb;
+    r.nmb = min(ly.chunk_mb, ly.mblocks - r.mb0);
+    r.nk = (int)((ly.T + kBK - 1) / kBK);
+    return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_constant__ SkinnyParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* xs = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ys = xs + (size_t)kXStages * kXStage;
+    Smem* sh = reinterpret_cast<Smem*>(ys + (size_t)kYStages * kYStage);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int* abort_flag = &sh->abort_flag;
+    // each CTA takes one contiguous range of items: consecutive items share a
+    // layer and its TMA descriptors
+    const int item_lo = (int)((int64_t)blockIdx.x * p.total_items / gridDim.x);
+    const int item_hi = (int)((int64_t)(blockIdx.x + 1) * p.total_items / gridDim.x);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kXStages; ++s) {
+            tc::mbar_init(&sh->full[s], 1);
+            tc::mbar_init(&sh->empty[s], 1);
+        }
+        for (int s = 0; s < kYStages; ++s) {
+            tc::mbar_init(&sh->yfull[s], 1);
+            tc::mbar_init(&sh->yempty[s], 1);
+        }
+        for (int a = 0; a < kAccSets; ++a) {
+            tc::mbar_init(&sh->acc_full[a], 1);
+            tc::mbar_init(&sh->acc_empty[a], 128);
+        }
+        tc::mbar_init(&sh->drain, 1);
+        sh->abort_flag = 0;
+        tc::fence_barrier_init();
+    }
+    if (warp == 1) tc::tmem_alloc(&sh->tmem_base, kTmemCols);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t it = 0, yit = 0;
+            if (item_lo < item_hi)
+                for (int l = find_layer(p, item_lo); l <= find_layer(p, item_hi - 1); ++l) {
+                    tc::tma_prefetch_desc(&p.L[l].tmX);
+                    tc::tma_prefetch_desc(&p.L[l].tmY);
+                }
+            int cur = find_layer(p, item_lo);
+            for (int item = item_lo; item < item_hi; ++item) {
+                advance_layer(p, item, cur);
+                const SkinnyLayer& ly = p.L[cur];
+                const ItemInfo in = item_info(ly, item);
+                for (int kt = 0; kt < in.nk; ++kt) {
+                    const int q = yit % kYStages;
+                    const uint32_t qph = (yit / kYStages) & 1u;
+                    if (!tc::mbar_wait(&sh->yempty[q], qph ^ 1u, abort_flag, p.status)) goto producer_done;
+                    tc::mbar_arrive_expect_tx(&sh->yfull[q], kYStage);
+                    tc::tma_load_3d(ys + (size_t)q * kYStage, &ly.tmY, &sh->yfull[q], 0, kt * kBK, in.rec);
+                    ++yit;
+                    for (int m = 0; m < in.nmb; ++m, ++it) {
+                        const int s = it % kXStages;
+                        const uint32_t ph = (it / kXStages) & 1u;
+                        if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort_flag, p.status)) goto producer_done;
+                        uint8_t* st = xs + (size_t)s * kXStage;
+                        const int col = (in.mb0 + m) * kBM;
+                        tc::mbar_arrive_expect_tx(&sh->full[s], kXStage);
+                        tc::tma_load_3d(st, &ly.tmX, &sh->full[s], col, kt * kBK, in.rec);
+                        tc::tma_load_3d(st + 8192, &ly.tmX, &sh->full[s], col + 64, kt * kBK, in.rec);
+                    }
+                }
+            }
+        producer_done:
+            // every copy this thread issued lands before the CTA may exit
+            for (uint32_t j = it > kXStages ? it - kXStages : 0; j < it; ++j)
+                tc::mbar_wait_drain(&sh->full[j % kXStages], (j / kXStages) & 1u);
+            for (uint32_t j = yit > kYStages ? yit - kYStages : 0; j < yit; ++j)
+                tc::mbar_wait_drain(&sh->yfull[j % kYStages], (j / kYStages) & 1u);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, yit = 0, lt = 0;
+            int cur = find_layer(p, item_lo);
+            bool ok = true;
+            for (int item = item_lo; item < item_hi && ok; ++item, ++lt) {
+                advance_layer(p, item, cur);
+                const ItemInfo in = item_info(p.L[cur], item);
+                const uint32_t a = lt % kAccSets, aph = (lt / kAccSets) & 1u;
+                if (!tc::mbar_wait(&sh->acc_empty[a], aph ^ 1u, abort_flag, p.status)) break;
+                tc::tc_fence_after();
+                for (int kt = 0; kt < in.nk && ok; ++kt) {
+                    const int q = yit % kYStages;
+                    const uint32_t qph = (yit / kYStages) & 1u;
+                    if (!tc::mbar_wait(&sh->yfull[q], qph, abort_flag, p.status)) { ok = false; break; }
+                    const uint32_t sy = tc::smem_u32(ys + (size_t)q * kYStage);
+                    for (int m = 0; m < in.nmb; ++m, ++it) {
+                        const int s = it % kXStages;
+                        const uint32_t ph = (it / kXStages) & 1u;
+                        if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) { ok = false; break; }
+                        tc::tc_fence_after();
+                        const uint32_t sx = tc::smem_u32(xs + (size_t)s * kXStage);
+                        const uint32_t d_tmem = tmem + a * (kMaxMb * kBN) + m * kBN;
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            // X: 128-byte swizzled, 16 rows = two 1 KB groups; Y: 32-byte rows, 16 rows = 512 B
+                            const uint64_t ad = tc::smem_desc(sx + kk * 2048, 8192, 1024, tc::SW_128B);
+                            const uint64_t bd = tc::smem_desc(sy + kk * 512, 2048, 256, tc::SW_32B);
+                            tc::mma_bf16(d_tmem, ad, bd, kIdesc, (kt | kk) != 0);
+                        }
+                        tc::mma_commit(&sh->empty[s]);
+                    }
+                    if (!ok) break;
+                    tc::mma_commit(&sh->yempty[q]);
+                    ++yit;
+                }
+                if (!ok) break;
+                tc::mma_commit(&sh->acc_full[a]);
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2-5)
+        const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
+        const int row = quarter * 32 + lane;
+        const int ew = warp - 2;
+        uint32_t lt = 0;
+        int cur = find_layer(p, item_lo);
+        for (int item = item_lo; item < item_hi; ++item, ++lt) {
+            advance_layer(p, item, cur);
+            const SkinnyLayer& ly = p.L[cur];
+            const ItemInfo in = item_info(ly, item);
+            const uint32_t a = lt % kAccSets, aph = (lt / kAccSets) & 1u;
+            if (!tc::mbar_wait(&sh->acc_full[a], aph, abort_flag, p.status)) break;
+            tc::tc_fence_after();
+            const int64_t ncl = ly.r * ly.D;
+            float* g = ly.gstore ? ly.gstore + (int64_t)in.rec * ncl : nullptr;
+            float* part = ly.partial + (int64_t)in.rec * ly.mblocks * 4;
+            for (int m = 0; m < in.nmb; ++m) {
+                float v[16];
+                tc::tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + a * (kMaxMb * kBN) + m * kBN, v);
+                const int mb = in.mb0 + m;
+                const int64_t d = (int64_t)mb * kBM + row;
+                float ss = 0.f;
+                if (d < ly.D) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (j < ly.r) ss = fmaf(v[j], v[j], ss);
+                }
+                if (g && ly.x_is_A) {
+                    // entry (j, d) of g [r x D]: for each j the warp's 32 rows d are contiguous
+                    if (d < ly.D) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (j < ly.r) g[(int64_t)j * ly.D + d] = v[j];
+                    }
+                } else if (g) {
+                    // entry (d, j) of g [D x r]: the warp's 32 rows are one contiguous run of
+                    // 32 r floats; stage it in shared memory, then store it as float4s
+                    float* stage = sh->gstage[ew];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (j < ly.r) stage[lane * ly.r + j] = v[j];
+                    __syncwarp();
+                    const int64_t d0 = (int64_t)mb * kBM + quarter * 32;
+                    const int64_t nvalid = min((int64_t)32, ly.D - d0) * ly.r;   // floats of this warp's run
+                    float* dst = g + d0 * ly.r;
+                    for (int q = lane; q * 4 < nvalid; q += 32)
+                        *reinterpret_cast<float4*>(dst + 4 * q) = *reinterpret_cast<const float4*>(stage + 4 * q);
+                    __syncwarp();
+                }
+                ss = warp_sum(ss);
+                if (lane == 0) part[mb * 4 + ew] = ss;
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&sh->acc_empty[a]);
+        }
+    }
+
+    if (warp == 1 && lane == 0) {
+        // no MMA may still be writing TMEM when it is released
+        tc::mma_commit(&sh->drain);
+        tc::mbar_wait_drain(&sh->drain, 0);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+bool encode3d(CUtensorMap* m, const void* base, const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+              CUtensorMapSwizzle swz) {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return false;
+        fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    cuuint64_t gd[3] = {dims[0], dims[1], dims[2]};
+    cuuint64_t gs[2] = {strides[0], strides[1]};
+    cuuint32_t bd[3] = {box[0], box[1], box[2]};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gd, gs, bd, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+}  // namespace
+
+bool tc_skinny_supported(int dtype, int64_t d_in, int64_t d_out, int has_bias) {
+    if (dtype != DT_BF16 || has_bias) return false;
+    const int64_t r = d_in < d_out ? d_in : d_out;
+    const int64_t D = d_in < d_out ? d_out : d_in;
+    return (r == 8 || r == 16) && D % 8 == 0 && D >= 64;
+}
+
+int nslots_skinny(int64_t d_in, int64_t d_out) {
+    const int64_t D = d_in < d_out ? d_out : d_in;
+    return (int)((D + kBM - 1) / kBM) * 4;   // one partial per (block, epilogue warp)
+}
+
+bool tc_encode_skinny(const NormTask& t, int64_t B, CUtensorMap* maps2) {
+    const bool x_is_A = t.d_in > t.d_out;
+    const int64_t D = x_is_A ? t.d_in : t.d_out;
+    const int64_t r = x_is_A ? t.d_out : t.d_in;
+    const void* X = x_is_A ? t.A : t.E;
+    const void* Y = x_is_A ? t.E : t.A;
+    const uint64_t xd[3] = {(uint64_t)D, (uint64_t)t.T, (uint64_t)B};
+    const uint64_t xs[2] = {(uint64_t)D * 2, (uint64_t)(D * t.T * 2)};
+    const uint32_t xb[3] = {64, (uint32_t)kBK, 1};
+    const uint64_t yd[3] = {(uint64_t)r, (uint64_t)t.T, (uint64_t)B};
+    const uint64_t ysr[2] = {(uint64_t)r * 2, (uint64_t)(r * t.T * 2)};
+    const uint32_t yb[3] = {16, (uint32_t)kBK, 1};
+    return encode3d(&maps2[0], X, xd, xs, xb, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           encode3d(&maps2[1], Y, yd, ysr, yb, CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsigned* status, cudaStream_t s) {
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_mat_skinny_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+        attr = true;
+    }
+    thread_local SkinnyParams p;   // host staging of the parameter block; each launch copies it
+    for (int base = 0; base < n; base += kMaxSkinnyGroup) {
+        p.nlayers = n - base < kMaxSkinnyGroup ? n - base : kMaxSkinnyGroup;
+        p.status = status;
+        int items = 0;
+        for (int i = 0; i < p.nlayers; ++i) {
+            const NormTask& t = tasks[base + i];
+            SkinnyLayer& L = p.L[i];
+            const bool x_is_A = t.d_in > t.d_out;
+            L.x_is_A = x_is_A ? 1 : 0;
+            L.D = x_is_A ? t.d_in : t.d_out;
+            L.r = x_is_A ? t.d_out : t.d_in;
+            L.T = t.T;
+            L.mblocks = (int)((L.D + kBM - 1) / kBM);
+            L.nchunks = (L.mblocks + kMaxMb - 1) / kMaxMb;
+            L.chunk_mb = (L.mblocks + L.nchunks - 1) / L.nchunks;
+            L.item_begin = items;
+            L.partial = t.partial;
+            L.gstore = t.gstore;
+            items += (int)(B * L.nchunks);
+            if (t.maps) {
+                L.tmX = t.maps[0];
+                L.tmY = t.maps[1];
+            } else {
+                CUtensorMap m[2];
+                if (!tc_encode_skinny(t, B, m)) return cudaErrorInvalidValue;
+                L.tmX = m[0];
+                L.tmY = m[1];
+            }
+        }
+        p.total_items = items;
+        const int sms = sm_count();
+        const int grid = items < sms ? items : sms;
+        k_mat_skinny_tc<<<grid, kThreads, kSmem, s>>>(p);
+        count_launches(1);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}

@@ -55,6 +55,13 @@ class PrivateGradient:
         sq = torch.empty(B, dtype=torch.float32, device=self.device)
         return grads, clip, sq
 
+    def prepare(self, A_list, E_list, T_list, outputs=None, L: float | None = None,
+                layer_norms: bool = False) -> "PreparedStep":
+        """Marshal the pointer arrays of a step once, for repeated steps on the same buffers."""
+        B = int(A_list[0].shape[0])
+        outputs = outputs if outputs is not None else self.alloc_outputs(B)
+        return PreparedStep(self, A_list, E_list, T_list, outputs, L, layer_norms)
+
     def step(self, A_list, E_list, T_list, C: float, sigma: float, seed: int, step: int,
              L: float | None = None, outputs=None, layer_norms: bool = False, batch: bool = True,
              check: bool = True) -> StepOutput:
@@ -77,3 +84,61 @@ class PrivateGradient:
             if st != b.DP_OK:
                 raise b.DPError(st, "dp_step_status", b.dp_last_error(self.ctx))
         return StepOutput(grads=grads, clip=clip, sqnorm=sq, layer_sqnorm=lsq)
+
+
+class PreparedStep:
+    """The four C calls of a step with their pointer arguments marshalled once.
+
+    Valid while the tensors given to ``PrivateGradient.prepare`` stay alive
+    and keep their storage (refill them in place between steps).
+    """
+
+    def __init__(self, pg: PrivateGradient, A_list, E_list, T_list, outputs, L, layer_norms):
+        import ctypes
+        n = len(A_list)
+        self.pg = pg
+        self.lib = b.load_library()
+        self.B = int(A_list[0].shape[0])
+        self.L = L
+        self.n = n
+        self.tensors = (list(A_list), list(E_list), outputs)   # keep the storage alive
+        self.grads, self.clip, self.sqnorm = outputs
+        self.layer_sqnorm = ([torch.empty(self.B, dtype=torch.float32, device=pg.device) for _ in range(n)]
+                             if layer_norms else None)
+        self._ids = (ctypes.c_int * n)(*range(n))
+        self._a = (ctypes.c_void_p * n)(*[int(x.data_ptr()) for x in A_list])
+        self._e = (ctypes.c_void_p * n)(*[int(x.data_ptr()) for x in E_list])
+        self._t = (ctypes.c_int64 * n)(*[int(t) for t in T_list])
+        self._sq = (None if self.layer_sqnorm is None
+                    else (ctypes.c_void_p * n)(*[int(x.data_ptr()) for x in self.layer_sqnorm]))
+        self._g = (ctypes.c_void_p * n)(*[int(g.data_ptr()) for g in self.grads])
+        self._clip = int(self.clip.data_ptr())
+        self._sqn = int(self.sqnorm.data_ptr())
+
+    def run(self, C: float, sigma: float, seed: int, step: int, events=None) -> None:
+        """Enqueue one step on the context's stream (asynchronous; no status check).
+
+        events: optional four CUDA events recorded on the stream before the
+        norms, after the norms, after the clip factors and after the gradient.
+        """
+        lib, ctx = self.lib, self.pg.ctx
+        stream = self.pg.stream
+        st = lib.dp_begin_step(ctx, self.B)
+        if st == b.DP_OK and self.L is not None:
+            st = lib.dp_set_normalizer(ctx, float(self.L))
+        if events:
+            events[0].record(stream)
+        if st == b.DP_OK:
+            st = lib.dp_norm_accumulate_batch(ctx, self.n, self._ids, self._a, self._e, self._t, self._sq)
+        if events:
+            events[1].record(stream)
+        if st == b.DP_OK:
+            st = lib.dp_clip_factors(ctx, C, self._clip, self._sqn)
+        if events:
+            events[2].record(stream)
+        if st == b.DP_OK:
+            st = lib.dp_clipped_noisy_grad(ctx, sigma, seed & (2 ** 64 - 1), step & (2 ** 64 - 1), self._g)
+        if events:
+            events[3].record(stream)
+        if st != b.DP_OK:
+            raise b.DPError(st, "PreparedStep.run", b.dp_last_error(ctx))
