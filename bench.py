@@ -362,9 +362,16 @@ def run_ours(args, w):
         ach = bytes_ / (t_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / peaks["hbm_gbs"]}
-    kernel_name = {("norm", "hbm"): "norm_mat", ("norm", "tensor"): "norm_ghost",
-                   ("grad", "tensor"): "grad_gemm", ("grad", "hbm"): "grad_wsum"}[(phase, roof["bound"])]
-    roof["traffic"] = kernel_traffic(kernel_name)
+    # the kernel that dominates that phase for this workload's layer shapes
+    ghost_T = [ly.T for ly in w.layers if dp.dp_choose_path(ly.T, ly.d_in, ly.d_out) == dp.DP_PATH_GHOST]
+    if phase == "norm":
+        kernel_name = ("k_ghost_gram_tc" if roof["bound"] == "tensor"
+                       else "k_norm_t1" if ghost_T and all(t == 1 for t in ghost_T) else "k_mat_skinny_tc")
+    else:
+        kernel_name = ("k_grad_wsum" if roof["bound"] == "hbm"
+                       else "k_clipped_sum_fold_tc" if all(t % 64 == 0 for t in ghost_T) else "k_clipped_sum_tc")
+    roof["traffic"] = kernel_traffic(f"{kernel_name}@{w.name}")
+    roof["kernel"] = kernel_name
     roof["phase"] = phase
     roof["peak_source"] = peaks["source"]
 
