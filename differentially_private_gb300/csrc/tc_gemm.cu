@@ -189,37 +189,48 @@ __global__ void __launch_bounds__(kThreads, 1) k_clipped_sum_tc(const __grid_con
     } else if (!skip && warp >= 2 && warp < 6) {
         // ------------------------------------------------ clip-factor rescale
         const int t = threadIdx.x - 64;
+        // 1024 chunks of 16 bytes per stage; chunk q = t + 128 r holds 8 columns of
+        // row (q / 8) % 64 = t / 8 + 16 (r % 4).  The row scales of a K tile are
+        // fetched one stage ahead, so their latency hides behind the TMA wait.
+        auto row_scales = [&](int kt, float (&cr)[4]) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                // K < 2^31 rows, so the record index fits 32-bit arithmetic
+                const uint32_t k = (uint32_t)kt * kBK + (uint32_t)(t >> 3) + 16u * i;
+                cr[i] = (k < (uint32_t)p.K) ? __ldg(p.c + k / (uint32_t)p.T) : 0.f;
+            }
+        };
+        float cnext[4];
+        row_scales(0, cnext);
         uint32_t it = 0;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
             for (int kt = 0; kt < nk; ++kt, ++it) {
                 const int s = it % kStages;
                 const uint32_t ph = (it / kStages) & 1u;
-                if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) goto scale_done;
-                uint8_t* st = tiles + (size_t)s * kStageBytes;
-                const int64_t k0 = (int64_t)kt * kBK;
-                // 1024 chunks of 16 bytes; chunk q = t + 128 r holds 8 columns of
-                // row (q / 8) % 64 = t / 8 + 16 (r % 4) of the stage
                 float crow[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    // K < 2^31 rows, so the record index fits 32-bit arithmetic
-                    const uint32_t k = (uint32_t)k0 + (uint32_t)(t >> 3) + 16u * i;
-                    crow[i] = (k < (uint32_t)p.K) ? __ldg(p.c + k / (uint32_t)p.T) : 0.f;
+                for (int i = 0; i < 4; ++i) crow[i] = cnext[i];
+                row_scales(kt + 1 < nk ? kt + 1 : 0, cnext);
+                if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) goto scale_done;
+                uint8_t* st = tiles + (size_t)s * kStageBytes;
+                const bool all_one = crow[0] == 1.0f && crow[1] == 1.0f && crow[2] == 1.0f && crow[3] == 1.0f;
+                if (!all_one) {
+                    uint4 v[8];
+#pragma unroll
+                    for (int r = 0; r < 8; ++r)
+                        v[r] = *reinterpret_cast<const uint4*>(st + (size_t)(t + 128 * r) * 16);
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const float cr = crow[r & 3];
+                        v[r].x = scale_bf16x2(v[r].x, cr);
+                        v[r].y = scale_bf16x2(v[r].y, cr);
+                        v[r].z = scale_bf16x2(v[r].z, cr);
+                        v[r].w = scale_bf16x2(v[r].w, cr);
+                    }
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) *reinterpret_cast<uint4*>(st + (size_t)(t + 128 * r) * 16) = v[r];
+                    tc::fence_proxy_async_smem();
                 }
-                uint4 v[8];
-#pragma unroll
-                for (int r = 0; r < 8; ++r) v[r] = *reinterpret_cast<const uint4*>(st + (size_t)(t + 128 * r) * 16);
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const float cr = crow[r & 3];
-                    v[r].x = scale_bf16x2(v[r].x, cr);
-                    v[r].y = scale_bf16x2(v[r].y, cr);
-                    v[r].z = scale_bf16x2(v[r].z, cr);
-                    v[r].w = scale_bf16x2(v[r].w, cr);
-                }
-#pragma unroll
-                for (int r = 0; r < 8; ++r) *reinterpret_cast<uint4*>(st + (size_t)(t + 128 * r) * 16) = v[r];
-                tc::fence_proxy_async_smem();
                 tc::mbar_arrive(&sh->scaled[s]);
             }
         }
