@@ -96,6 +96,43 @@ __device__ __forceinline__ float4 noise4(uint64_t seed, uint64_t step, uint64_t 
     return make_float4(a.x, a.y, b.x, b.y);
 }
 
+// The 4 NB normals of blocks j0 .. j0+NB-1.  The NB Philox evaluations run
+// round by round side by side and the 2 NB Box-Muller pairs are independent,
+// so a thread has several dependency chains in flight (the GEMM epilogues run
+// with few warps per SM and would otherwise wait on one long chain).
+template <int NB>
+__device__ __forceinline__ void noise_blocks(uint64_t seed, uint64_t step, uint64_t j0, float (&z)[4 * NB]) {
+    uint4 c[NB];
+#pragma unroll
+    for (int q = 0; q < NB; ++q) {
+        const uint64_t j = j0 + q;
+        c[q] = make_uint4((uint32_t)j, (uint32_t)(j >> 32), (uint32_t)step, (uint32_t)(step >> 32));
+    }
+    uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+#pragma unroll
+        for (int q = 0; q < NB; ++q) {
+            const uint32_t p0_lo = 0xD2511F53u * c[q].x;
+            const uint32_t p0_hi = __umulhi(0xD2511F53u, c[q].x);
+            const uint32_t p1_lo = 0xCD9E8D57u * c[q].z;
+            const uint32_t p1_hi = __umulhi(0xCD9E8D57u, c[q].z);
+            c[q] = make_uint4(p1_hi ^ c[q].y ^ k0, p1_lo, p0_hi ^ c[q].w ^ k1, p0_lo);
+        }
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+#pragma unroll
+    for (int q = 0; q < NB; ++q) {
+        const float2 a = box_muller(c[q].x, c[q].y);
+        const float2 b = box_muller(c[q].z, c[q].w);
+        z[4 * q] = a.x;
+        z[4 * q + 1] = a.y;
+        z[4 * q + 2] = b.x;
+        z[4 * q + 3] = b.y;
+    }
+}
+
 // The normal of one coordinate k (computes its whole block).
 __device__ __forceinline__ float noise_at(uint64_t seed, uint64_t step, uint64_t k) {
     const uint4 w = noise_block(seed, step, k >> 2);

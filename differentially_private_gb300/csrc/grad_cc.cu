@@ -231,6 +231,31 @@ __global__ void __launch_bounds__(256) k_bias_sum(const GradTask t, const float*
     t.G[p] = (acc + sc.sigma * sc.C * noise_at(sc.seed, sc.step, (uint64_t)(t.coord_off + p))) / sc.L;
 }
 
+// ------------------------------------- clip factor folded into the operand
+// E'[k, :] = bf16(c[k / T] * E[k, :]) for the tensor-core clipped sum of
+// layers whose records do not span whole 64-row tiles (T = 1 included).
+// One thread per 8 consecutive elements of a row (d % 8 == 0); the product is
+// formed in fp32 and rounded to nearest.
+__global__ void __launch_bounds__(256) k_prescale_rows(const uint4* __restrict__ E, uint4* __restrict__ E2,
+                                                       const float* __restrict__ c, int64_t K, int64_t T,
+                                                       int64_t d8) {
+    const int64_t n = K * d8;
+    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n; q += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t k = q / d8;
+        const float ck = __ldg(c + k / T);
+        uint4 v = __ldcs(E + q);
+        uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w[i]);
+            const float2 f = __bfloat1622float2(h);
+            h = __floats2bfloat162_rn(f.x * ck, f.y * ck);
+            w[i] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        E2[q] = v;
+    }
+}
+
 // ------------------------------------------------------- noise test hook
 __global__ void k_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int64_t n,
                                  uint32_t* __restrict__ raw, float* __restrict__ z) {
@@ -310,6 +335,16 @@ cudaError_t launch_bias_sum(const GradTask& t, const float* c, const unsigned* s
     const unsigned grid = (unsigned)((t.d_out + 255) / 256);
     if (t.dtype == DT_F32) k_bias_sum<DT_F32><<<grid, 256, 0, s>>>(t, c, status, sc);
     else k_bias_sum<DT_BF16><<<grid, 256, 0, s>>>(t, c, status, sc);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prescale_rows(const void* E, void* E2, const float* c, int64_t K, int64_t T, int64_t d,
+                                 cudaStream_t s) {
+    const int64_t n = K * (d / 8);
+    int64_t grid = (n + 255) / 256;
+    if (grid > 152 * 16) grid = 152 * 16;
+    k_prescale_rows<<<(unsigned)grid, 256, 0, s>>>((const uint4*)E, (uint4*)E2, c, K, T, d / 8);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -104,6 +104,9 @@ cudaError_t launch_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int
                                   uint32_t* raw, float* z, cudaStream_t s);
 cudaError_t launch_bias_sum(const GradTask& t, const float* c, const unsigned* status,
                             const StepScalars& sc, cudaStream_t s);
+// E2 = c[row / T] * E row by row (bf16, d % 8 == 0, 16-byte aligned)
+cudaError_t launch_prescale_rows(const void* E, void* E2, const float* c, int64_t K, int64_t T, int64_t d,
+                                 cudaStream_t s);
 
 // ---- tcgen05 kernels (tc_gemm.cu)
 bool tc_sum_supported(int dtype, int64_t d_in, int64_t d_out, int has_bias);

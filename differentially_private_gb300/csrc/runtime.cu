@@ -47,6 +47,11 @@ struct Layer {
     size_t partial_cap = 0;   // floats
     float* gstore = nullptr;
     size_t gstore_cap = 0;    // floats
+    // c_i E_i in bf16 for the tensor-core sum of a layer whose T is not a
+    // multiple of 64 (the clip factor folded into the operand before the sum)
+    bool prescale = false;
+    float* escaled = nullptr;
+    size_t escaled_cap = 0;   // floats (two bf16 each)
     // TMA descriptors of the tensor-core kernels, encoded once per request
     // shape: reused while (A, E, T, B) stay the same from step to step
     struct MapKey {
@@ -79,6 +84,7 @@ struct dp_ctx {
     size_t bcap = 0;
     size_t ccap = 0;
     unsigned* status = nullptr;
+    float* one = nullptr;              // device constant 1.0f
     LayerSlots* d_table = nullptr;     // clip kernel's view of every layer's partials
     size_t d_table_cap = 0;
     std::vector<LayerSlots> h_table;   // what d_table holds
@@ -255,10 +261,19 @@ dp_status prepare(dp_ctx* ctx, int id, const void* A, const void* E, int64_t T, 
             plan.nkey = key;
         }
     }
+    plan.prescale = plan.grad_kernel == GK_GEMM_TC && T % 64 != 0;
+    if (plan.prescale) {
+        st = grow(ctx, &ly.escaled, &ly.escaled_cap, ((size_t)ctx->B * T * plan.d_out + 1) / 2);
+        if (st != DP_OK) return st;
+        plan.escaled = ly.escaled;
+        plan.escaled_cap = ly.escaled_cap;
+    }
     if (plan.grad_kernel == GK_GEMM_TC) {
+        // the sum reads the pre-scaled copy as one record of B*T rows when prescaling
+        const void* Esum = plan.prescale ? static_cast<const void*>(plan.escaled) : E;
         Layer::MapKey key;
         key.A = A;
-        key.E = E;
+        key.E = Esum;
         key.T = T;
         key.B = ctx->B;
         key.kind = GK_GEMM_TC;
@@ -266,7 +281,7 @@ dp_status prepare(dp_ctx* ctx, int id, const void* A, const void* E, int64_t T, 
             plan.gkey = Layer::MapKey();
             GradTask g{};
             g.A = A;
-            g.E = E;
+            g.E = Esum;
             g.T = T;
             g.d_in = plan.d_in;
             g.d_out = plan.d_out;
@@ -363,6 +378,16 @@ dp_status dp_create(dp_ctx** out, int device, void* cuda_stream) {
         delete ctx;
         return DP_ERR_CUDA;
     }
+    // the clip factor 1 of a layer whose operand was pre-scaled
+    const float one = 1.0f;
+    if (cudaMalloc(reinterpret_cast<void**>(&ctx->one), sizeof(float)) != cudaSuccess ||
+        cudaMemcpy(ctx->one, &one, sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(ctx->one);
+        cudaFree(ctx->status);
+        delete ctx;
+        return DP_ERR_OOM;
+    }
     *out = ctx;
     return DP_OK;
 }
@@ -374,10 +399,12 @@ dp_status dp_destroy(dp_ctx* ctx) {
     for (Layer& ly : ctx->layers) {
         cudaFree(ly.partial);
         cudaFree(ly.gstore);
+        cudaFree(ly.escaled);
     }
     cudaFree(ctx->n2);
     cudaFree(ctx->c);
     cudaFree(ctx->status);
+    cudaFree(ctx->one);
     cudaFree(ctx->d_table);
     delete ctx;
     return DP_OK;
@@ -580,7 +607,18 @@ dp_status dp_clipped_noisy_grad(dp_ctx* ctx, float sigma, uint64_t seed, uint64_
             continue;
         }
         cudaError_t e;
-        if (ly.grad_kernel == GK_GEMM_TC) {
+        if (ly.grad_kernel == GK_GEMM_TC && ly.prescale) {
+            // c_i folded into a bf16 copy of E, then one "record" of B*T rows with factor 1
+            const int64_t K = ctx->B * ly.T;
+            e = launch_prescale_rows(ly.E, ly.escaled, ctx->c, K, ly.T, ly.d_out, ctx->stream);
+            GradTask ts = t;
+            ts.E = ly.escaled;
+            ts.T = K;
+            StepScalars s1 = sc;
+            s1.B = 1;
+            if (e == cudaSuccess) e = launch_clipped_sum_tc(ts, ctx->one, ctx->status, s1, ctx->stream);
+            if (e == cudaSuccess && ly.has_bias) e = launch_bias_sum(t, ctx->c, ctx->status, sc, ctx->stream);
+        } else if (ly.grad_kernel == GK_GEMM_TC) {
             e = launch_clipped_sum_tc(t, ctx->c, ctx->status, sc, ctx->stream);
             if (e == cudaSuccess && ly.has_bias) e = launch_bias_sum(t, ctx->c, ctx->status, sc, ctx->stream);
         } else {

@@ -1,21 +1,21 @@
 // tcgen05 / TMA kernels for the reweighted clipped sum, whose operands are
 // both "row = contraction index" (MN-major) arrays:
 //
-//  * k_clipped_sum_tc: the reweighted clipped sum of one layer,
+//  * k_clipped_sum_fold_tc: the reweighted clipped sum of one layer,
 //        S = E^T diag(c) A = sum_i c_i E_i^T A_i     (K = B*T rows),
-//    with the clip factor of every row applied to the TMA-staged E tile in
-//    shared memory before the tensor cores read it, and the noise epilogue
-//        G = (S + sigma C z) / L
-//    computed from TMEM ("Privacy-Preserving Machine Learning", section
-//    "Differentially private stochastic gradient descent", phases 3-5;
-//    "Sensitivity Inflation from Cross-Record Precision Routing in Private
-//    Quantized Fine-Tuning", Eq. 3).
+//    and the noise epilogue G = (S + sigma C z) / L computed from TMEM
+//    ("Privacy-Preserving Machine Learning", section "Differentially private
+//    stochastic gradient descent", phases 3-5; "Sensitivity Inflation from
+//    Cross-Record Precision Routing in Private Quantized Fine-Tuning", Eq. 3).
+//    When T is a multiple of 64 the clip factor is folded per record in fp32
+//    (below).  Otherwise the runtime first writes c_i E_i into scratch
+//    (k_prescale_rows, the clip factor folded into the staged operand) and
+//    runs this kernel as a single "record" of K rows with factor 1.
 //
-// Warp roles (one CTA per SM, persistent over work items):
+// Warp roles (one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer (one lane)
 //   warp 1      TMEM owner and MMA issuer (one lane)
-//   warps 2-5   clip-factor rescale of staged E tiles (clipped sum only)
-//   warps 6-9   epilogue: TMEM -> registers -> global
+//   warps 2-17  fold S += c_i P_i, then the noise epilogue
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -30,7 +30,6 @@ constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
 constexpr int kAStage = kBM * kBK * 2;  // E tile: 2 boxes of 64 columns x 64 rows
 constexpr int kBStage = kBN * kBK * 2;  // A tile: 4 boxes
 constexpr int kStageBytes = kAStage + kBStage;
-constexpr int kThreads = 320;
 constexpr int kAccCols = kBN;           // fp32 accumulator columns per buffer
 constexpr uint32_t kIdescSum = tc::idesc_bf16_f32(kBM, kBN, 1, 1);
 constexpr size_t kSumSmem = 1024 + (size_t)kStages * kStageBytes + 256;
@@ -45,19 +44,8 @@ struct SumParams {
     float* G;
     int64_t coord_off;
     float scale;       // sigma * C
-    float L;
+    float inv_L;       // 1 / L
     uint64_t seed, step;
-};
-
-struct SumSmem {
-    uint64_t full[kStages];
-    uint64_t scaled[kStages];
-    uint64_t empty[kStages];
-    uint64_t acc_full[2];
-    uint64_t acc_empty[2];
-    uint64_t drain;
-    uint32_t tmem_base;
-    int abort_flag;
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks, int& mb, int& nb) {
@@ -73,236 +61,18 @@ __device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks
     nb = r / gm;
 }
 
-__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float c) {
-    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&v);
-    const float2 f = __bfloat1622float2(h);
-    h = __floats2bfloat162_rn(f.x * c, f.y * c);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// z for 32 consecutive coordinates starting at kb
-__device__ __forceinline__ void noise32(uint64_t seed, uint64_t step, uint64_t kb, float (&z)[32]) {
-    if ((kb & 3u) == 0) {
-        const uint64_t j0 = kb >> 2;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float4 v = noise4(seed, step, j0 + q);
-            z[4 * q] = v.x;
-            z[4 * q + 1] = v.y;
-            z[4 * q + 2] = v.z;
-            z[4 * q + 3] = v.w;
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) z[j] = noise_at(seed, step, kb + j);
-    }
-}
-
-__global__ void __launch_bounds__(kThreads, 1) k_clipped_sum_tc(const __grid_constant__ SumParams p) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    SumSmem* sh = reinterpret_cast<SumSmem*>(tiles + (size_t)kStages * kStageBytes);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ntiles = p.m_blocks * p.n_blocks;
-    const int nk = (int)((p.K + kBK - 1) / kBK);
-    volatile int* abort_flag = &sh->abort_flag;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            tc::mbar_init(&sh->full[s], 1);
-            tc::mbar_init(&sh->scaled[s], 128);
-            tc::mbar_init(&sh->empty[s], 1);
-        }
-        for (int a = 0; a < 2; ++a) {
-            tc::mbar_init(&sh->acc_full[a], 1);
-            tc::mbar_init(&sh->acc_empty[a], 128);
-        }
-        tc::mbar_init(&sh->drain, 1);
-        sh->abort_flag = 0;
-        tc::fence_barrier_init();
-        tc::tma_prefetch_desc(&p.tmE);
-        tc::tma_prefetch_desc(&p.tmA);
-    }
-    if (warp == 1) tc::tmem_alloc(&sh->tmem_base, 2 * kAccCols);
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
-    const uint32_t tmem = sh->tmem_base;
-    // a step that saw a non-finite norm writes nothing
-    const bool skip = status_bad(p.status);
-
-    if (!skip && warp == 0) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
-            uint32_t it = 0;
-            for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-                int mb, nb;
-                tile_coords(tile, p.m_blocks, p.n_blocks, mb, nb);
-                for (int kt = 0; kt < nk; ++kt, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1u;
-                    if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort_flag, p.status)) goto producer_done;
-                    uint8_t* st = tiles + (size_t)s * kStageBytes;
-                    tc::mbar_arrive_expect_tx(&sh->full[s], kStageBytes);
-                    const int k0 = kt * kBK;
-                    tc::tma_load_2d(st, &p.tmE, &sh->full[s], mb * kBM, k0);
-                    tc::tma_load_2d(st + 8192, &p.tmE, &sh->full[s], mb * kBM + 64, k0);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        tc::tma_load_2d(st + kAStage + q * 8192, &p.tmA, &sh->full[s], nb * kBN + 64 * q, k0);
-                }
-            }
-        producer_done:
-            for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j)
-                tc::mbar_wait_drain(&sh->full[j % kStages], (j / kStages) & 1u);
-        }
-    } else if (!skip && warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t it = 0, lt = 0;
-            for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++lt) {
-                const uint32_t a = lt & 1u, aph = (lt >> 1) & 1u;
-                if (!tc::mbar_wait(&sh->acc_empty[a], aph ^ 1u, abort_flag, p.status)) break;
-                tc::tc_fence_after();
-                const uint32_t d_tmem = tmem + a * kAccCols;
-                bool ok = true;
-                for (int kt = 0; kt < nk; ++kt, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1u;
-                    if (!tc::mbar_wait(&sh->scaled[s], ph, abort_flag, p.status)) { ok = false; break; }
-                    tc::tc_fence_after();
-                    const uint32_t sa = tc::smem_u32(tiles + (size_t)s * kStageBytes);
-                    const uint32_t sb = sa + kAStage;
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        // 16 contraction rows = two 8-row groups of 1024 bytes
-                        const uint64_t ad = tc::smem_desc(sa + kk * 2048, 8192, 1024, tc::SW_128B);
-                        const uint64_t bd = tc::smem_desc(sb + kk * 2048, 8192, 1024, tc::SW_128B);
-                        tc::mma_bf16(d_tmem, ad, bd, kIdescSum, (kt | kk) != 0);
-                    }
-                    tc::mma_commit(&sh->empty[s]);
-                }
-                if (!ok) break;
-                tc::mma_commit(&sh->acc_full[a]);
-            }
-        }
-    } else if (!skip && warp >= 2 && warp < 6) {
-        // ------------------------------------------------ clip-factor rescale
-        const int t = threadIdx.x - 64;
-        // 1024 chunks of 16 bytes per stage; chunk q = t + 128 r holds 8 columns of
-        // row (q / 8) % 64 = t / 8 + 16 (r % 4).  The row scales of a K tile are
-        // fetched one stage ahead, so their latency hides behind the TMA wait.
-        auto row_scales = [&](int kt, float (&cr)[4]) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                // K < 2^31 rows, so the record index fits 32-bit arithmetic
-                const uint32_t k = (uint32_t)kt * kBK + (uint32_t)(t >> 3) + 16u * i;
-                cr[i] = (k < (uint32_t)p.K) ? __ldg(p.c + k / (uint32_t)p.T) : 0.f;
-            }
-        };
-        float cnext[4];
-        row_scales(0, cnext);
-        uint32_t it = 0;
-        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-            for (int kt = 0; kt < nk; ++kt, ++it) {
-                const int s = it % kStages;
-                const uint32_t ph = (it / kStages) & 1u;
-                float crow[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) crow[i] = cnext[i];
-                row_scales(kt + 1 < nk ? kt + 1 : 0, cnext);
-                if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) goto scale_done;
-                uint8_t* st = tiles + (size_t)s * kStageBytes;
-                const bool all_one = crow[0] == 1.0f && crow[1] == 1.0f && crow[2] == 1.0f && crow[3] == 1.0f;
-                if (!all_one) {
-                    uint4 v[8];
-#pragma unroll
-                    for (int r = 0; r < 8; ++r)
-                        v[r] = *reinterpret_cast<const uint4*>(st + (size_t)(t + 128 * r) * 16);
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        const float cr = crow[r & 3];
-                        v[r].x = scale_bf16x2(v[r].x, cr);
-                        v[r].y = scale_bf16x2(v[r].y, cr);
-                        v[r].z = scale_bf16x2(v[r].z, cr);
-                        v[r].w = scale_bf16x2(v[r].w, cr);
-                    }
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) *reinterpret_cast<uint4*>(st + (size_t)(t + 128 * r) * 16) = v[r];
-                    tc::fence_proxy_async_smem();
-                }
-                tc::mbar_arrive(&sh->scaled[s]);
-            }
-        }
-    scale_done:;
-    } else if (!skip && warp >= 6) {
-        // ------------------------------------------------ epilogue
-        const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
-        const int row = quarter * 32 + lane;
-        uint32_t lt = 0;
-        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++lt) {
-            int mb, nb;
-            tile_coords(tile, p.m_blocks, p.n_blocks, mb, nb);
-            const uint32_t a = lt & 1u, aph = (lt >> 1) & 1u;
-            if (!tc::mbar_wait(&sh->acc_full[a], aph, abort_flag, p.status)) break;
-            tc::tc_fence_after();
-            const int64_t m = (int64_t)mb * kBM + row;
-            const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + a * kAccCols;
-            for (int ch = 0; ch < kBN / 32; ++ch) {
-                float v[32];
-                float h[16];
-                tc::tmem_ld16(tbase + ch * 32, h);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = h[j];
-                tc::tmem_ld16(tbase + ch * 32 + 16, h);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) v[16 + j] = h[j];
-                const int64_t n = (int64_t)nb * kBN + ch * 32;
-                if (m >= p.d_out || n >= p.d_in) continue;
-                float z[32];
-                noise32(p.seed, p.step, (uint64_t)(p.coord_off + m * p.d_in + n), z);
-                float* out = p.G + m * p.d_in + n;
-                if (n + 32 <= p.d_in) {
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        float4 o;
-                        o.x = (v[j] + p.scale * z[j]) / p.L;
-                        o.y = (v[j + 1] + p.scale * z[j + 1]) / p.L;
-                        o.z = (v[j + 2] + p.scale * z[j + 2]) / p.L;
-                        o.w = (v[j + 3] + p.scale * z[j + 3]) / p.L;
-                        *reinterpret_cast<float4*>(out + j) = o;
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (n + j < p.d_in) out[j] = (v[j] + p.scale * z[j]) / p.L;
-                }
-            }
-            tc::tc_fence_before();
-            tc::mbar_arrive(&sh->acc_empty[a]);
-        }
-    }
-
-    if (!skip && warp == 1 && lane == 0) {
-        tc::mma_commit(&sh->drain);
-        tc::mbar_wait_drain(&sh->drain, 0);
-    }
-    tc::tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, 2 * kAccCols);
-    }
-}
-
 // ============================================== clipped sum, per-record fold
-// When every record spans whole 64-row K tiles (T % 64 == 0), the tensor
-// cores accumulate each record's unscaled partial P_i = E_i^T A_i in TMEM
-// (two buffers) and the epilogue warps fold S += c_i * P_i in fp32
-// registers: the clip factor is applied exactly, without rounding the
-// scaled operand back to bf16 and without a shared-memory rescale pass.
-// Warps 2-9: two per TMEM lane quarter, each owning 128 of the 256 columns.
-constexpr int kFoldThreads = 320;
+// Requires T % 64 == 0 (every record spans whole 64-row K tiles) or a single
+// record (B = K / T = 1; a partial last K tile is zero-filled by TMA).  The
+// tensor cores accumulate each record's unscaled partial P_i = E_i^T A_i in
+// TMEM (two buffers) and the epilogue warps fold S += c_i * P_i in fp32
+// registers: the clip factor is applied exactly, without rounding a scaled
+// operand back to bf16.  Warps 2-17: four per TMEM lane quarter, each owning
+// 64 of the 256 columns (sixteen epilogue warps keep enough chains in flight
+// for the Philox / Box-Muller epilogue).
+constexpr int kEpiWarps = 16;
+constexpr int kColsPerWarp = kBN / (kEpiWarps / 4);
+constexpr int kFoldThreads = 32 * (2 + kEpiWarps);
 
 struct FoldSmem {
     uint64_t full[kStages];
@@ -314,21 +84,13 @@ struct FoldSmem {
     int abort_flag;
 };
 
-// z for 16 consecutive coordinates starting at kb
-__device__ __forceinline__ void noise16(uint64_t seed, uint64_t step, uint64_t kb, float (&z)[16]) {
+// z for 8 consecutive coordinates starting at kb
+__device__ __forceinline__ void noise8(uint64_t seed, uint64_t step, uint64_t kb, float (&z)[8]) {
     if ((kb & 3u) == 0) {
-        const uint64_t j0 = kb >> 2;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 v = noise4(seed, step, j0 + q);
-            z[4 * q] = v.x;
-            z[4 * q + 1] = v.y;
-            z[4 * q + 2] = v.z;
-            z[4 * q + 3] = v.w;
-        }
+        noise_blocks<2>(seed, step, kb >> 2, z);
     } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) z[j] = noise_at(seed, step, kb + j);
+        for (int j = 0; j < 8; ++j) z[j] = noise_at(seed, step, kb + j);
     }
 }
 
@@ -338,7 +100,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
     FoldSmem* sh = reinterpret_cast<FoldSmem*>(tiles + (size_t)kStages * kStageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ntiles = p.m_blocks * p.n_blocks;
-    const int kpr = (int)(p.T / kBK);              // K tiles per record
+    const int kpr = (int)((p.T + kBK - 1) / kBK);  // K tiles per record (zero-filled past K)
     const int64_t B = p.K / p.T;
     volatile int* abort_flag = &sh->abort_flag;
 
@@ -349,7 +111,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&sh->p_full[b], 1);
-            tc::mbar_init(&sh->p_empty[b], 256);
+            tc::mbar_init(&sh->p_empty[b], 32 * kEpiWarps);
         }
         tc::mbar_init(&sh->drain, 1);
         sh->abort_flag = 0;
@@ -422,24 +184,73 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
         }
     } else if (!skip && warp >= 2) {
         const int quarter = warp & 3;
-        const int half = (warp - 2) >> 2;          // columns half*128 .. +127
+        const int part = (warp - 2) >> 2;          // columns part*64 .. +63
         const int row = quarter * 32 + lane;
         uint32_t rc = 0;
-        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        for (int tile = blockIdx.x; tile < ntiles && B == 1; tile += gridDim.x, ++rc) {
+            // one record: the noise does not depend on the sum, so it is drawn
+            // while the tensor cores are still accumulating this tile
             int mb, nb;
             tile_coords(tile, p.m_blocks, p.n_blocks, mb, nb);
-            float S[128];
+            const int64_t m = (int64_t)mb * kBM + row;
+            const int64_t n0 = (int64_t)nb * kBN + part * kColsPerWarp;
+            float z[kColsPerWarp];
+            if (m < p.d_out) {
 #pragma unroll
-            for (int j = 0; j < 128; ++j) S[j] = 0.f;
+                for (int ch = 0; ch < kColsPerWarp / 8; ++ch) {
+                    float zc[8];
+                    noise8(p.seed, p.step, (uint64_t)(p.coord_off + m * p.d_in + n0 + ch * 8), zc);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) z[ch * 8 + j] = zc[j];
+                }
+            }
+            const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
+            if (!tc::mbar_wait(&sh->p_full[b], bph, abort_flag, p.status)) break;
+            tc::tc_fence_after();
+            const float c0 = __ldg(p.c);
+            const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + part * kColsPerWarp;
+            float* out = p.G + m * p.d_in + n0;
+#pragma unroll
+            for (int ch = 0; ch < kColsPerWarp / 16; ++ch) {
+                float v[16];
+                tc::tmem_ld16(tb + ch * 16, v);
+                if (m >= p.d_out) continue;
+                const int64_t n = n0 + ch * 16;
+                if (n + 16 <= p.d_in) {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) {
+                        float4 o;
+                        o.x = (c0 * v[j] + p.scale * z[ch * 16 + j]) * p.inv_L;
+                        o.y = (c0 * v[j + 1] + p.scale * z[ch * 16 + j + 1]) * p.inv_L;
+                        o.z = (c0 * v[j + 2] + p.scale * z[ch * 16 + j + 2]) * p.inv_L;
+                        o.w = (c0 * v[j + 3] + p.scale * z[ch * 16 + j + 3]) * p.inv_L;
+                        *reinterpret_cast<float4*>(out + ch * 16 + j) = o;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (n + j < p.d_in) out[ch * 16 + j] = (c0 * v[j] + p.scale * z[ch * 16 + j]) * p.inv_L;
+                }
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&sh->p_empty[b]);
+        }
+        for (int tile = blockIdx.x; tile < ntiles && B > 1; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, p.m_blocks, p.n_blocks, mb, nb);
+            float S[kColsPerWarp];
+#pragma unroll
+            for (int j = 0; j < kColsPerWarp; ++j) S[j] = 0.f;
             bool ok = true;
             for (int64_t i = 0; i < B; ++i, ++rc) {
                 const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
                 if (!tc::mbar_wait(&sh->p_full[b], bph, abort_flag, p.status)) { ok = false; break; }
                 tc::tc_fence_after();
                 const float ci = __ldg(p.c + i);
-                const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + half * 128;
+                const uint32_t tb =
+                    tmem + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + part * kColsPerWarp;
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
+                for (int ch = 0; ch < kColsPerWarp / 16; ++ch) {
                     float v[16];
                     tc::tmem_ld16(tb + ch * 16, v);
 #pragma unroll
@@ -452,26 +263,26 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
             const int64_t m = (int64_t)mb * kBM + row;
             if (m < p.d_out) {
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const int64_t n = (int64_t)nb * kBN + half * 128 + ch * 16;
+                for (int ch = 0; ch < kColsPerWarp / 8; ++ch) {
+                    const int64_t n = (int64_t)nb * kBN + part * kColsPerWarp + ch * 8;
                     if (n >= p.d_in) continue;
-                    float z[16];
-                    noise16(p.seed, p.step, (uint64_t)(p.coord_off + m * p.d_in + n), z);
+                    float z[8];
+                    noise8(p.seed, p.step, (uint64_t)(p.coord_off + m * p.d_in + n), z);
                     float* out = p.G + m * p.d_in + n;
-                    if (n + 16 <= p.d_in) {
+                    if (n + 8 <= p.d_in) {
 #pragma unroll
-                        for (int j = 0; j < 16; j += 4) {
+                        for (int j = 0; j < 8; j += 4) {
                             float4 o;
-                            o.x = (S[ch * 16 + j] + p.scale * z[j]) / p.L;
-                            o.y = (S[ch * 16 + j + 1] + p.scale * z[j + 1]) / p.L;
-                            o.z = (S[ch * 16 + j + 2] + p.scale * z[j + 2]) / p.L;
-                            o.w = (S[ch * 16 + j + 3] + p.scale * z[j + 3]) / p.L;
+                            o.x = (S[ch * 8 + j] + p.scale * z[j]) * p.inv_L;
+                            o.y = (S[ch * 8 + j + 1] + p.scale * z[j + 1]) * p.inv_L;
+                            o.z = (S[ch * 8 + j + 2] + p.scale * z[j + 2]) * p.inv_L;
+                            o.w = (S[ch * 8 + j + 3] + p.scale * z[j + 3]) * p.inv_L;
                             *reinterpret_cast<float4*>(out + j) = o;
                         }
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            if (n + j < p.d_in) out[j] = (S[ch * 16 + j] + p.scale * z[j]) / p.L;
+                        for (int j = 0; j < 8; ++j)
+                            if (n + j < p.d_in) out[j] = (S[ch * 8 + j] + p.scale * z[j]) * p.inv_L;
                     }
                 }
             }
@@ -560,7 +371,6 @@ cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* s
                                   cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(k_clipped_sum_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSumSmem);
         cudaFuncSetAttribute(k_clipped_sum_fold_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSumSmem);
         attr = true;
     }
@@ -585,15 +395,12 @@ cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* s
     p.G = t.G;
     p.coord_off = t.coord_off;
     p.scale = sc.sigma * sc.C;
-    p.L = sc.L;
+    p.inv_L = 1.0f / sc.L;
     p.seed = sc.seed;
     p.step = sc.step;
     const int ntiles = p.m_blocks * p.n_blocks;
     const int grid = ntiles < sm_count_cached() ? ntiles : sm_count_cached();
-    if (t.T % kBK == 0)
-        k_clipped_sum_fold_tc<<<grid, kFoldThreads, kSumSmem, s>>>(p);
-    else
-        k_clipped_sum_tc<<<grid, kThreads, kSumSmem, s>>>(p);
+    k_clipped_sum_fold_tc<<<grid, kFoldThreads, kSumSmem, s>>>(p);
     count_launches(1);
     return cudaGetLastError();
 }
