@@ -366,10 +366,10 @@ def run_ours(args, w):
     ghost_T = [ly.T for ly in w.layers if dp.dp_choose_path(ly.T, ly.d_in, ly.d_out) == dp.DP_PATH_GHOST]
     if phase == "norm":
         kernel_name = ("k_ghost_gram_tc" if roof["bound"] == "tensor"
-                       else "k_norm_t1" if ghost_T and all(t == 1 for t in ghost_T) else "k_mat_skinny_tc")
+                       else "k_norm_t1_group" if ghost_T and all(t == 1 for t in ghost_T) else "k_mat_skinny_tc")
     else:
         kernel_name = ("k_grad_wsum" if roof["bound"] == "hbm"
-                       else "k_clipped_sum_fold_tc" if all(t % 64 == 0 for t in ghost_T) else "k_clipped_sum_tc")
+                       else "k_clipped_sum_fold_tc")
     roof["traffic"] = kernel_traffic(f"{kernel_name}@{w.name}")
     roof["kernel"] = kernel_name
     roof["phase"] = phase

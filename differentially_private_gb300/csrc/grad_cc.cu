@@ -288,12 +288,14 @@ __global__ void k_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int6
 
 cudaError_t launch_clip(const ClipParams& p, float* n2, float* c, float* n2_user, float* c_user,
                         unsigned* status, cudaStream_t s) {
-    const int threads = 256;
-    (void)threads;
+    // one thread per flat slot up to kClipThreads (a record with few slots
+    // gets a small block); the block size depends on the shapes only
+    int threads = 32;
+    while (threads < kClipThreads && threads < p.total_slots) threads *= 2;
     const size_t smem = (size_t)(2 * p.nlayers + 1) * sizeof(int64_t);
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(k_clip, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k_clip<<<(unsigned)p.B, kClipThreads, smem, s>>>(p, n2, c, n2_user, c_user, status);
+    k_clip<<<(unsigned)p.B, threads, smem, s>>>(p, n2, c, n2_user, c_user, status);
     count_launches(1);
     return cudaGetLastError();
 }

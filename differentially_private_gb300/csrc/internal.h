@@ -78,6 +78,7 @@ struct ClipParams {
     int64_t B;
     float C;
     const LayerSlots* table;   // device array of nlayers entries, registration order
+    int64_t total_slots;       // sum of the layers' slot counts (sizes the clip blocks)
 };
 
 // ---- every kernel launch of the library is counted here (dp_kernel_launches)
@@ -91,6 +92,9 @@ int nslots_cc(int kernel, int64_t T, int64_t d_in, int64_t d_out);
 
 // ---- launchers; each returns the cudaGetLastError() of its launches
 cudaError_t launch_norm_t1(const NormTask& t, int64_t B, cudaStream_t s);
+// several bf16 T == 1 layers with 16-byte rows in one launch (same result per record as launch_norm_t1)
+bool t1_groupable(const NormTask& t);
+cudaError_t launch_norm_t1_group(const NormTask* tasks, int n, int64_t B, cudaStream_t s);
 cudaError_t launch_norm_ghost_cc(const NormTask& t, int64_t B, cudaStream_t s);
 cudaError_t launch_norm_mat_cc(const NormTask& t, int64_t B, cudaStream_t s);
 cudaError_t launch_layer_sqnorm(const float* partial, int nslots, int64_t B, float* out, cudaStream_t s);

@@ -24,6 +24,58 @@ namespace {
 constexpr int kGT = 32;   // Gram / gradient tile edge
 
 // ------------------------------------------------------------------ T == 1
+// Sum of squares of one row read as 16-byte vectors by a warp: lane l takes
+// vectors l, l + 32, ... in that order (four loads in flight per lane).
+template <typename T>
+__device__ __forceinline__ float sumsq_vec(const uint4* __restrict__ p, int64_t n4, int lane) {
+    constexpr int PER = 16 / (int)sizeof(T);
+    float s = 0.f;
+    int64_t k = lane;
+    for (; k + 96 < n4; k += 128) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = __ldg(p + k + 32 * u);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const T* x = (const T*)&v[u];
+#pragma unroll
+            for (int q = 0; q < PER; ++q) { const float f = (float)x[q]; s = fmaf(f, f, s); }
+        }
+    }
+    for (; k < n4; k += 32) {
+        const uint4 v = __ldg(p + k);
+        const T* x = (const T*)&v;
+#pragma unroll
+        for (int q = 0; q < PER; ++q) { const float f = (float)x[q]; s = fmaf(f, f, s); }
+    }
+    return s;
+}
+
+// Several T == 1 layers in one launch (bf16, rows of whole 16-byte vectors):
+// blockIdx.y selects the layer, one warp per record.
+struct T1Group {
+    int n;
+    int64_t B;
+    struct {
+        const void* A;
+        const void* E;
+        int64_t d_in, d_out;
+        int has_bias;
+        float* partial;
+    } L[kMaxGroup];
+};
+
+__global__ void __launch_bounds__(256) k_norm_t1_group(const T1Group g) {
+    using T = __nv_bfloat16;
+    const auto& ly = g.L[blockIdx.y];
+    const int64_t rec = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (rec >= g.B) return;
+    const float sa = warp_sum(sumsq_vec<T>((const uint4*)ly.A + rec * (ly.d_in / 8), ly.d_in / 8, lane));
+    const float se = warp_sum(sumsq_vec<T>((const uint4*)ly.E + rec * (ly.d_out / 8), ly.d_out / 8, lane));
+    if (lane == 0) ly.partial[rec] = sa * se + (ly.has_bias ? se : 0.f);
+}
+
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(256) k_norm_t1(const void* __restrict__ Av, const void* __restrict__ Ev,
                                                  int64_t B, int64_t d_in, int64_t d_out, int has_bias,
@@ -36,23 +88,8 @@ __global__ void __launch_bounds__(256) k_norm_t1(const void* __restrict__ Av, co
     const T* e = (const T*)Ev + rec * d_out;
     float sa = 0.f, se = 0.f;
     if constexpr (VEC) {
-        // 16-byte vectors: 8 bf16 or 4 f32 per load
-        constexpr int PER = 16 / (int)sizeof(T);
-        const uint4* a4 = (const uint4*)a;
-        const uint4* e4 = (const uint4*)e;
-        const int64_t na = d_in / PER, ne = d_out / PER;
-        for (int64_t k = lane; k < na; k += 32) {
-            const uint4 v = __ldg(a4 + k);
-            const T* x = (const T*)&v;
-#pragma unroll
-            for (int q = 0; q < PER; ++q) { const float f = (float)x[q]; sa = fmaf(f, f, sa); }
-        }
-        for (int64_t k = lane; k < ne; k += 32) {
-            const uint4 v = __ldg(e4 + k);
-            const T* x = (const T*)&v;
-#pragma unroll
-            for (int q = 0; q < PER; ++q) { const float f = (float)x[q]; se = fmaf(f, f, se); }
-        }
+        sa = sumsq_vec<T>((const uint4*)a, d_in / (16 / (int)sizeof(T)), lane);
+        se = sumsq_vec<T>((const uint4*)e, d_out / (16 / (int)sizeof(T)), lane);
     } else {
         for (int64_t k = lane; k < d_in; k += 32) { const float f = Elem<DT>::ld(a + k); sa = fmaf(f, f, sa); }
         for (int64_t k = lane; k < d_out; k += 32) { const float f = Elem<DT>::ld(e + k); se = fmaf(f, f, se); }
@@ -224,6 +261,31 @@ cudaError_t launch_norm_t1(const NormTask& t, int64_t B, cudaStream_t s) {
     }
     count_launches(1);
     return cudaGetLastError();
+}
+
+bool t1_groupable(const NormTask& t) { return t.dtype == DT_BF16 && t.d_in % 8 == 0 && t.d_out % 8 == 0; }
+
+cudaError_t launch_norm_t1_group(const NormTask* tasks, int n, int64_t B, cudaStream_t s) {
+    for (int base = 0; base < n; base += kMaxGroup) {
+        T1Group g;
+        g.n = n - base < kMaxGroup ? n - base : kMaxGroup;
+        g.B = B;
+        for (int i = 0; i < g.n; ++i) {
+            const NormTask& t = tasks[base + i];
+            g.L[i].A = t.A;
+            g.L[i].E = t.E;
+            g.L[i].d_in = t.d_in;
+            g.L[i].d_out = t.d_out;
+            g.L[i].has_bias = t.has_bias;
+            g.L[i].partial = t.partial;
+        }
+        const dim3 grid((unsigned)((B * 32 + 255) / 256), (unsigned)g.n);
+        k_norm_t1_group<<<grid, 256, 0, s>>>(g);
+        count_launches(1);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_norm_ghost_cc(const NormTask& t, int64_t B, cudaStream_t s) {

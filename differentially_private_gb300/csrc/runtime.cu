@@ -508,14 +508,21 @@ dp_status dp_norm_accumulate_batch(dp_ctx* ctx, int n, const int* layer_ids, con
         if (st != DP_OK) return st;
     }
     // one grouped launch for every skinny materialized layer, one launch each for the rest
-    std::vector<NormTask> skinny;
+    std::vector<NormTask> skinny, t1;
     for (int i = 0; i < n; ++i) {
+        const NormTask t = make_norm_task(plans[i]);
         if (plans[i].norm_kernel == NK_MAT_TC) {
-            skinny.push_back(make_norm_task(plans[i]));
+            skinny.push_back(t);
+        } else if (plans[i].norm_kernel == NK_T1 && t1_groupable(t)) {
+            t1.push_back(t);
         } else {
             dp_status st = launch_norm(ctx, plans[i]);
             if (st != DP_OK) return st;
         }
+    }
+    if (!t1.empty()) {
+        const cudaError_t e = launch_norm_t1_group(t1.data(), (int)t1.size(), ctx->B, ctx->stream);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "grouped norm kernel launch");
     }
     if (!skinny.empty()) {
         const cudaError_t e = launch_mat_skinny_tc(skinny.data(), (int)skinny.size(), ctx->B, ctx->status, ctx->stream);
@@ -565,6 +572,8 @@ dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnor
     p.B = ctx->B;
     p.C = C;
     p.table = ctx->d_table;
+    p.total_slots = 0;
+    for (const LayerSlots& ls : cur) p.total_slots += ls.nslots;
     const cudaError_t e = launch_clip(p, ctx->n2, ctx->c, total_sqnorm_out, c_out, ctx->status, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "clip kernel launch");
     ctx->C = C;

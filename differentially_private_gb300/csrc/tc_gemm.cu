@@ -31,6 +31,8 @@ constexpr int kAStage = kBM * kBK * 2;  // E tile: 2 boxes of 64 columns x 64 ro
 constexpr int kBStage = kBN * kBK * 2;  // A tile: 4 boxes
 constexpr int kStageBytes = kAStage + kBStage;
 constexpr int kAccCols = kBN;           // fp32 accumulator columns per buffer
+// TMEM allocation (a power of two) holding both accumulator buffers
+constexpr uint32_t kTmemCols = 2 * kAccCols <= 256 ? 256 : 512;
 constexpr uint32_t kIdescSum = tc::idesc_bf16_f32(kBM, kBN, 1, 1);
 constexpr size_t kSumSmem = 1024 + (size_t)kStages * kStageBytes + 256;
 
@@ -119,7 +121,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
         tc::tma_prefetch_desc(&p.tmE);
         tc::tma_prefetch_desc(&p.tmA);
     }
-    if (warp == 1) tc::tmem_alloc(&sh->tmem_base, 2 * kAccCols);
+    if (warp == 1) tc::tmem_alloc(&sh->tmem_base, kTmemCols);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -143,7 +145,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
                     tc::tma_load_2d(st, &p.tmE, &sh->full[s], mb * kBM, k0);
                     tc::tma_load_2d(st + 8192, &p.tmE, &sh->full[s], mb * kBM + 64, k0);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
+                    for (int q = 0; q < kBN / 64; ++q)
                         tc::tma_load_2d(st + kAStage + q * 8192, &p.tmA, &sh->full[s], nb * kBN + 64 * q, k0);
                 }
             }
@@ -297,7 +299,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
     __syncthreads();
     if (warp == 1) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, 2 * kAccCols);
+        tc::tmem_dealloc(tmem, kTmemCols);
     }
 }
 

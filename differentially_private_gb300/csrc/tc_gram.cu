@@ -29,6 +29,7 @@ constexpr int kGBStage = kGN * kGK * 2;   // 32 KB: 256 rows
 constexpr int kGStageBytes = kGAStage + kGBStage;
 constexpr int kGThreads = 192;
 constexpr uint32_t kIdescGram = tc::idesc_bf16_f32(kGM, kGN, 0, 0);
+constexpr uint32_t kIdescGramHalf = tc::idesc_bf16_f32(kGM, kGN / 2, 0, 0);
 constexpr size_t kGramSmem = 1024 + (size_t)kGStages * kGStageBytes + 256;
 
 struct GramParams {
@@ -103,6 +104,9 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
                 const int rec = item / p.tiles_per_rec;
                 int pb, qb;
                 gram_tile(item % p.tiles_per_rec, p.np, p.nq, pb, qb);
+                // the left 128 columns of the tile lie below the diagonal when p = 2q + 1:
+                // they are neither loaded nor multiplied
+                const bool left = pb <= 2 * qb;
                 for (int kt = 0; kt < nkA + nkE; ++kt, ++it) {
                     const int s = it % kGStages;
                     const uint32_t ph = (it / kGStages) & 1u;
@@ -110,9 +114,9 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
                     uint8_t* st = tiles + (size_t)s * kGStageBytes;
                     const CUtensorMap* tm = kt < nkA ? &p.tmA : &p.tmE;
                     const int k0 = (kt < nkA ? kt : kt - nkA) * kGK;
-                    tc::mbar_arrive_expect_tx(&sh->full[s], kGStageBytes);
+                    tc::mbar_arrive_expect_tx(&sh->full[s], left ? kGStageBytes : kGStageBytes - kGAStage);
                     tc::tma_load_3d(st, tm, &sh->full[s], k0, pb * kGM, rec);
-                    tc::tma_load_3d(st + kGAStage, tm, &sh->full[s], k0, qb * kGN, rec);
+                    if (left) tc::tma_load_3d(st + kGAStage, tm, &sh->full[s], k0, qb * kGN, rec);
                     tc::tma_load_3d(st + kGAStage + kGAStage, tm, &sh->full[s], k0, qb * kGN + 128, rec);
                 }
             }
@@ -124,6 +128,13 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
         if (lane == 0) {
             uint32_t it = 0, lt = 0;
             for (int item = blockIdx.x; item < p.total_items; item += gridDim.x, ++lt) {
+                int pb, qb;
+                gram_tile(item % p.tiles_per_rec, p.np, p.nq, pb, qb);
+                const bool left = pb <= 2 * qb;
+                // full tile: N = 256 from the first B row; right half only: N = 128 from row 128
+                const uint32_t idesc = left ? kIdescGram : kIdescGramHalf;
+                const uint32_t boff = left ? 0u : (uint32_t)kGAStage;
+                const uint32_t coff = left ? 0u : 128u;
                 if (!tc::mbar_wait(&sh->acc_empty, (lt & 1u) ^ 1u, abort_flag, p.status)) break;
                 tc::tc_fence_after();
                 bool ok = true;
@@ -133,16 +144,16 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
                     if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) { ok = false; break; }
                     tc::tc_fence_after();
                     const uint32_t sa = tc::smem_u32(tiles + (size_t)s * kGStageBytes);
-                    const uint32_t sb = sa + kGAStage;
+                    const uint32_t sb = sa + kGAStage + boff;
                     const bool phaseA = kt < nkA;
-                    const uint32_t d_tmem = tmem + (phaseA ? 0u : 256u);
+                    const uint32_t d_tmem = tmem + (phaseA ? 0u : 256u) + coff;
                     const int kl = phaseA ? kt : kt - nkA;
 #pragma unroll
                     for (int kk = 0; kk < kGK / 16; ++kk) {
                         // K-major, 128B swizzle: 16 features = 32 bytes inside the swizzle row
                         const uint64_t ad = tc::smem_desc(sa + kk * 32, 16, 1024, tc::SW_128B);
                         const uint64_t bd = tc::smem_desc(sb + kk * 32, 16, 1024, tc::SW_128B);
-                        tc::mma_bf16(d_tmem, ad, bd, kIdescGram, (kl | kk) != 0);
+                        tc::mma_bf16(d_tmem, ad, bd, idesc, (kl | kk) != 0);
                     }
                     tc::mma_commit(&sh->empty[s]);
                 }
