@@ -141,6 +141,16 @@ __device__ __forceinline__ float noise_at(uint64_t seed, uint64_t step, uint64_t
     return (lane & 1) ? p.y : p.x;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the kernel before it on the stream is still
+// running.  grid_dep_wait() returns once that kernel has completed and its
+// writes are visible (a no-op after a normal launch); nothing the previous
+// kernels wrote may be read before it.  grid_dep_trigger() lets the next
+// kernel of the stream begin launching; it is issued only after the wait, so
+// a kernel that starts early can never overtake the kernel two places ahead.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ bool status_bad(const unsigned* status) {
     return (*(volatile const unsigned*)status) != 0u;
 }

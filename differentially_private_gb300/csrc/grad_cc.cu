@@ -11,47 +11,60 @@
 // Gaussian Noise Addition"; "Sensitivity Inflation from Cross-Record
 // Precision Routing in Private Quantized Fine-Tuning", Eq. 2 and Eq. 3.)
 #include "common.cuh"
+#include "launch.cuh"
 
 using namespace dpk;
 
 namespace {
 
 // --------------------------------------------------------------- clipping
-// One block per record.  The record's partial slots of all layers, in
-// registration order, form one flat index space; thread t sums flat slots
-// t, t + blockDim, ... (so every load of the record is in flight at once),
-// then a fixed-order block reduction combines the threads.  The order
-// depends only on the slot counts, never on B or on other records.
-constexpr int kClipThreads = 512;
+// The partial slots of a record, all layers in registration order, form one
+// flat index space of total_slots entries; slot j of record i lives at
+// slots[j].base[i * slots[j].stride] (a table the host builds once per layer
+// set).  A group of G threads serves one record: thread t sums slots t,
+// t + G, t + 2G, ... in ascending order, kClipLoads loads in flight at a
+// time, then a fixed-order butterfly (G = 32, a warp per record) or block
+// reduction (G = blockDim) combines the threads.  G depends on total_slots
+// only, never on B, so a record's norm does not depend on the batch.
+constexpr int kClipLoads = 8;
+constexpr int kClipMaxThreads = 512;
+constexpr int kClipWarpBlock = 256;   // warp-per-record mode: 8 records per block
 
-__global__ void __launch_bounds__(kClipThreads) k_clip(const ClipParams p, float* __restrict__ n2_out,
-                                                       float* __restrict__ c_out, float* __restrict__ n2_user,
-                                                       float* __restrict__ c_user, unsigned* __restrict__ status) {
-    extern __shared__ int64_t clip_smem[];
-    int64_t* pref = clip_smem;                                            // [nlayers + 1] first flat slot
-    const float** base = reinterpret_cast<const float**>(clip_smem + p.nlayers + 1);  // [nlayers]
+template <bool kWarpPerRecord>
+__global__ void __launch_bounds__(kClipMaxThreads) k_clip(const ClipParams p, float* __restrict__ n2_out,
+                                                          float* __restrict__ c_out, float* __restrict__ n2_user,
+                                                          float* __restrict__ c_user, unsigned* __restrict__ status) {
     __shared__ float red[32];
-    const int64_t rec = blockIdx.x;
-    for (int l = threadIdx.x; l < p.nlayers; l += blockDim.x) {
-        const LayerSlots ls = p.table[l];
-        base[l] = ls.partial + rec * ls.nslots;
-        pref[l + 1] = ls.nslots;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        pref[0] = 0;
-        for (int l = 0; l < p.nlayers; ++l) pref[l + 1] += pref[l];
-    }
-    __syncthreads();
-    const int64_t total = pref[p.nlayers];
+    grid_dep_wait();
+    grid_dep_trigger();
+    const int64_t rec = kWarpPerRecord ? (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)
+                                       : (int64_t)blockIdx.x;
+    const int t = kWarpPerRecord ? (int)(threadIdx.x & 31) : (int)threadIdx.x;
+    const int G = kWarpPerRecord ? 32 : (int)blockDim.x;
     float s = 0.f;
-    int l = 0;
-    for (int64_t j = threadIdx.x; j < total; j += blockDim.x) {
-        while (pref[l + 1] <= j) ++l;
-        s += base[l][j - pref[l]];
+    if (rec < p.B) {   // uniform per warp in warp mode; always true in block mode
+        for (int64_t j0 = t; j0 < p.total_slots; j0 += (int64_t)G * kClipLoads) {
+            float v[kClipLoads];
+#pragma unroll
+            for (int u = 0; u < kClipLoads; ++u) {
+                const int64_t j = j0 + (int64_t)u * G;
+                v[u] = 0.f;
+                if (j < p.total_slots) {
+                    const SlotRef r = p.slots[j];
+                    v[u] = __ldcg(r.base + rec * r.stride);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kClipLoads; ++u) s += v[u];
+        }
     }
-    s = block_sum(s, red);
-    if (threadIdx.x == 0) {
+    if (kWarpPerRecord) {
+        if (rec >= p.B) return;
+        s = warp_sum(s);
+    } else {
+        s = block_sum(s, red);
+    }
+    if (t == 0) {
         float c;
         if (!isfinite(s)) {
             atomicOr(status, 1u);
@@ -79,16 +92,20 @@ struct WsumParams {
 // in ascending order.
 __global__ void __launch_bounds__(256) k_grad_wsum(const WsumParams P, const float* __restrict__ c,
                                                    const unsigned* __restrict__ status, StepScalars sc) {
-    if (status_bad(status)) return;
     const GradTask& t = P.t[blockIdx.y];
     const int64_t ncl = t.d_out * t.d_in + (t.has_bias ? t.d_out : 0);
     const int64_t j0 = t.coord_off >> 2;
     const int64_t j_last = (t.coord_off + ncl - 1) >> 2;
     const float scale = sc.sigma * sc.C;
     const bool vec = ((t.coord_off | ncl) & 3) == 0;   // Philox blocks = aligned float4 of G and g_i
-    for (int64_t j = j0 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j <= j_last;
-         j += (int64_t)gridDim.x * blockDim.x) {
-        const float4 z4 = noise4(sc.seed, sc.step, (uint64_t)j);
+    int64_t j = j0 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    // the first block's noise depends on no earlier kernel: drawn before waiting for them
+    float4 z4 = j <= j_last ? noise4(sc.seed, sc.step, (uint64_t)j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    grid_dep_wait();
+    grid_dep_trigger();
+    if (status_bad(status)) return;
+    for (bool first = true; j <= j_last; j += (int64_t)gridDim.x * blockDim.x, first = false) {
+        if (!first) z4 = noise4(sc.seed, sc.step, (uint64_t)j);
         if (vec) {
             const int64_t p = 4 * j - t.coord_off;
             const float4* g4 = reinterpret_cast<const float4*>(t.gstore + p);
@@ -101,8 +118,8 @@ __global__ void __launch_bounds__(256) k_grad_wsum(const WsumParams P, const flo
                 float cv[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    v[u] = __ldg(g4 + (i + u) * stride4);
-                    cv[u] = __ldg(c + i + u);
+                    v[u] = __ldcg(g4 + (i + u) * stride4);
+                    cv[u] = __ldcg(c + i + u);
                 }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -113,8 +130,8 @@ __global__ void __launch_bounds__(256) k_grad_wsum(const WsumParams P, const flo
                 }
             }
             for (; i < sc.B; ++i) {
-                const float4 v = __ldg(g4 + i * stride4);
-                const float ci = __ldg(c + i);
+                const float4 v = __ldcg(g4 + i * stride4);
+                const float ci = __ldcg(c + i);
                 acc.x = fmaf(ci, v.x, acc.x);
                 acc.y = fmaf(ci, v.y, acc.y);
                 acc.z = fmaf(ci, v.z, acc.z);
@@ -133,7 +150,7 @@ __global__ void __launch_bounds__(256) k_grad_wsum(const WsumParams P, const flo
                 const int64_t p = 4 * j + q - t.coord_off;
                 if (p < 0 || p >= ncl) continue;
                 float acc = 0.f;
-                for (int64_t i = 0; i < sc.B; ++i) acc = fmaf(c[i], t.gstore[i * ncl + p], acc);
+                for (int64_t i = 0; i < sc.B; ++i) acc = fmaf(__ldcg(c + i), __ldcg(t.gstore + i * ncl + p), acc);
                 t.G[p] = (acc + scale * zz[q]) / sc.L;
             }
         }
@@ -147,6 +164,8 @@ template <int DT>
 __global__ void __launch_bounds__(256) k_grad_gemm_cc(const GradTask t, const float* __restrict__ c,
                                                       const unsigned* __restrict__ status, StepScalars sc) {
     using Tt = typename Elem<DT>::T;
+    grid_dep_wait();
+    grid_dep_trigger();
     if (status_bad(status)) return;
     __shared__ float Es[kBK][kBM];
     __shared__ float As[kBK][kBN];
@@ -167,7 +186,7 @@ __global__ void __launch_bounds__(256) k_grad_gemm_cc(const GradTask t, const fl
             const int64_t k = k0 + kk;
             float e = 0.f, a = 0.f;
             if (k < K) {
-                const float ck = c[k / t.T];
+                const float ck = __ldcg(c + k / t.T);
                 if (m0 + col < t.d_out) e = ck * Elem<DT>::ld(E + k * t.d_out + m0 + col);
                 if (n0 + col < t.d_in) a = Elem<DT>::ld(A + k * t.d_in + n0 + col);
             }
@@ -220,13 +239,15 @@ template <int DT>
 __global__ void __launch_bounds__(256) k_bias_sum(const GradTask t, const float* __restrict__ c,
                                                   const unsigned* __restrict__ status, StepScalars sc) {
     using Tt = typename Elem<DT>::T;
+    grid_dep_wait();
+    grid_dep_trigger();
     if (status_bad(status)) return;
     const int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (m >= t.d_out) return;
     const Tt* E = (const Tt*)t.E;
     const int64_t K = sc.B * t.T;
     float acc = 0.f;
-    for (int64_t k = 0; k < K; ++k) acc = fmaf(c[k / t.T], Elem<DT>::ld(E + k * t.d_out + m), acc);
+    for (int64_t k = 0; k < K; ++k) acc = fmaf(__ldcg(c + k / t.T), Elem<DT>::ld(E + k * t.d_out + m), acc);
     const int64_t p = t.d_out * t.d_in + m;
     t.G[p] = (acc + sc.sigma * sc.C * noise_at(sc.seed, sc.step, (uint64_t)(t.coord_off + p))) / sc.L;
 }
@@ -239,10 +260,12 @@ __global__ void __launch_bounds__(256) k_bias_sum(const GradTask t, const float*
 __global__ void __launch_bounds__(256) k_prescale_rows(const uint4* __restrict__ E, uint4* __restrict__ E2,
                                                        const float* __restrict__ c, int64_t K, int64_t T,
                                                        int64_t d8) {
+    grid_dep_wait();
+    grid_dep_trigger();
     const int64_t n = K * d8;
     for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n; q += (int64_t)gridDim.x * blockDim.x) {
         const int64_t k = q / d8;
-        const float ck = __ldg(c + k / T);
+        const float ck = __ldcg(c + k / T);
         uint4 v = __ldcs(E + q);
         uint32_t* w = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
@@ -288,16 +311,20 @@ __global__ void k_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int6
 
 cudaError_t launch_clip(const ClipParams& p, float* n2, float* c, float* n2_user, float* c_user,
                         unsigned* status, cudaStream_t s) {
-    // one thread per flat slot up to kClipThreads (a record with few slots
-    // gets a small block); the block size depends on the shapes only
-    int threads = 32;
-    while (threads < kClipThreads && threads < p.total_slots) threads *= 2;
-    const size_t smem = (size_t)(2 * p.nlayers + 1) * sizeof(int64_t);
-    if (smem > 48 * 1024)
-        cudaFuncSetAttribute(k_clip, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k_clip<<<(unsigned)p.B, threads, smem, s>>>(p, n2, c, n2_user, c_user, status);
+    // G = smallest power of two with G * kClipLoads >= total_slots, at least
+    // a warp and at most kClipMaxThreads; it depends on the shapes only
+    cudaError_t e;
+    int G = 32;
+    while (G < kClipMaxThreads && (int64_t)G * kClipLoads < p.total_slots) G *= 2;
+    if (G == 32) {
+        const int per_block = kClipWarpBlock / 32;
+        const unsigned grid = (unsigned)((p.B + per_block - 1) / per_block);
+        e = launch_dependent(k_clip<true>, dim3(grid), dim3(kClipWarpBlock), 0, s, p, n2, c, n2_user, c_user, status);
+    } else {
+        e = launch_dependent(k_clip<false>, dim3((unsigned)p.B), dim3(G), 0, s, p, n2, c, n2_user, c_user, status);
+    }
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_grad_wsum(const GradTask* tasks, int n, const float* c, const unsigned* status,
@@ -315,9 +342,9 @@ cudaError_t launch_grad_wsum(const GradTask* tasks, int n, const float* c, const
         }
         int64_t gx = (maxblk + 255) / 256;
         if (gx > 4096) gx = 4096;
-        k_grad_wsum<<<dim3((unsigned)gx, (unsigned)P.n), 256, 0, s>>>(P, c, status, sc);
+        const cudaError_t e = launch_dependent(k_grad_wsum, dim3((unsigned)gx, (unsigned)P.n), dim3(256), 0, s, P, c,
+                                               status, sc);
         count_launches(1);
-        const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -326,19 +353,21 @@ cudaError_t launch_grad_wsum(const GradTask* tasks, int n, const float* c, const
 cudaError_t launch_grad_gemm_cc(const GradTask& t, const float* c, const unsigned* status,
                                 const StepScalars& sc, cudaStream_t s) {
     const dim3 grid((unsigned)((t.d_in + kBN - 1) / kBN), (unsigned)((t.d_out + kBM - 1) / kBM));
-    if (t.dtype == DT_F32) k_grad_gemm_cc<DT_F32><<<grid, 256, 0, s>>>(t, c, status, sc);
-    else k_grad_gemm_cc<DT_BF16><<<grid, 256, 0, s>>>(t, c, status, sc);
+    const cudaError_t e = t.dtype == DT_F32
+                              ? launch_dependent(k_grad_gemm_cc<DT_F32>, grid, dim3(256), 0, s, t, c, status, sc)
+                              : launch_dependent(k_grad_gemm_cc<DT_BF16>, grid, dim3(256), 0, s, t, c, status, sc);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_bias_sum(const GradTask& t, const float* c, const unsigned* status, const StepScalars& sc,
                             cudaStream_t s) {
     const unsigned grid = (unsigned)((t.d_out + 255) / 256);
-    if (t.dtype == DT_F32) k_bias_sum<DT_F32><<<grid, 256, 0, s>>>(t, c, status, sc);
-    else k_bias_sum<DT_BF16><<<grid, 256, 0, s>>>(t, c, status, sc);
+    const cudaError_t e = t.dtype == DT_F32
+                              ? launch_dependent(k_bias_sum<DT_F32>, dim3(grid), dim3(256), 0, s, t, c, status, sc)
+                              : launch_dependent(k_bias_sum<DT_BF16>, dim3(grid), dim3(256), 0, s, t, c, status, sc);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_prescale_rows(const void* E, void* E2, const float* c, int64_t K, int64_t T, int64_t d,
@@ -346,9 +375,10 @@ cudaError_t launch_prescale_rows(const void* E, void* E2, const float* c, int64_
     const int64_t n = K * (d / 8);
     int64_t grid = (n + 255) / 256;
     if (grid > 152 * 16) grid = 152 * 16;
-    k_prescale_rows<<<(unsigned)grid, 256, 0, s>>>((const uint4*)E, (uint4*)E2, c, K, T, d / 8);
+    const cudaError_t e = launch_dependent(k_prescale_rows, dim3((unsigned)grid), dim3(256), 0, s,
+                                           (const uint4*)E, (uint4*)E2, c, K, T, d / 8);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int64_t n,

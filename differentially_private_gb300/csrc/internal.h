@@ -67,18 +67,19 @@ struct StepScalars {
     uint64_t step;
 };
 
-// Where a layer's per-record partial squared norms live ([B][nslots]).
-struct LayerSlots {
-    const float* partial;
-    int64_t nslots;
+// One flat partial-norm slot of every record: record i's value is
+// base[i * stride] (a layer's partials are [B][nslots], so base = the
+// layer's partial array + the slot index and stride = nslots).
+struct SlotRef {
+    const float* base;
+    int64_t stride;
 };
 
 struct ClipParams {
-    int nlayers;
     int64_t B;
     float C;
-    const LayerSlots* table;   // device array of nlayers entries, registration order
-    int64_t total_slots;       // sum of the layers' slot counts (sizes the clip blocks)
+    const SlotRef* slots;      // device array: layers in registration order, each layer's slots in order
+    int64_t total_slots;
 };
 
 // ---- every kernel launch of the library is counted here (dp_kernel_launches)

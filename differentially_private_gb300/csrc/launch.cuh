@@ -1,0 +1,23 @@
+// Host helper: launch a kernel that may start before the previous kernel on
+// the stream has finished (programmatic stream serialization).  The kernel
+// must call dpk::grid_dep_wait() before it reads anything that an earlier
+// launch wrote, and dpk::grid_dep_trigger() only after that wait.
+#pragma once
+
+#include <cuda_runtime.h>
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                    Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}

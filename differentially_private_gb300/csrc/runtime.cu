@@ -11,6 +11,7 @@
 #include <cstring>
 #include <new>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "../../include/dp_clip.h"
@@ -85,9 +86,10 @@ struct dp_ctx {
     size_t ccap = 0;
     unsigned* status = nullptr;
     float* one = nullptr;              // device constant 1.0f
-    LayerSlots* d_table = nullptr;     // clip kernel's view of every layer's partials
-    size_t d_table_cap = 0;
-    std::vector<LayerSlots> h_table;   // what d_table holds
+    SlotRef* d_slots = nullptr;        // clip kernel's flat view of every layer's partial slots
+    size_t d_slots_cap = 0;
+    std::vector<std::pair<const float*, int64_t>> slots_key;   // (partial, nslots) per layer d_slots was built from
+    std::vector<SlotRef> h_slots;      // host copy of d_slots (the source of its last upload)
     std::string err;
 };
 
@@ -405,7 +407,7 @@ dp_status dp_destroy(dp_ctx* ctx) {
     cudaFree(ctx->c);
     cudaFree(ctx->status);
     cudaFree(ctx->one);
-    cudaFree(ctx->d_table);
+    cudaFree(ctx->d_slots);
     delete ctx;
     return DP_OK;
 }
@@ -543,37 +545,39 @@ dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnor
         if (!ctx->layers[l].accumulated)
             return fail(ctx, DP_ERR_STATE, "layer %zu was not accumulated in this step", l);
     DeviceGuard g(ctx->device);
-    std::vector<LayerSlots> cur(ctx->layers.size());
+    std::vector<std::pair<const float*, int64_t>> key(ctx->layers.size());
+    int64_t total = 0;
     for (size_t l = 0; l < ctx->layers.size(); ++l) {
-        cur[l].partial = ctx->layers[l].partial;
-        cur[l].nslots = ctx->layers[l].nslots;
+        key[l] = {ctx->layers[l].partial, (int64_t)ctx->layers[l].nslots};
+        total += ctx->layers[l].nslots;
     }
-    bool same = cur.size() == ctx->h_table.size();
-    for (size_t l = 0; same && l < cur.size(); ++l)
-        same = cur[l].partial == ctx->h_table[l].partial && cur[l].nslots == ctx->h_table[l].nslots;
-    if (!same) {
-        if (ctx->d_table_cap < cur.size()) {
+    if (key != ctx->slots_key) {
+        // the flat slot table changes only when the layer set or its scratch does
+        if (ctx->d_slots_cap < (size_t)total) {
             cudaError_t e = cudaStreamSynchronize(ctx->stream);
             if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamSynchronize");
-            cudaFree(ctx->d_table);
-            ctx->d_table = nullptr;
-            ctx->d_table_cap = 0;
-            e = cudaMalloc(reinterpret_cast<void**>(&ctx->d_table), cur.size() * sizeof(LayerSlots));
-            if (e != cudaSuccess) return fail(ctx, DP_ERR_OOM, "cudaMalloc of the layer table failed");
-            ctx->d_table_cap = cur.size();
+            cudaFree(ctx->d_slots);
+            ctx->d_slots = nullptr;
+            ctx->d_slots_cap = 0;
+            e = cudaMalloc(reinterpret_cast<void**>(&ctx->d_slots), (size_t)total * sizeof(SlotRef));
+            if (e != cudaSuccess) return fail(ctx, DP_ERR_OOM, "cudaMalloc of the slot table failed");
+            ctx->d_slots_cap = (size_t)total;
         }
-        ctx->h_table = cur;
-        const cudaError_t e = cudaMemcpyAsync(ctx->d_table, ctx->h_table.data(), cur.size() * sizeof(LayerSlots),
+        // an upload from pageable memory has been staged when the call returns,
+        // so h_slots can be rebuilt while an earlier upload is still in flight
+        ctx->h_slots.clear();
+        for (const auto& k : key)
+            for (int64_t j = 0; j < k.second; ++j) ctx->h_slots.push_back(SlotRef{k.first + j, k.second});
+        ctx->slots_key = key;
+        const cudaError_t e = cudaMemcpyAsync(ctx->d_slots, ctx->h_slots.data(), (size_t)total * sizeof(SlotRef),
                                               cudaMemcpyHostToDevice, ctx->stream);
-        if (e != cudaSuccess) return cuda_fail(ctx, e, "layer table upload");
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "slot table upload");
     }
     ClipParams p;
-    p.nlayers = (int)ctx->layers.size();
     p.B = ctx->B;
     p.C = C;
-    p.table = ctx->d_table;
-    p.total_slots = 0;
-    for (const LayerSlots& ls : cur) p.total_slots += ls.nslots;
+    p.slots = ctx->d_slots;
+    p.total_slots = total;
     const cudaError_t e = launch_clip(p, ctx->n2, ctx->c, total_sqnorm_out, c_out, ctx->status, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "clip kernel launch");
     ctx->C = C;

@@ -19,6 +19,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "launch.cuh"
 #include "tc_common.cuh"
 
 using namespace dpk;
@@ -126,6 +127,10 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
+    // everything above overlaps the previous kernel; its outputs (c, the
+    // pre-scaled operand, the status word) are read only from here on
+    grid_dep_wait();
+    grid_dep_trigger();
     const bool skip = status_bad(p.status);
 
     if (!skip && warp == 0) {
@@ -209,7 +214,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
             const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
             if (!tc::mbar_wait(&sh->p_full[b], bph, abort_flag, p.status)) break;
             tc::tc_fence_after();
-            const float c0 = __ldg(p.c);
+            const float c0 = __ldcg(p.c);
             const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + part * kColsPerWarp;
             float* out = p.G + m * p.d_in + n0;
 #pragma unroll
@@ -248,7 +253,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
                 const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
                 if (!tc::mbar_wait(&sh->p_full[b], bph, abort_flag, p.status)) { ok = false; break; }
                 tc::tc_fence_after();
-                const float ci = __ldg(p.c + i);
+                const float ci = __ldcg(p.c + i);
                 const uint32_t tb =
                     tmem + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + part * kColsPerWarp;
 #pragma unroll
@@ -402,7 +407,7 @@ cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* s
     p.step = sc.step;
     const int ntiles = p.m_blocks * p.n_blocks;
     const int grid = ntiles < sm_count_cached() ? ntiles : sm_count_cached();
-    k_clipped_sum_fold_tc<<<grid, kFoldThreads, kSumSmem, s>>>(p);
+    const cudaError_t e = launch_dependent(k_clipped_sum_fold_tc, dim3(grid), dim3(kFoldThreads), kSumSmem, s, p);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }

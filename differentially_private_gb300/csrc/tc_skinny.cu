@@ -322,6 +322,34 @@ int sm_count() {
     return n > 0 ? n : 1;
 }
 
+// Largest number of column blocks per item.  Each CTA takes a contiguous
+// range of about items / grid items, so its load is bounded by
+// ceil(items / grid) x (blocks of the largest item + a fixed per-item cost);
+// the cap minimizing that bound is taken (the largest on ties).
+int chunk_cap(const NormTask* tasks, int n, int64_t B, int grid) {
+    constexpr double kItemCost = 0.25;   // per-item overhead in units of one 128-column block
+    int best = kMaxMb;
+    double best_cost = 0.0;
+    for (int cap = kMaxMb; cap >= 1; --cap) {
+        int64_t items = 0;
+        int widest = 1;
+        for (int i = 0; i < n; ++i) {
+            const int64_t D = tasks[i].d_in > tasks[i].d_out ? tasks[i].d_in : tasks[i].d_out;
+            const int mb = (int)((D + kBM - 1) / kBM);
+            const int nch = (mb + cap - 1) / cap;
+            const int w = (mb + nch - 1) / nch;
+            items += B * nch;
+            widest = w > widest ? w : widest;
+        }
+        const double cost = (double)((items + grid - 1) / grid) * (widest + kItemCost);
+        if (cap == kMaxMb || cost < best_cost) {
+            best = cap;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
 }  // namespace
 
 bool tc_skinny_supported(int dtype, int64_t d_in, int64_t d_out, int has_bias) {
@@ -359,9 +387,11 @@ cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsign
         attr = true;
     }
     thread_local SkinnyParams p;   // host staging of the parameter block; each launch copies it
+    const int sms = sm_count();
     for (int base = 0; base < n; base += kMaxSkinnyGroup) {
         p.nlayers = n - base < kMaxSkinnyGroup ? n - base : kMaxSkinnyGroup;
         p.status = status;
+        const int cap = chunk_cap(tasks + base, p.nlayers, B, sms);
         int items = 0;
         for (int i = 0; i < p.nlayers; ++i) {
             const NormTask& t = tasks[base + i];
@@ -372,7 +402,7 @@ cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsign
             L.r = x_is_A ? t.d_out : t.d_in;
             L.T = t.T;
             L.mblocks = (int)((L.D + kBM - 1) / kBM);
-            L.nchunks = (L.mblocks + kMaxMb - 1) / kMaxMb;
+            L.nchunks = (L.mblocks + cap - 1) / cap;
             L.chunk_mb = (L.mblocks + L.nchunks - 1) / L.nchunks;
             L.item_begin = items;
             L.partial = t.partial;
@@ -389,7 +419,6 @@ cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsign
             }
         }
         p.total_items = items;
-        const int sms = sm_count();
         const int grid = items < sms ? items : sms;
         k_mat_skinny_tc<<<grid, kThreads, kSmem, s>>>(p);
         count_launches(1);
