@@ -151,6 +151,13 @@ __device__ __forceinline__ float noise_at(uint64_t seed, uint64_t step, uint64_t
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Loads after grid_dep_wait().  Data another kernel wrote that each address
+// of is read once (partial norms, stored per-example gradients) is loaded
+// with __ldcg (L2 only).  The clip factors c_i are read by every warp of the
+// grid: they are loaded with __ldca (cached in L1 as well), so that each SM
+// fetches a line once instead of every warp sending a request to the same
+// L2 line.
+
 __device__ __forceinline__ bool status_bad(const unsigned* status) {
     return (*(volatile const unsigned*)status) != 0u;
 }

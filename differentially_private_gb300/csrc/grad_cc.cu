@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(256) k_grad_wsum(const WsumParams P, const flo
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     v[u] = __ldcg(g4 + (i + u) * stride4);
-                    cv[u] = __ldcg(c + i + u);
+                    cv[u] = __ldca(c + i + u);
                 }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(256) k_grad_wsum(const WsumParams P, const flo
             }
             for (; i < sc.B; ++i) {
                 const float4 v = __ldcg(g4 + i * stride4);
-                const float ci = __ldcg(c + i);
+                const float ci = __ldca(c + i);
                 acc.x = fmaf(ci, v.x, acc.x);
                 acc.y = fmaf(ci, v.y, acc.y);
                 acc.z = fmaf(ci, v.z, acc.z);
@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(256) k_grad_wsum(const WsumParams P, const flo
                 const int64_t p = 4 * j + q - t.coord_off;
                 if (p < 0 || p >= ncl) continue;
                 float acc = 0.f;
-                for (int64_t i = 0; i < sc.B; ++i) acc = fmaf(__ldcg(c + i), __ldcg(t.gstore + i * ncl + p), acc);
+                for (int64_t i = 0; i < sc.B; ++i) acc = fmaf(__ldca(c + i), __ldcg(t.gstore + i * ncl + p), acc);
                 t.G[p] = (acc + scale * zz[q]) / sc.L;
             }
         }
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(256) k_grad_gemm_cc(const GradTask t, const fl
             const int64_t k = k0 + kk;
             float e = 0.f, a = 0.f;
             if (k < K) {
-                const float ck = __ldcg(c + k / t.T);
+                const float ck = __ldca(c + k / t.T);
                 if (m0 + col < t.d_out) e = ck * Elem<DT>::ld(E + k * t.d_out + m0 + col);
                 if (n0 + col < t.d_in) a = Elem<DT>::ld(A + k * t.d_in + n0 + col);
             }
@@ -247,14 +247,15 @@ __global__ void __launch_bounds__(256) k_bias_sum(const GradTask t, const float*
     const Tt* E = (const Tt*)t.E;
     const int64_t K = sc.B * t.T;
     float acc = 0.f;
-    for (int64_t k = 0; k < K; ++k) acc = fmaf(__ldcg(c + k / t.T), Elem<DT>::ld(E + k * t.d_out + m), acc);
+    for (int64_t k = 0; k < K; ++k) acc = fmaf(__ldca(c + k / t.T), Elem<DT>::ld(E + k * t.d_out + m), acc);
     const int64_t p = t.d_out * t.d_in + m;
     t.G[p] = (acc + sc.sigma * sc.C * noise_at(sc.seed, sc.step, (uint64_t)(t.coord_off + p))) / sc.L;
 }
 
 // ------------------------------------- clip factor folded into the operand
-// E'[k, :] = bf16(c[k / T] * E[k, :]) for the tensor-core clipped sum of
-// layers whose records do not span whole 64-row tiles (T = 1 included).
+// X'[k, :] = bf16(c[k / T] * X[k, :]), X the operand (A or E) with fewer
+// columns, for the tensor-core clipped sum of layers whose records do not
+// span whole 64-row tiles (T = 1 included).
 // One thread per 8 consecutive elements of a row (d % 8 == 0); the product is
 // formed in fp32 and rounded to nearest.
 __global__ void __launch_bounds__(256) k_prescale_rows(const uint4* __restrict__ E, uint4* __restrict__ E2,
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(256) k_prescale_rows(const uint4* __restrict__
     const int64_t n = K * d8;
     for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n; q += (int64_t)gridDim.x * blockDim.x) {
         const int64_t k = q / d8;
-        const float ck = __ldcg(c + k / T);
+        const float ck = __ldca(c + k / T);
         uint4 v = __ldcs(E + q);
         uint32_t* w = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll

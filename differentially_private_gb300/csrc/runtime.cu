@@ -50,8 +50,9 @@ struct Layer {
     size_t gstore_cap = 0;    // floats
     // c_i E_i in bf16 for the tensor-core sum of a layer whose T is not a
     // multiple of 64 (the clip factor folded into the operand before the sum)
-    bool prescale = false;
-    float* escaled = nullptr;
+    bool prescale = false;     // clip factors folded into a bf16 copy of one operand
+    bool prescale_A = false;   // that operand is A (fewer columns than E), else E
+    float* escaled = nullptr;  // the pre-scaled copy
     size_t escaled_cap = 0;   // floats (two bf16 each)
     // TMA descriptors of the tensor-core kernels, encoded once per request
     // shape: reused while (A, E, T, B) stay the same from step to step
@@ -264,17 +265,21 @@ dp_status prepare(dp_ctx* ctx, int id, const void* A, const void* E, int64_t T, 
         }
     }
     plan.prescale = plan.grad_kernel == GK_GEMM_TC && T % 64 != 0;
+    // c_i can scale either operand's rows: the narrower one is copied
+    plan.prescale_A = plan.prescale && plan.d_in < plan.d_out;
     if (plan.prescale) {
-        st = grow(ctx, &ly.escaled, &ly.escaled_cap, ((size_t)ctx->B * T * plan.d_out + 1) / 2);
+        const int64_t dsc = plan.prescale_A ? plan.d_in : plan.d_out;
+        st = grow(ctx, &ly.escaled, &ly.escaled_cap, ((size_t)ctx->B * T * dsc + 1) / 2);
         if (st != DP_OK) return st;
         plan.escaled = ly.escaled;
         plan.escaled_cap = ly.escaled_cap;
     }
     if (plan.grad_kernel == GK_GEMM_TC) {
         // the sum reads the pre-scaled copy as one record of B*T rows when prescaling
-        const void* Esum = plan.prescale ? static_cast<const void*>(plan.escaled) : E;
+        const void* Asum = plan.prescale_A ? static_cast<const void*>(plan.escaled) : A;
+        const void* Esum = plan.prescale && !plan.prescale_A ? static_cast<const void*>(plan.escaled) : E;
         Layer::MapKey key;
-        key.A = A;
+        key.A = Asum;
         key.E = Esum;
         key.T = T;
         key.B = ctx->B;
@@ -282,7 +287,7 @@ dp_status prepare(dp_ctx* ctx, int id, const void* A, const void* E, int64_t T, 
         if (!(key == plan.gkey)) {
             plan.gkey = Layer::MapKey();
             GradTask g{};
-            g.A = A;
+            g.A = Asum;
             g.E = Esum;
             g.T = T;
             g.d_in = plan.d_in;
@@ -621,11 +626,13 @@ dp_status dp_clipped_noisy_grad(dp_ctx* ctx, float sigma, uint64_t seed, uint64_
         }
         cudaError_t e;
         if (ly.grad_kernel == GK_GEMM_TC && ly.prescale) {
-            // c_i folded into a bf16 copy of E, then one "record" of B*T rows with factor 1
+            // c_i folded into a bf16 copy of the narrower operand, then one "record" of B*T rows with factor 1
             const int64_t K = ctx->B * ly.T;
-            e = launch_prescale_rows(ly.E, ly.escaled, ctx->c, K, ly.T, ly.d_out, ctx->stream);
+            e = ly.prescale_A ? launch_prescale_rows(ly.A, ly.escaled, ctx->c, K, ly.T, ly.d_in, ctx->stream)
+                              : launch_prescale_rows(ly.E, ly.escaled, ctx->c, K, ly.T, ly.d_out, ctx->stream);
             GradTask ts = t;
-            ts.E = ly.escaled;
+            if (ly.prescale_A) ts.A = ly.escaled;
+            else ts.E = ly.escaled;
             ts.T = K;
             StepScalars s1 = sc;
             s1.B = 1;

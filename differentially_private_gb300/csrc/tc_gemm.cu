@@ -8,9 +8,10 @@
 //    stochastic gradient descent", phases 3-5; "Sensitivity Inflation from
 //    Cross-Record Precision Routing in Private Quantized Fine-Tuning", Eq. 3).
 //    When T is a multiple of 64 the clip factor is folded per record in fp32
-//    (below).  Otherwise the runtime first writes c_i E_i into scratch
-//    (k_prescale_rows, the clip factor folded into the staged operand) and
-//    runs this kernel as a single "record" of K rows with factor 1.
+//    (below).  Otherwise the runtime first writes c_i A_i or c_i E_i (the
+//    operand with fewer columns) into scratch (k_prescale_rows, the clip
+//    factor folded into the staged operand) and runs this kernel as a single
+//    "record" of K rows with factor 1.
 //
 // Warp roles (one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer (one lane)
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
             const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
             if (!tc::mbar_wait(&sh->p_full[b], bph, abort_flag, p.status)) break;
             tc::tc_fence_after();
-            const float c0 = __ldcg(p.c);
+            const float c0 = __ldca(p.c);
             const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + part * kColsPerWarp;
             float* out = p.G + m * p.d_in + n0;
 #pragma unroll
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
                 const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
                 if (!tc::mbar_wait(&sh->p_full[b], bph, abort_flag, p.status)) { ok = false; break; }
                 tc::tc_fence_after();
-                const float ci = __ldcg(p.c + i);
+                const float ci = __ldca(p.c + i);
                 const uint32_t tb =
                     tmem + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + part * kColsPerWarp;
 #pragma unroll

@@ -52,7 +52,6 @@ struct SkinnyLayer {
     int mblocks;       // 128-column blocks of D
     int nchunks;       // items per record
     int chunk_mb;      // blocks per item (the last item of a record may have fewer)
-    int item_begin;
     float* partial;    // [B][mblocks * 4]
     float* gstore;     // [B][r * D] or nullptr
 };
@@ -61,6 +60,10 @@ struct SkinnyParams {
     int nlayers;
     int total_items;
     unsigned* status;
+    // first item of each layer (+ total): kept apart from the layer records so
+    // that the search for a CTA's first layer reads two cache lines of the
+    // parameter bank, not one line per layer
+    int item_begin[kMaxSkinnyGroup + 1];
     SkinnyLayer L[kMaxSkinnyGroup];
 };
 
@@ -75,25 +78,36 @@ struct Smem {
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
+    int l_first;                             // layer of the CTA's first item
+    int warm[32];                            // sink of the parameter-bank warm-up loads
 };
 
-__device__ __forceinline__ int find_layer(const SkinnyParams& p, int item) {
+// Layer of an item, found by a whole warp: lane i compares item_begin[1 + i],
+// item_begin[33 + i] with the item (parallel parameter-bank reads instead of a
+// chain of dependent ones) and the ballots count the layers starting at or
+// before it.
+static_assert(sizeof(Smem) <= 8192 + 512, "skinny kernel shared-memory budget");
+
+__device__ __forceinline__ int warp_find_layer(const SkinnyParams& p, int item, int lane) {
     int l = 0;
-    while (l + 1 < p.nlayers && p.L[l + 1].item_begin <= item) ++l;
+    for (int base = 1; base < p.nlayers; base += 32) {
+        const int j = base + lane;
+        l += __popc(__ballot_sync(0xffffffffu, j < p.nlayers && p.item_begin[j] <= item));
+    }
     return l;
 }
 
 // items of a CTA increase, so the layer cursor only moves forward
 __device__ __forceinline__ void advance_layer(const SkinnyParams& p, int item, int& l) {
-    while (l + 1 < p.nlayers && p.L[l + 1].item_begin <= item) ++l;
+    while (l + 1 < p.nlayers && p.item_begin[l + 1] <= item) ++l;
 }
 
 struct ItemInfo {
     int rec, mb0, nmb, nk;
 };
 
-__device__ __forceinline__ ItemInfo item_info(const SkinnyLayer& ly, int item) {
-    const int local = item - ly.item_begin;
+__device__ __forceinline__ ItemInfo item_info(const SkinnyLayer& ly, int begin, int item) {
+    const int local = item - begin;
     ItemInfo r;
     r.rec = local / ly.nchunks;
     const int chunk = local % ly.nchunks;
@@ -133,25 +147,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
         tc::fence_barrier_init();
     }
     if (warp == 1) tc::tmem_alloc(&sh->tmem_base, kTmemCols);
+    if (warp == 2) {
+        // while the barriers and TMEM are set up: find the CTA's layers, start
+        // fetching their TMA descriptors and pull their parameter lines into
+        // the constant cache with parallel reads
+        const int lf = item_lo < item_hi ? warp_find_layer(p, item_lo, lane) : 0;
+        const int ll = item_lo < item_hi ? warp_find_layer(p, item_hi - 1, lane) : -1;
+        if (lane == 0) sh->l_first = lf;
+        int acc = 0;
+        for (int l = lf + lane; l <= ll; l += 32) {
+            tc::tma_prefetch_desc(&p.L[l].tmX);
+            tc::tma_prefetch_desc(&p.L[l].tmY);
+            acc += p.L[l].nchunks + p.item_begin[l];
+        }
+        sh->warm[lane] = acc;
+    }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
+    const int l_first = sh->l_first;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             uint32_t it = 0, yit = 0;
-            if (item_lo < item_hi)
-                for (int l = find_layer(p, item_lo); l <= find_layer(p, item_hi - 1); ++l) {
-                    tc::tma_prefetch_desc(&p.L[l].tmX);
-                    tc::tma_prefetch_desc(&p.L[l].tmY);
-                }
-            int cur = find_layer(p, item_lo);
+            int cur = l_first;
             for (int item = item_lo; item < item_hi; ++item) {
                 advance_layer(p, item, cur);
                 const SkinnyLayer& ly = p.L[cur];
-                const ItemInfo in = item_info(ly, item);
+                const ItemInfo in = item_info(ly, p.item_begin[cur], item);
                 for (int kt = 0; kt < in.nk; ++kt) {
                     const int q = yit % kYStages;
                     const uint32_t qph = (yit / kYStages) & 1u;
@@ -182,11 +207,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t it = 0, yit = 0, lt = 0;
-            int cur = find_layer(p, item_lo);
+            int cur = l_first;
             bool ok = true;
             for (int item = item_lo; item < item_hi && ok; ++item, ++lt) {
                 advance_layer(p, item, cur);
-                const ItemInfo in = item_info(p.L[cur], item);
+                const ItemInfo in = item_info(p.L[cur], p.item_begin[cur], item);
                 const uint32_t a = lt % kAccSets, aph = (lt / kAccSets) & 1u;
                 if (!tc::mbar_wait(&sh->acc_empty[a], aph ^ 1u, abort_flag, p.status)) break;
                 tc::tc_fence_after();
@@ -225,11 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
         const int row = quarter * 32 + lane;
         const int ew = warp - 2;
         uint32_t lt = 0;
-        int cur = find_layer(p, item_lo);
+        int cur = l_first;
         for (int item = item_lo; item < item_hi; ++item, ++lt) {
             advance_layer(p, item, cur);
             const SkinnyLayer& ly = p.L[cur];
-            const ItemInfo in = item_info(ly, item);
+            const ItemInfo in = item_info(ly, p.item_begin[cur], item);
             const uint32_t a = lt % kAccSets, aph = (lt / kAccSets) & 1u;
             if (!tc::mbar_wait(&sh->acc_full[a], aph, abort_flag, p.status)) break;
             tc::tc_fence_after();
@@ -404,7 +429,7 @@ cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsign
             L.mblocks = (int)((L.D + kBM - 1) / kBM);
             L.nchunks = (L.mblocks + cap - 1) / cap;
             L.chunk_mb = (L.mblocks + L.nchunks - 1) / L.nchunks;
-            L.item_begin = items;
+            p.item_begin[i] = items;
             L.partial = t.partial;
             L.gstore = t.gstore;
             items += (int)(B * L.nchunks);
@@ -419,6 +444,7 @@ cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsign
             }
         }
         p.total_items = items;
+        p.item_begin[p.nlayers] = items;
         const int grid = items < sms ? items : sms;
         k_mat_skinny_tc<<<grid, kThreads, kSmem, s>>>(p);
         count_launches(1);
