@@ -98,6 +98,7 @@ __device__ __forceinline__ void noise8(uint64_t seed, uint64_t step, uint64_t kb
     }
 }
 
+template <bool kMulti>
 __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const __grid_constant__ SumParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -195,7 +196,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
         const int part = (warp - 2) >> 2;          // columns part*64 .. +63
         const int row = quarter * 32 + lane;
         uint32_t rc = 0;
-        for (int tile = blockIdx.x; tile < ntiles && B == 1; tile += gridDim.x, ++rc) {
+        for (int tile = blockIdx.x; tile < ntiles && !kMulti; tile += gridDim.x, ++rc) {
             // one record: the noise does not depend on the sum, so it is drawn
             // while the tensor cores are still accumulating this tile
             int mb, nb;
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
             tc::tc_fence_before();
             tc::mbar_arrive(&sh->p_empty[b]);
         }
-        for (int tile = blockIdx.x; tile < ntiles && B > 1; tile += gridDim.x) {
+        for (int tile = blockIdx.x; tile < ntiles && kMulti; tile += gridDim.x) {
             int mb, nb;
             tile_coords(tile, p.m_blocks, p.n_blocks, mb, nb);
             float S[kColsPerWarp];
@@ -379,7 +380,8 @@ cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* s
                                   cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(k_clipped_sum_fold_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSumSmem);
+        cudaFuncSetAttribute(k_clipped_sum_fold_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSumSmem);
+        cudaFuncSetAttribute(k_clipped_sum_fold_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSumSmem);
         attr = true;
     }
     SumParams p;
@@ -408,7 +410,9 @@ cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* s
     p.step = sc.step;
     const int ntiles = p.m_blocks * p.n_blocks;
     const int grid = ntiles < sm_count_cached() ? ntiles : sm_count_cached();
-    const cudaError_t e = launch_dependent(k_clipped_sum_fold_tc, dim3(grid), dim3(kFoldThreads), kSumSmem, s, p);
+    const cudaError_t e =
+        sc.B > 1 ? launch_dependent(k_clipped_sum_fold_tc<true>, dim3(grid), dim3(kFoldThreads), kSumSmem, s, p)
+                 : launch_dependent(k_clipped_sum_fold_tc<false>, dim3(grid), dim3(kFoldThreads), kSumSmem, s, p);
     count_launches(1);
     return e;
 }

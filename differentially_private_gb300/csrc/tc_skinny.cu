@@ -10,13 +10,15 @@
 // [T, r] operand, the kernel computes g_i^T or g_i as X_i^T Y_i: M = 128
 // columns of X per MMA, N = 16 (r padded with the TMA's zero fill), K = T.
 //
-// Work item = (layer, record, chunk of up to 8 128-column blocks of D).
-// Stages walk the item k-tile by k-tile and, inside a k-tile, block by
-// block, so the blocks of one 64-row slab are read back to back (whole rows
-// of X in DRAM order).  Y has its own small ring and is loaded once per
-// k-tile for all blocks.  Each block accumulates into its own 16 TMEM
-// columns; items alternate between two accumulator sets.  One launch serves
-// up to kMaxSkinnyGroup layers; each CTA takes a contiguous range of items.
+// The 128-column blocks of D of every (layer, record) of the launch form one
+// index space; each CTA takes a contiguous range of it, so the CTAs' loads
+// differ by at most one block.  Work item = a run of at most item_cap blocks
+// of one (layer, record) inside the CTA's range.  Stages walk an item k-tile
+// by k-tile and, inside a k-tile, block by block, so the blocks of one
+// 64-row slab are read back to back (whole rows of X in DRAM order).  Y has
+// its own small ring and is loaded once per k-tile for all blocks.  Each
+// block accumulates into its own 16 TMEM columns; items alternate between
+// two accumulator sets.  One launch serves up to kMaxSkinnyGroup layers.
 //
 // The epilogue writes one partial squared norm per (record, block, epilogue
 // warp) -- no barrier, no atomics: a record's norm depends only on its own
@@ -37,7 +39,8 @@ constexpr int kXStages = 8;                 // 16 KB: 128 columns x 64 rows (two
 constexpr int kYStages = 4;                 //  2 KB: 16 columns x 64 rows, 32-byte swizzle
 constexpr int kXStage = kBM * kBK * 2;
 constexpr int kYStage = kBN * kBK * 2;
-constexpr int kMaxMb = 8;                   // column blocks per work item
+constexpr int kMaxMb = 8;                   // column blocks per work item (TMEM columns of one set)
+constexpr int kEpiGroup = 4;                // blocks whose TMEM columns the epilogue loads at once
 constexpr int kAccSets = 2;
 constexpr uint32_t kTmemCols = 256;         // kAccSets * kMaxMb * kBN
 constexpr int kThreads = 192;
@@ -50,20 +53,18 @@ struct SkinnyLayer {
     int64_t T, D, r;
     int x_is_A;        // 1: X = A (d_in = D, d_out = r); 0: X = E (d_out = D, d_in = r)
     int mblocks;       // 128-column blocks of D
-    int nchunks;       // items per record
-    int chunk_mb;      // blocks per item (the last item of a record may have fewer)
+    int item_cap;      // blocks per work item, at most kMaxMb
     float* partial;    // [B][mblocks * 4]
     float* gstore;     // [B][r * D] or nullptr
 };
 
 struct SkinnyParams {
     int nlayers;
-    int total_items;
     unsigned* status;
-    // first item of each layer (+ total): kept apart from the layer records so
-    // that the search for a CTA's first layer reads two cache lines of the
-    // parameter bank, not one line per layer
-    int item_begin[kMaxSkinnyGroup + 1];
+    // first block of each layer (+ the total): kept apart from the layer
+    // records so that the search for a CTA's first layer reads a few cache
+    // lines of the parameter bank, not one line per layer
+    int64_t blk_begin[kMaxSkinnyGroup + 1];
     SkinnyLayer L[kMaxSkinnyGroup];
 };
 
@@ -82,39 +83,71 @@ struct Smem {
     int warm[32];                            // sink of the parameter-bank warm-up loads
 };
 
-// Layer of an item, found by a whole warp: lane i compares item_begin[1 + i],
-// item_begin[33 + i] with the item (parallel parameter-bank reads instead of a
-// chain of dependent ones) and the ballots count the layers starting at or
-// before it.
 static_assert(sizeof(Smem) <= 8192 + 512, "skinny kernel shared-memory budget");
 
-__device__ __forceinline__ int warp_find_layer(const SkinnyParams& p, int item, int lane) {
+// Layer of a block, found by a whole warp: lane i compares blk_begin[1 + i],
+// blk_begin[33 + i] with the block (parallel parameter-bank reads instead of
+// a chain of dependent ones) and the ballots count the layers starting at or
+// before it.
+__device__ __forceinline__ int warp_find_layer(const SkinnyParams& p, int64_t q, int lane) {
     int l = 0;
     for (int base = 1; base < p.nlayers; base += 32) {
         const int j = base + lane;
-        l += __popc(__ballot_sync(0xffffffffu, j < p.nlayers && p.item_begin[j] <= item));
+        l += __popc(__ballot_sync(0xffffffffu, j < p.nlayers && p.blk_begin[j] <= q));
     }
     return l;
-}
-
-// items of a CTA increase, so the layer cursor only moves forward
-__device__ __forceinline__ void advance_layer(const SkinnyParams& p, int item, int& l) {
-    while (l + 1 < p.nlayers && p.item_begin[l + 1] <= item) ++l;
 }
 
 struct ItemInfo {
     int rec, mb0, nmb, nk;
 };
 
-__device__ __forceinline__ ItemInfo item_info(const SkinnyLayer& ly, int begin, int item) {
-    const int local = item - begin;
-    ItemInfo r;
-    r.rec = local / ly.nchunks;
-    const int chunk = local % ly.nchunks;
-    r.mb0 = chunk * ly.chunk_mb;
-    r.nmb = min(ly.chunk_mb, ly.mblocks - r.mb0);
-    r.nk = (int)((ly.T + kBK - 1) / kBK);
-    return r;
+// The next item of a CTA's block range [q, hi): the run of blocks of one
+// (layer, record) starting at block q, at most item_cap long.  Blocks of a
+// CTA increase, so the layer cursor l only moves forward.
+__device__ __forceinline__ bool next_item(const SkinnyParams& p, int64_t& q, int64_t hi, int& l, ItemInfo& in) {
+    if (q >= hi) return false;
+    while (l + 1 < p.nlayers && p.blk_begin[l + 1] <= q) ++l;
+    const SkinnyLayer& ly = p.L[l];
+    const int64_t local = q - p.blk_begin[l];
+    in.rec = (int)(local / ly.mblocks);
+    in.mb0 = (int)(local - (int64_t)in.rec * ly.mblocks);
+    int n = ly.mblocks - in.mb0;
+    if (n > ly.item_cap) n = ly.item_cap;
+    if ((int64_t)n > hi - q) n = (int)(hi - q);
+    in.nmb = n;
+    in.nk = (int)((ly.T + kBK - 1) / kBK);
+    q += n;
+    return true;
+}
+
+// TMEM columns of kEpiGroup consecutive 16-column blocks (64 columns of this
+// warp's 32 lanes), one wait for all four loads
+__device__ __forceinline__ void tmem_ld_group(uint32_t taddr, float (&v)[kEpiGroup][16]) {
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%65];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47}, [%66];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%67];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr), "r"(taddr + 16), "r"(taddr + 32), "r"(taddr + 48));
+#pragma unroll
+    for (int b = 0; b < kEpiGroup; ++b)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[b][i] = __uint_as_float(r[16 * b + i]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_constant__ SkinnyParams p) {
@@ -124,10 +157,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
     Smem* sh = reinterpret_cast<Smem*>(ys + (size_t)kYStages * kYStage);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int* abort_flag = &sh->abort_flag;
-    // each CTA takes one contiguous range of items: consecutive items share a
+    // each CTA takes one contiguous range of blocks: consecutive items share a
     // layer and its TMA descriptors
-    const int item_lo = (int)((int64_t)blockIdx.x * p.total_items / gridDim.x);
-    const int item_hi = (int)((int64_t)(blockIdx.x + 1) * p.total_items / gridDim.x);
+    const int64_t total = p.blk_begin[p.nlayers];
+    const int64_t blk_lo = (int64_t)blockIdx.x * total / gridDim.x;
+    const int64_t blk_hi = (int64_t)(blockIdx.x + 1) * total / gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kXStages; ++s) {
@@ -151,14 +185,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
         // while the barriers and TMEM are set up: find the CTA's layers, start
         // fetching their TMA descriptors and pull their parameter lines into
         // the constant cache with parallel reads
-        const int lf = item_lo < item_hi ? warp_find_layer(p, item_lo, lane) : 0;
-        const int ll = item_lo < item_hi ? warp_find_layer(p, item_hi - 1, lane) : -1;
+        const int lf = blk_lo < blk_hi ? warp_find_layer(p, blk_lo, lane) : 0;
+        const int ll = blk_lo < blk_hi ? warp_find_layer(p, blk_hi - 1, lane) : -1;
         if (lane == 0) sh->l_first = lf;
         int acc = 0;
         for (int l = lf + lane; l <= ll; l += 32) {
             tc::tma_prefetch_desc(&p.L[l].tmX);
             tc::tma_prefetch_desc(&p.L[l].tmY);
-            acc += p.L[l].nchunks + p.item_begin[l];
+            acc += p.L[l].mblocks + (int)p.blk_begin[l];
         }
         sh->warm[lane] = acc;
     }
@@ -173,16 +207,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
         if (lane == 0) {
             uint32_t it = 0, yit = 0;
             int cur = l_first;
-            for (int item = item_lo; item < item_hi; ++item) {
-                advance_layer(p, item, cur);
+            int64_t q = blk_lo;
+            ItemInfo in;
+            while (next_item(p, q, blk_hi, cur, in)) {
                 const SkinnyLayer& ly = p.L[cur];
-                const ItemInfo in = item_info(ly, p.item_begin[cur], item);
                 for (int kt = 0; kt < in.nk; ++kt) {
-                    const int q = yit % kYStages;
+                    const int qs = yit % kYStages;
                     const uint32_t qph = (yit / kYStages) & 1u;
-                    if (!tc::mbar_wait(&sh->yempty[q], qph ^ 1u, abort_flag, p.status)) goto producer_done;
-                    tc::mbar_arrive_expect_tx(&sh->yfull[q], kYStage);
-                    tc::tma_load_3d(ys + (size_t)q * kYStage, &ly.tmY, &sh->yfull[q], 0, kt * kBK, in.rec);
+                    if (!tc::mbar_wait(&sh->yempty[qs], qph ^ 1u, abort_flag, p.status)) goto producer_done;
+                    tc::mbar_arrive_expect_tx(&sh->yfull[qs], kYStage);
+                    tc::tma_load_3d(ys + (size_t)qs * kYStage, &ly.tmY, &sh->yfull[qs], 0, kt * kBK, in.rec);
                     ++yit;
                     for (int m = 0; m < in.nmb; ++m, ++it) {
                         const int s = it % kXStages;
@@ -208,18 +242,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
         if (lane == 0) {
             uint32_t it = 0, yit = 0, lt = 0;
             int cur = l_first;
+            int64_t q = blk_lo;
+            ItemInfo in;
             bool ok = true;
-            for (int item = item_lo; item < item_hi && ok; ++item, ++lt) {
-                advance_layer(p, item, cur);
-                const ItemInfo in = item_info(p.L[cur], p.item_begin[cur], item);
+            while (ok && next_item(p, q, blk_hi, cur, in)) {
                 const uint32_t a = lt % kAccSets, aph = (lt / kAccSets) & 1u;
+                ++lt;
                 if (!tc::mbar_wait(&sh->acc_empty[a], aph ^ 1u, abort_flag, p.status)) break;
                 tc::tc_fence_after();
                 for (int kt = 0; kt < in.nk && ok; ++kt) {
-                    const int q = yit % kYStages;
+                    const int qs = yit % kYStages;
                     const uint32_t qph = (yit / kYStages) & 1u;
-                    if (!tc::mbar_wait(&sh->yfull[q], qph, abort_flag, p.status)) { ok = false; break; }
-                    const uint32_t sy = tc::smem_u32(ys + (size_t)q * kYStage);
+                    if (!tc::mbar_wait(&sh->yfull[qs], qph, abort_flag, p.status)) { ok = false; break; }
+                    const uint32_t sy = tc::smem_u32(ys + (size_t)qs * kYStage);
                     for (int m = 0; m < in.nmb; ++m, ++it) {
                         const int s = it % kXStages;
                         const uint32_t ph = (it / kXStages) & 1u;
@@ -237,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
                         tc::mma_commit(&sh->empty[s]);
                     }
                     if (!ok) break;
-                    tc::mma_commit(&sh->yempty[q]);
+                    tc::mma_commit(&sh->yempty[qs]);
                     ++yit;
                 }
                 if (!ok) break;
@@ -251,51 +286,68 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
         const int ew = warp - 2;
         uint32_t lt = 0;
         int cur = l_first;
-        for (int item = item_lo; item < item_hi; ++item, ++lt) {
-            advance_layer(p, item, cur);
+        int64_t q = blk_lo;
+        ItemInfo in;
+        while (next_item(p, q, blk_hi, cur, in)) {
             const SkinnyLayer& ly = p.L[cur];
-            const ItemInfo in = item_info(ly, p.item_begin[cur], item);
             const uint32_t a = lt % kAccSets, aph = (lt / kAccSets) & 1u;
+            ++lt;
             if (!tc::mbar_wait(&sh->acc_full[a], aph, abort_flag, p.status)) break;
             tc::tc_fence_after();
             const int64_t ncl = ly.r * ly.D;
             float* g = ly.gstore ? ly.gstore + (int64_t)in.rec * ncl : nullptr;
             float* part = ly.partial + (int64_t)in.rec * ly.mblocks * 4;
-            for (int m = 0; m < in.nmb; ++m) {
-                float v[16];
-                tc::tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + a * (kMaxMb * kBN) + m * kBN, v);
-                const int mb = in.mb0 + m;
-                const int64_t d = (int64_t)mb * kBM + row;
-                float ss = 0.f;
-                if (d < ly.D) {
+            for (int m0 = 0; m0 < in.nmb; m0 += kEpiGroup) {
+                // the TMEM columns of up to four blocks at once (columns past the
+                // item's blocks are read but unused; they stay inside the set)
+                float v[kEpiGroup][16];
+                tmem_ld_group(tmem + ((uint32_t)(quarter * 32) << 16) + a * (kMaxMb * kBN) + m0 * kBN, v);
+                float ss[kEpiGroup];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (j < ly.r) ss = fmaf(v[j], v[j], ss);
-                }
-                if (g && ly.x_is_A) {
-                    // entry (j, d) of g [r x D]: for each j the warp's 32 rows d are contiguous
+                for (int b = 0; b < kEpiGroup; ++b) {
+                    const int m = m0 + b;
+                    ss[b] = 0.f;
+                    if (m >= in.nmb) continue;
+                    const int mb = in.mb0 + m;
+                    const int64_t d = (int64_t)mb * kBM + row;
                     if (d < ly.D) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            if (j < ly.r) g[(int64_t)j * ly.D + d] = v[j];
+                            if (j < ly.r) ss[b] = fmaf(v[b][j], v[b][j], ss[b]);
                     }
-                } else if (g) {
-                    // entry (d, j) of g [D x r]: the warp's 32 rows are one contiguous run of
-                    // 32 r floats; stage it in shared memory, then store it as float4s
-                    float* stage = sh->gstage[ew];
+                    if (g && ly.x_is_A) {
+                        // entry (j, d) of g [r x D]: for each j the warp's 32 rows d are contiguous
+                        if (d < ly.D) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (j < ly.r) stage[lane * ly.r + j] = v[j];
-                    __syncwarp();
-                    const int64_t d0 = (int64_t)mb * kBM + quarter * 32;
-                    const int64_t nvalid = min((int64_t)32, ly.D - d0) * ly.r;   // floats of this warp's run
-                    float* dst = g + d0 * ly.r;
-                    for (int q = lane; q * 4 < nvalid; q += 32)
-                        *reinterpret_cast<float4*>(dst + 4 * q) = *reinterpret_cast<const float4*>(stage + 4 * q);
-                    __syncwarp();
+                            for (int j = 0; j < 16; ++j)
+                                if (j < ly.r) g[(int64_t)j * ly.D + d] = v[b][j];
+                        }
+                    } else if (g) {
+                        // entry (d, j) of g [D x r]: the warp's 32 rows are one contiguous run of
+                        // 32 r floats; stage it in shared memory, then store it as float4s
+                        float* stage = sh->gstage[ew];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (j < ly.r) stage[lane * ly.r + j] = v[b][j];
+                        __syncwarp();
+                        const int64_t d0 = (int64_t)mb * kBM + quarter * 32;
+                        const int64_t nvalid = min((int64_t)32, ly.D - d0) * ly.r;   // floats of this warp's run
+                        float* dst = g + d0 * ly.r;
+                        for (int qq = lane; qq * 4 < nvalid; qq += 32)
+                            *reinterpret_cast<float4*>(dst + 4 * qq) = *reinterpret_cast<const float4*>(stage + 4 * qq);
+                        __syncwarp();
+                    }
                 }
-                ss = warp_sum(ss);
-                if (lane == 0) part[mb * 4 + ew] = ss;
+                // the blocks' warp sums, butterflies interleaved (same order per block as one warp_sum)
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                    for (int b = 0; b < kEpiGroup; ++b) ss[b] += __shfl_xor_sync(0xffffffffu, ss[b], o);
+                if (lane == 0) {
+#pragma unroll
+                    for (int b = 0; b < kEpiGroup; ++b)
+                        if (m0 + b < in.nmb) part[(in.mb0 + m0 + b) * 4 + ew] = ss[b];
+                }
             }
             tc::tc_fence_before();
             tc::mbar_arrive(&sh->acc_empty[a]);
@@ -347,32 +399,11 @@ int sm_count() {
     return n > 0 ? n : 1;
 }
 
-// Largest number of column blocks per item.  Each CTA takes a contiguous
-// range of about items / grid items, so its load is bounded by
-// ceil(items / grid) x (blocks of the largest item + a fixed per-item cost);
-// the cap minimizing that bound is taken (the largest on ties).
-int chunk_cap(const NormTask* tasks, int n, int64_t B, int grid) {
-    constexpr double kItemCost = 0.25;   // per-item overhead in units of one 128-column block
-    int best = kMaxMb;
-    double best_cost = 0.0;
-    for (int cap = kMaxMb; cap >= 1; --cap) {
-        int64_t items = 0;
-        int widest = 1;
-        for (int i = 0; i < n; ++i) {
-            const int64_t D = tasks[i].d_in > tasks[i].d_out ? tasks[i].d_in : tasks[i].d_out;
-            const int mb = (int)((D + kBM - 1) / kBM);
-            const int nch = (mb + cap - 1) / cap;
-            const int w = (mb + nch - 1) / nch;
-            items += B * nch;
-            widest = w > widest ? w : widest;
-        }
-        const double cost = (double)((items + grid - 1) / grid) * (widest + kItemCost);
-        if (cap == kMaxMb || cost < best_cost) {
-            best = cap;
-            best_cost = cost;
-        }
-    }
-    return best;
+// Blocks per work item of a layer: the record's blocks in the fewest runs of
+// at most four (one TMEM load group of the epilogue), as even as possible.
+int item_cap(int mblocks) {
+    const int runs = (mblocks + kEpiGroup - 1) / kEpiGroup;
+    return (mblocks + runs - 1) / runs;
 }
 
 }  // namespace
@@ -416,8 +447,7 @@ cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsign
     for (int base = 0; base < n; base += kMaxSkinnyGroup) {
         p.nlayers = n - base < kMaxSkinnyGroup ? n - base : kMaxSkinnyGroup;
         p.status = status;
-        const int cap = chunk_cap(tasks + base, p.nlayers, B, sms);
-        int items = 0;
+        int64_t blocks = 0;
         for (int i = 0; i < p.nlayers; ++i) {
             const NormTask& t = tasks[base + i];
             SkinnyLayer& L = p.L[i];
@@ -427,12 +457,11 @@ cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsign
             L.r = x_is_A ? t.d_out : t.d_in;
             L.T = t.T;
             L.mblocks = (int)((L.D + kBM - 1) / kBM);
-            L.nchunks = (L.mblocks + cap - 1) / cap;
-            L.chunk_mb = (L.mblocks + L.nchunks - 1) / L.nchunks;
-            p.item_begin[i] = items;
+            L.item_cap = item_cap(L.mblocks);
+            p.blk_begin[i] = blocks;
             L.partial = t.partial;
             L.gstore = t.gstore;
-            items += (int)(B * L.nchunks);
+            blocks += B * L.mblocks;
             if (t.maps) {
                 L.tmX = t.maps[0];
                 L.tmY = t.maps[1];
@@ -443,9 +472,8 @@ cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsign
                 L.tmY = m[1];
             }
         }
-        p.total_items = items;
-        p.item_begin[p.nlayers] = items;
-        const int grid = items < sms ? items : sms;
+        p.blk_begin[p.nlayers] = blocks;
+        const int grid = (int)(blocks < sms ? blocks : sms);
         k_mat_skinny_tc<<<grid, kThreads, kSmem, s>>>(p);
         count_launches(1);
         const cudaError_t e = cudaGetLastError();
