@@ -67,6 +67,9 @@ struct T1Group {
 
 __global__ void __launch_bounds__(256) k_norm_t1_group(const T1Group g) {
     using T = __nv_bfloat16;
+    // a normal launch: every earlier kernel has completed, so the next kernel
+    // (the clip factors, which waits for this one) may begin launching now
+    grid_dep_trigger();
     const auto& ly = g.L[blockIdx.y];
     const int64_t rec = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;

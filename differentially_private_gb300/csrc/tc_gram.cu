@@ -77,6 +77,9 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
     const int nkA = (int)((p.d_in + kGK - 1) / kGK);
     const int nkE = (int)((p.d_out + kGK - 1) / kGK);
     volatile int* abort_flag = &sh->abort_flag;
+    // a normal launch: every earlier kernel has completed, so the next kernel
+    // (the clip factors, which waits for this one) may begin launching now
+    grid_dep_trigger();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kGStages; ++s) {
@@ -173,6 +176,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
             if (!tc::mbar_wait(&sh->acc_full, lt & 1u, abort_flag, p.status)) break;
             tc::tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16);
+            const float bias = p.has_bias ? 1.f : 0.f;
             float acc = 0.f;
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
@@ -181,13 +185,16 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
                 if (w == 0.f) continue;          // uniform across the CTA
                 float part = 0.f;
 #pragma unroll 1
-                for (int ch = 0; ch < 8; ++ch) {
-                    float ga[16], ge[16];
-                    const uint32_t col = half * 128 + ch * 16;
-                    tc::tmem_ld16(tb + col, ga);
-                    tc::tmem_ld16(tb + 256 + col, ge);
+                for (int g = 0; g < 2; ++g) {
+                    // 64 columns of GA and of GE, four loads and one wait each
+                    float ga[4][16], ge[4][16];
+                    const uint32_t col = half * 128 + g * 64;
+                    tc::tmem_ld16x4(tb + col, ga);
+                    tc::tmem_ld16x4(tb + 256 + col, ge);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) part = fmaf(ga[j] + (p.has_bias ? 1.f : 0.f), ge[j], part);
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) part = fmaf(ga[c][j] + bias, ge[c][j], part);
                 }
                 acc = fmaf(w, part, acc);
             }

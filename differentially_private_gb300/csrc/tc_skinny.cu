@@ -40,7 +40,7 @@ constexpr int kYStages = 4;                 //  2 KB: 16 columns x 64 rows, 32-b
 constexpr int kXStage = kBM * kBK * 2;
 constexpr int kYStage = kBN * kBK * 2;
 constexpr int kMaxMb = 8;                   // column blocks per work item (TMEM columns of one set)
-constexpr int kEpiGroup = 4;                // blocks whose TMEM columns the epilogue loads at once
+constexpr int kEpiGroup = 4;                // blocks whose TMEM columns the epilogue loads at once (tmem_ld16x4)
 constexpr int kAccSets = 2;
 constexpr uint32_t kTmemCols = 256;         // kAccSets * kMaxMb * kBN
 constexpr int kThreads = 192;
@@ -121,35 +121,6 @@ __device__ __forceinline__ bool next_item(const SkinnyParams& p, int64_t& q, int
     return true;
 }
 
-// TMEM columns of kEpiGroup consecutive 16-column blocks (64 columns of this
-// warp's 32 lanes), one wait for all four loads
-__device__ __forceinline__ void tmem_ld_group(uint32_t taddr, float (&v)[kEpiGroup][16]) {
-    uint32_t r[64];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%64];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%65];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47}, [%66];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%67];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
-          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
-          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
-          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
-          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-        : "r"(taddr), "r"(taddr + 16), "r"(taddr + 32), "r"(taddr + 48));
-#pragma unroll
-    for (int b = 0; b < kEpiGroup; ++b)
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[b][i] = __uint_as_float(r[16 * b + i]);
-}
-
 __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_constant__ SkinnyParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* xs = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -162,6 +133,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
     const int64_t total = p.blk_begin[p.nlayers];
     const int64_t blk_lo = (int64_t)blockIdx.x * total / gridDim.x;
     const int64_t blk_hi = (int64_t)(blockIdx.x + 1) * total / gridDim.x;
+    // a normal launch: every earlier kernel has completed, so the next kernel
+    // (the clip factors, which waits for this one) may begin launching now
+    grid_dep_trigger();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kXStages; ++s) {
@@ -301,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
                 // the TMEM columns of up to four blocks at once (columns past the
                 // item's blocks are read but unused; they stay inside the set)
                 float v[kEpiGroup][16];
-                tmem_ld_group(tmem + ((uint32_t)(quarter * 32) << 16) + a * (kMaxMb * kBN) + m0 * kBN, v);
+                tc::tmem_ld16x4(tmem + ((uint32_t)(quarter * 32) << 16) + a * (kMaxMb * kBN) + m0 * kBN, v);
                 float ss[kEpiGroup];
 #pragma unroll
                 for (int b = 0; b < kEpiGroup; ++b) {
