@@ -144,6 +144,24 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest x over the ranks of the default process group (x itself
+    without one): the job is as slow as its slowest rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, B: int, steps: int, total_ms: float) -> float:
+    """Examples per second of the whole job: every rank clips and noises its
+    own B records each step (weak scaling), in the slowest rank's time."""
+    return world * B * steps / (total_ms / 1e3)
+
+
 # ----------------------------------------------------------- work accounting
 def work_model(w):
     """Algorithmic work of one step, per phase (one batch of w.B records).
@@ -356,12 +374,8 @@ def run_ours(args, w):
     norm_ms = [e[0].elapsed_time(e[1]) for e in pevs]
     clip_ms = [e[1].elapsed_time(e[2]) for e in pevs]
     grad_ms = [e[2].elapsed_time(e[3]) for e in pevs]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * w.B * K / (total_ms / 1e3)
+    total_ms = max_over_ranks(sum(step_ms), device)
+    value = job_throughput(world, w.B, K, total_ms)
 
     # roofline of the dominant phase
     peaks = load_peaks()
@@ -419,12 +433,8 @@ def run_ours(args, w):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ems], device=device, dtype=torch.float64)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * w.B * ke / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        ems = max_over_ranks(e0.elapsed_time(e1), device)
+        e2e = {"value": job_throughput(world, w.B, ke, ems), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
 
     cpu = None
