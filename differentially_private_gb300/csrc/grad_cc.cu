@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(kClipMaxThreads) k_clip(const ClipParams p, fl
     __shared__ float red[32];
     grid_dep_wait();
     grid_dep_trigger();
+    if (p.status_next && blockIdx.x == 0 && threadIdx.x == 0) *p.status_next = 0u;
     const int64_t rec = kWarpPerRecord ? (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)
                                        : (int64_t)blockIdx.x;
     const int t = kWarpPerRecord ? (int)(threadIdx.x & 31) : (int)threadIdx.x;

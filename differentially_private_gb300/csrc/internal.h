@@ -80,6 +80,7 @@ struct ClipParams {
     float C;
     const SlotRef* slots;      // device array: layers in registration order, each layer's slots in order
     int64_t total_slots;
+    unsigned* status_next;     // status word of the next step, zeroed by the kernel (or nullptr)
 };
 
 // ---- every kernel launch of the library is counted here (dp_kernel_launches)

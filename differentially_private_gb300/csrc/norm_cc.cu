@@ -16,6 +16,7 @@
 // Inflation from Cross-Record Precision Routing in Private Quantized
 // Fine-Tuning", Proposition 2).
 #include "common.cuh"
+#include "launch.cuh"
 
 using namespace dpk;
 
@@ -67,8 +68,9 @@ struct T1Group {
 
 __global__ void __launch_bounds__(256) k_norm_t1_group(const T1Group g) {
     using T = __nv_bfloat16;
-    // a normal launch: every earlier kernel has completed, so the next kernel
-    // (the clip factors, which waits for this one) may begin launching now
+    // may start while the previous kernel of the stream runs: A and E are read
+    // only after it completed
+    grid_dep_wait();
     grid_dep_trigger();
     const auto& ly = g.L[blockIdx.y];
     const int64_t rec = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -283,9 +285,8 @@ cudaError_t launch_norm_t1_group(const NormTask* tasks, int n, int64_t B, cudaSt
             g.L[i].partial = t.partial;
         }
         const dim3 grid((unsigned)((B * 32 + 255) / 256), (unsigned)g.n);
-        k_norm_t1_group<<<grid, 256, 0, s>>>(g);
+        const cudaError_t e = launch_dependent(k_norm_t1_group, grid, dim3(256), 0, s, g);
         count_launches(1);
-        const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -85,7 +85,10 @@ struct dp_ctx {
     float* c = nullptr;
     size_t bcap = 0;
     size_t ccap = 0;
-    unsigned* status = nullptr;
+    unsigned* status_words = nullptr; // two status words: steps alternate between them
+    unsigned* status = nullptr;        // the current step's word
+    int slot = 1;                      // index of the current step's word
+    bool clean[2] = {true, true};      // the word is known to be zero for the next step that takes it
     float* one = nullptr;              // device constant 1.0f
     SlotRef* d_slots = nullptr;        // clip kernel's flat view of every layer's partial slots
     size_t d_slots_cap = 0;
@@ -375,23 +378,24 @@ dp_status dp_create(dp_ctx** out, int device, void* cuda_stream) {
     ctx->stream = static_cast<cudaStream_t>(cuda_stream);
     ctx->sm_count = prop.multiProcessorCount;
     DeviceGuard g(device);
-    if (cudaMalloc(reinterpret_cast<void**>(&ctx->status), sizeof(unsigned)) != cudaSuccess) {
+    if (cudaMalloc(reinterpret_cast<void**>(&ctx->status_words), 2 * sizeof(unsigned)) != cudaSuccess) {
         cudaGetLastError();
         delete ctx;
         return DP_ERR_OOM;
     }
-    if (cudaMemsetAsync(ctx->status, 0, sizeof(unsigned), ctx->stream) != cudaSuccess) {
-        cudaFree(ctx->status);
+    if (cudaMemsetAsync(ctx->status_words, 0, 2 * sizeof(unsigned), ctx->stream) != cudaSuccess) {
+        cudaFree(ctx->status_words);
         delete ctx;
         return DP_ERR_CUDA;
     }
+    ctx->status = ctx->status_words + ctx->slot;
     // the clip factor 1 of a layer whose operand was pre-scaled
     const float one = 1.0f;
     if (cudaMalloc(reinterpret_cast<void**>(&ctx->one), sizeof(float)) != cudaSuccess ||
         cudaMemcpy(ctx->one, &one, sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) {
         cudaGetLastError();
         cudaFree(ctx->one);
-        cudaFree(ctx->status);
+        cudaFree(ctx->status_words);
         delete ctx;
         return DP_ERR_OOM;
     }
@@ -410,7 +414,7 @@ dp_status dp_destroy(dp_ctx* ctx) {
     }
     cudaFree(ctx->n2);
     cudaFree(ctx->c);
-    cudaFree(ctx->status);
+    cudaFree(ctx->status_words);
     cudaFree(ctx->one);
     cudaFree(ctx->d_slots);
     delete ctx;
@@ -458,8 +462,16 @@ dp_status dp_begin_step(dp_ctx* ctx, int64_t B) {
     if (st != DP_OK) return st;
     st = grow(ctx, &ctx->c, &ctx->ccap, (size_t)B);
     if (st != DP_OK) return st;
-    const cudaError_t e = cudaMemsetAsync(ctx->status, 0, sizeof(unsigned), ctx->stream);
-    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMemsetAsync");
+    // the step takes the other status word; the previous step's clip kernel
+    // zeroed it, otherwise it is cleared here
+    const int next = ctx->slot ^ 1;
+    if (!ctx->clean[next]) {
+        const cudaError_t e = cudaMemsetAsync(ctx->status_words + next, 0, sizeof(unsigned), ctx->stream);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMemsetAsync");
+    }
+    ctx->clean[next] = false;
+    ctx->slot = next;
+    ctx->status = ctx->status_words + next;
     for (Layer& ly : ctx->layers) {
         ly.accumulated = false;
         ly.A = ly.E = nullptr;
@@ -583,8 +595,12 @@ dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnor
     p.C = C;
     p.slots = ctx->d_slots;
     p.total_slots = total;
+    // the clip kernel also zeroes the other status word for the next step
+    // (every kernel that could write it belongs to an earlier, finished step)
+    p.status_next = ctx->status_words + (ctx->slot ^ 1);
     const cudaError_t e = launch_clip(p, ctx->n2, ctx->c, total_sqnorm_out, c_out, ctx->status, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "clip kernel launch");
+    ctx->clean[ctx->slot ^ 1] = true;
     ctx->C = C;
     ctx->phase = CLIPPED;
     return DP_OK;

@@ -98,6 +98,25 @@ __device__ __forceinline__ void noise8(uint64_t seed, uint64_t step, uint64_t kb
     }
 }
 
+// S[4q .. 4q+3] += sigma C z at this thread's coordinates k0 + 4q .. k0 + 4q + 3
+constexpr int kNoiseChunks = kColsPerWarp / 4;
+__device__ __forceinline__ void add_noise_chunk(const SumParams& p, uint64_t k0, int q, float (&S)[kColsPerWarp]) {
+    const uint64_t k = k0 + 4u * (uint64_t)q;
+    float z[4];
+    if ((k & 3u) == 0) {
+        noise_blocks<1>(p.seed, p.step, k >> 2, z);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) z[j] = noise_at(p.seed, p.step, k + j);
+    }
+#pragma unroll
+    for (int qq = 0; qq < kNoiseChunks; ++qq)
+        if (qq == q) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) S[4 * qq + j] = fmaf(p.scale, z[j], S[4 * qq + j]);
+        }
+}
+
 template <bool kMulti>
 __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const __grid_constant__ SumParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -247,6 +266,9 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
         for (int tile = blockIdx.x; tile < ntiles && kMulti; tile += gridDim.x) {
             int mb, nb;
             tile_coords(tile, p.m_blocks, p.n_blocks, mb, nb);
+            const int64_t m = (int64_t)mb * kBM + row;
+            const int64_t n0 = (int64_t)nb * kBN + part * kColsPerWarp;
+            const uint64_t k0 = (uint64_t)(p.coord_off + m * p.d_in + n0);   // this thread's first coordinate
             float S[kColsPerWarp];
 #pragma unroll
             for (int j = 0; j < kColsPerWarp; ++j) S[j] = 0.f;
@@ -267,31 +289,33 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
                 }
                 tc::tc_fence_before();
                 tc::mbar_arrive(&sh->p_empty[b]);
+                // the noise joins the sum four columns at a time, one chunk after
+                // each of the first records, while the tensor cores work on the next
+                if (i < kNoiseChunks && m < p.d_out) add_noise_chunk(p, k0, (int)i, S);
             }
             if (!ok) break;
-            const int64_t m = (int64_t)mb * kBM + row;
             if (m < p.d_out) {
+                for (int q = (int)(B < kNoiseChunks ? B : kNoiseChunks); q < kNoiseChunks; ++q)
+                    add_noise_chunk(p, k0, q, S);
 #pragma unroll
                 for (int ch = 0; ch < kColsPerWarp / 8; ++ch) {
-                    const int64_t n = (int64_t)nb * kBN + part * kColsPerWarp + ch * 8;
+                    const int64_t n = n0 + ch * 8;
                     if (n >= p.d_in) continue;
-                    float z[8];
-                    noise8(p.seed, p.step, (uint64_t)(p.coord_off + m * p.d_in + n), z);
                     float* out = p.G + m * p.d_in + n;
                     if (n + 8 <= p.d_in) {
 #pragma unroll
                         for (int j = 0; j < 8; j += 4) {
                             float4 o;
-                            o.x = (S[ch * 8 + j] + p.scale * z[j]) * p.inv_L;
-                            o.y = (S[ch * 8 + j + 1] + p.scale * z[j + 1]) * p.inv_L;
-                            o.z = (S[ch * 8 + j + 2] + p.scale * z[j + 2]) * p.inv_L;
-                            o.w = (S[ch * 8 + j + 3] + p.scale * z[j + 3]) * p.inv_L;
+                            o.x = S[ch * 8 + j] * p.inv_L;
+                            o.y = S[ch * 8 + j + 1] * p.inv_L;
+                            o.z = S[ch * 8 + j + 2] * p.inv_L;
+                            o.w = S[ch * 8 + j + 3] * p.inv_L;
                             *reinterpret_cast<float4*>(out + j) = o;
                         }
                     } else {
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            if (n + j < p.d_in) out[j] = (S[ch * 8 + j] + p.scale * z[j]) * p.inv_L;
+                            if (n + j < p.d_in) out[j] = S[ch * 8 + j] * p.inv_L;
                     }
                 }
             }

@@ -17,6 +17,7 @@
 // Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
 // warps 2-5 epilogue.
 #include "common.cuh"
+#include "launch.cuh"
 #include "tc_common.cuh"
 
 using namespace dpk;
@@ -77,9 +78,6 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
     const int nkA = (int)((p.d_in + kGK - 1) / kGK);
     const int nkE = (int)((p.d_out + kGK - 1) / kGK);
     volatile int* abort_flag = &sh->abort_flag;
-    // a normal launch: every earlier kernel has completed, so the next kernel
-    // (the clip factors, which waits for this one) may begin launching now
-    grid_dep_trigger();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kGStages; ++s) {
@@ -99,6 +97,10 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
+    // the set-up above may overlap the previous kernel of the stream; A and E
+    // are read only after it completed
+    grid_dep_wait();
+    grid_dep_trigger();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -295,7 +297,7 @@ cudaError_t launch_ghost_gram_tc(const NormTask& t, int64_t B, unsigned* status,
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int grid = p.total_items < sms ? p.total_items : sms;
-    k_ghost_gram_tc<<<grid, kGThreads, kGramSmem, s>>>(p);
+    const cudaError_t e = launch_dependent(k_ghost_gram_tc, dim3(grid), dim3(kGThreads), kGramSmem, s, p);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }

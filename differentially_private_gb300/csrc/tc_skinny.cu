@@ -28,6 +28,7 @@
 // Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
 // warps 2-5 epilogue.
 #include "common.cuh"
+#include "launch.cuh"
 #include "tc_common.cuh"
 
 using namespace dpk;
@@ -133,9 +134,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
     const int64_t total = p.blk_begin[p.nlayers];
     const int64_t blk_lo = (int64_t)blockIdx.x * total / gridDim.x;
     const int64_t blk_hi = (int64_t)(blockIdx.x + 1) * total / gridDim.x;
-    // a normal launch: every earlier kernel has completed, so the next kernel
-    // (the clip factors, which waits for this one) may begin launching now
-    grid_dep_trigger();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kXStages; ++s) {
@@ -175,6 +173,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
     tc::tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
     const int l_first = sh->l_first;
+    // the set-up above (which reads only the parameters) may overlap the
+    // previous kernel of the stream; A and E are read only after it completed
+    grid_dep_wait();
+    grid_dep_trigger();
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -448,9 +450,8 @@ cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsign
         }
         p.blk_begin[p.nlayers] = blocks;
         const int grid = (int)(blocks < sms ? blocks : sms);
-        k_mat_skinny_tc<<<grid, kThreads, kSmem, s>>>(p);
+        const cudaError_t e = launch_dependent(k_mat_skinny_tc, dim3(grid), dim3(kThreads), kSmem, s, p);
         count_launches(1);
-        const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
