@@ -135,44 +135,54 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
     const int64_t blk_lo = (int64_t)blockIdx.x * total / gridDim.x;
     const int64_t blk_hi = (int64_t)(blockIdx.x + 1) * total / gridDim.x;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kXStages; ++s) {
-            tc::mbar_init(&sh->full[s], 1);
-            tc::mbar_init(&sh->empty[s], 1);
+    // Warp 0 sets up the barriers, finds its first layer and starts loading
+    // at once; the other warps meet at named barrier 1, which warp 0 passes
+    // with an arrive (no wait), while warp 1 allocates TMEM and warp 2 pulls
+    // the layers' descriptors and parameter lines into the caches.
+    constexpr uint32_t kSetupBar = 1;
+    int l_first = 0;
+    uint32_t tmem = 0;
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int s = 0; s < kXStages; ++s) {
+                tc::mbar_init(&sh->full[s], 1);
+                tc::mbar_init(&sh->empty[s], 1);
+            }
+            for (int s = 0; s < kYStages; ++s) {
+                tc::mbar_init(&sh->yfull[s], 1);
+                tc::mbar_init(&sh->yempty[s], 1);
+            }
+            for (int a = 0; a < kAccSets; ++a) {
+                tc::mbar_init(&sh->acc_full[a], 1);
+                tc::mbar_init(&sh->acc_empty[a], 128);
+            }
+            tc::mbar_init(&sh->drain, 1);
+            sh->abort_flag = 0;
+            tc::fence_barrier_init();
         }
-        for (int s = 0; s < kYStages; ++s) {
-            tc::mbar_init(&sh->yfull[s], 1);
-            tc::mbar_init(&sh->yempty[s], 1);
+        __syncwarp();
+        tc::named_bar_arrive(kSetupBar, kThreads);
+        l_first = blk_lo < blk_hi ? warp_find_layer(p, blk_lo, lane) : 0;
+    } else {
+        if (warp == 1) tc::tmem_alloc(&sh->tmem_base, kTmemCols);
+        if (warp == 2) {
+            const int lf = blk_lo < blk_hi ? warp_find_layer(p, blk_lo, lane) : 0;
+            const int ll = blk_lo < blk_hi ? warp_find_layer(p, blk_hi - 1, lane) : -1;
+            if (lane == 0) sh->l_first = lf;
+            int acc = 0;
+            for (int l = lf + lane; l <= ll; l += 32) {
+                tc::tma_prefetch_desc(&p.L[l].tmX);
+                tc::tma_prefetch_desc(&p.L[l].tmY);
+                acc += p.L[l].mblocks + (int)p.blk_begin[l];
+            }
+            sh->warm[lane] = acc;
         }
-        for (int a = 0; a < kAccSets; ++a) {
-            tc::mbar_init(&sh->acc_full[a], 1);
-            tc::mbar_init(&sh->acc_empty[a], 128);
-        }
-        tc::mbar_init(&sh->drain, 1);
-        sh->abort_flag = 0;
-        tc::fence_barrier_init();
+        tc::tc_fence_before();
+        tc::named_bar_sync(kSetupBar, kThreads);
+        tc::tc_fence_after();
+        tmem = sh->tmem_base;
+        l_first = sh->l_first;
     }
-    if (warp == 1) tc::tmem_alloc(&sh->tmem_base, kTmemCols);
-    if (warp == 2) {
-        // while the barriers and TMEM are set up: find the CTA's layers, start
-        // fetching their TMA descriptors and pull their parameter lines into
-        // the constant cache with parallel reads
-        const int lf = blk_lo < blk_hi ? warp_find_layer(p, blk_lo, lane) : 0;
-        const int ll = blk_lo < blk_hi ? warp_find_layer(p, blk_hi - 1, lane) : -1;
-        if (lane == 0) sh->l_first = lf;
-        int acc = 0;
-        for (int l = lf + lane; l <= ll; l += 32) {
-            tc::tma_prefetch_desc(&p.L[l].tmX);
-            tc::tma_prefetch_desc(&p.L[l].tmY);
-            acc += p.L[l].mblocks + (int)p.blk_begin[l];
-        }
-        sh->warm[lane] = acc;
-    }
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
-    const uint32_t tmem = sh->tmem_base;
-    const int l_first = sh->l_first;
     // the set-up above (which reads only the parameters) may overlap the
     // previous kernel of the stream; A and E are read only after it completed
     grid_dep_wait();
