@@ -195,6 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
             int cur = l_first;
             int64_t q = blk_lo;
             ItemInfo in;
+            // A and E are read once: evict them first, keep the stored g in L2
+            const uint64_t stream_policy = tc::l2_evict_first();
             while (next_item(p, q, blk_hi, cur, in)) {
                 const SkinnyLayer& ly = p.L[cur];
                 for (int kt = 0; kt < in.nk; ++kt) {
@@ -202,7 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
                     const uint32_t qph = (yit / kYStages) & 1u;
                     if (!tc::mbar_wait(&sh->yempty[qs], qph ^ 1u, abort_flag, p.status)) goto producer_done;
                     tc::mbar_arrive_expect_tx(&sh->yfull[qs], kYStage);
-                    tc::tma_load_3d(ys + (size_t)qs * kYStage, &ly.tmY, &sh->yfull[qs], 0, kt * kBK, in.rec);
+                    tc::tma_load_3d_hint(ys + (size_t)qs * kYStage, &ly.tmY, &sh->yfull[qs], 0, kt * kBK, in.rec,
+                                         stream_policy);
                     ++yit;
                     for (int m = 0; m < in.nmb; ++m, ++it) {
                         const int s = it % kXStages;
@@ -211,8 +214,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
                         uint8_t* st = xs + (size_t)s * kXStage;
                         const int col = (in.mb0 + m) * kBM;
                         tc::mbar_arrive_expect_tx(&sh->full[s], kXStage);
-                        tc::tma_load_3d(st, &ly.tmX, &sh->full[s], col, kt * kBK, in.rec);
-                        tc::tma_load_3d(st + 8192, &ly.tmX, &sh->full[s], col + 64, kt * kBK, in.rec);
+                        tc::tma_load_3d_hint(st, &ly.tmX, &sh->full[s], col, kt * kBK, in.rec, stream_policy);
+                        tc::tma_load_3d_hint(st + 8192, &ly.tmX, &sh->full[s], col + 64, kt * kBK, in.rec,
+                                             stream_policy);
                     }
                 }
             }
