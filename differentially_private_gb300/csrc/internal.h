@@ -115,11 +115,21 @@ cudaError_t launch_prescale_rows(const void* E, void* E2, const float* c, int64_
                                  cudaStream_t s);
 
 // ---- tcgen05 kernels (tc_gemm.cu)
+// Scratch of the tensor-core clipped sum for the tiles of a partial last wave
+// that are split into record ranges over the grid.
+struct FoldWork {
+    float* scratch;                  // fold_scratch_floats(sms) floats
+    unsigned long long* counters;    // sms entries; zero when allocated, never reset
+    unsigned epoch;                  // different for every launch (never 0)
+};
+size_t fold_scratch_floats(int sms);
+int device_sm_count();
 bool tc_sum_supported(int dtype, int64_t d_in, int64_t d_out, int has_bias);
 bool tc_skinny_supported(int dtype, int64_t d_in, int64_t d_out, int has_bias);
 int nslots_skinny(int64_t d_in, int64_t d_out);
+// work == nullptr: every tile is done whole by one CTA
 cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* status,
-                                  const StepScalars& sc, cudaStream_t s);
+                                  const StepScalars& sc, const FoldWork* work, cudaStream_t s);
 cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsigned* status, cudaStream_t s);
 // TMA descriptors of a layer, encoded once per (pointers, T, B) and cached by the runtime
 bool tc_encode_skinny(const NormTask& t, int64_t B, CUtensorMap* maps2);

@@ -90,6 +90,9 @@ struct dp_ctx {
     int slot = 1;                      // index of the current step's word
     bool clean[2] = {true, true};      // the word is known to be zero for the next step that takes it
     float* one = nullptr;              // device constant 1.0f
+    float* fold_scratch = nullptr;     // partial sums of split tiles of the tensor-core clipped sum
+    unsigned long long* fold_counters = nullptr;   // their arrival counters (zeroed once)
+    unsigned fold_epoch = 0;           // tag of the last clipped-sum launch
     SlotRef* d_slots = nullptr;        // clip kernel's flat view of every layer's partial slots
     size_t d_slots_cap = 0;
     std::vector<std::pair<const float*, int64_t>> slots_key;   // (partial, nslots) per layer d_slots was built from
@@ -98,6 +101,13 @@ struct dp_ctx {
 };
 
 namespace {
+
+// launch tag of the clipped-sum split counters; 0 is never used, so the
+// zeroed counters match no launch
+unsigned next_fold_epoch(dp_ctx* ctx) {
+    if (++ctx->fold_epoch == 0) ++ctx->fold_epoch;
+    return ctx->fold_epoch;
+}
 
 struct DeviceGuard {
     int prev = -1;
@@ -277,6 +287,21 @@ dp_status prepare(dp_ctx* ctx, int id, const void* A, const void* E, int64_t T, 
         plan.escaled = ly.escaled;
         plan.escaled_cap = ly.escaled_cap;
     }
+    if (plan.grad_kernel == GK_GEMM_TC && !ctx->fold_scratch) {
+        const int sms = device_sm_count();
+        cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&ctx->fold_scratch), fold_scratch_floats(sms) * sizeof(float));
+        if (e == cudaSuccess)
+            e = cudaMalloc(reinterpret_cast<void**>(&ctx->fold_counters), (size_t)sms * sizeof(unsigned long long));
+        if (e == cudaSuccess) e = cudaMemset(ctx->fold_counters, 0, (size_t)sms * sizeof(unsigned long long));
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(ctx->fold_scratch);
+            cudaFree(ctx->fold_counters);
+            ctx->fold_scratch = nullptr;
+            ctx->fold_counters = nullptr;
+            return fail(ctx, DP_ERR_OOM, "allocation of the clipped-sum scratch failed");
+        }
+    }
     if (plan.grad_kernel == GK_GEMM_TC) {
         // the sum reads the pre-scaled copy as one record of B*T rows when prescaling
         const void* Asum = plan.prescale_A ? static_cast<const void*>(plan.escaled) : A;
@@ -417,6 +442,8 @@ dp_status dp_destroy(dp_ctx* ctx) {
     cudaFree(ctx->status_words);
     cudaFree(ctx->one);
     cudaFree(ctx->d_slots);
+    cudaFree(ctx->fold_scratch);
+    cudaFree(ctx->fold_counters);
     delete ctx;
     return DP_OK;
 }
@@ -652,10 +679,11 @@ dp_status dp_clipped_noisy_grad(dp_ctx* ctx, float sigma, uint64_t seed, uint64_
             ts.T = K;
             StepScalars s1 = sc;
             s1.B = 1;
-            if (e == cudaSuccess) e = launch_clipped_sum_tc(ts, ctx->one, ctx->status, s1, ctx->stream);
+            if (e == cudaSuccess) e = launch_clipped_sum_tc(ts, ctx->one, ctx->status, s1, nullptr, ctx->stream);
             if (e == cudaSuccess && ly.has_bias) e = launch_bias_sum(t, ctx->c, ctx->status, sc, ctx->stream);
         } else if (ly.grad_kernel == GK_GEMM_TC) {
-            e = launch_clipped_sum_tc(t, ctx->c, ctx->status, sc, ctx->stream);
+            const FoldWork fw{ctx->fold_scratch, ctx->fold_counters, next_fold_epoch(ctx)};
+            e = launch_clipped_sum_tc(t, ctx->c, ctx->status, sc, &fw, ctx->stream);
             if (e == cudaSuccess && ly.has_bias) e = launch_bias_sum(t, ctx->c, ctx->status, sc, ctx->stream);
         } else {
             e = launch_grad_gemm_cc(t, ctx->c, ctx->status, sc, ctx->stream);

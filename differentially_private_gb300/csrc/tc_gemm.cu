@@ -19,6 +19,8 @@
 //   warps 2-17  fold S += c_i P_i, then the noise epilogue
 #include <cuda_bf16.h>
 
+#include <climits>
+
 #include "common.cuh"
 #include "launch.cuh"
 #include "tc_common.cuh"
@@ -50,6 +52,12 @@ struct SumParams {
     float scale;       // sigma * C
     float inv_L;       // 1 / L
     uint64_t seed, step;
+    // split of the last partial wave (records mode only; see next_work)
+    int full_tiles;                 // tiles done whole, strided over the grid
+    int nsplit;                     // record ranges per remaining tile (1: no split)
+    float* scratch;                 // [grid][kBN][kBM] partial sums of the split tiles
+    unsigned long long* counters;   // [ntiles - full_tiles] arrivals, (epoch << 32) | count
+    unsigned epoch;                 // this launch's tag for the counters
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks, int& mb, int& nb) {
@@ -63,6 +71,43 @@ __device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks
     const int r = tile - g * per_group;
     mb = first + r % gm;
     nb = r / gm;
+}
+
+// ------------------------------------------------------------ work split
+// With records (B > 1), a CTA does the whole tiles blockIdx.x, + grid, ...
+// below full_tiles.  When the tile count leaves a partial last wave of R
+// tiles, the remaining tiles are each cut into nsplit = grid / R ranges of
+// records, all run at once: CTA b < R * nsplit takes tile full_tiles + b % R,
+// records of range b / R.  The CTAs working on one range read the same K rows
+// of E and A at the same time, as a whole wave would.  Every range writes its
+// partial sum to the CTA's scratch slot; the CTA that arrives last at the
+// tile's counter adds the slots in range order and writes G (a fixed order,
+// so the result does not depend on timing).
+struct Work {
+    int tile;
+    int seg;            // record range of a split tile, -1 for a whole tile
+    int64_t r0, r1;     // records [r0, r1)
+};
+
+__device__ __forceinline__ bool next_work(const SumParams& p, int ntiles, int64_t B, int& cursor, Work& w) {
+    if (cursor < p.full_tiles) {
+        w.tile = cursor;
+        w.seg = -1;
+        w.r0 = 0;
+        w.r1 = B;
+        cursor += gridDim.x;
+        return true;
+    }
+    if (cursor == INT_MAX || p.nsplit < 2) return false;
+    cursor = INT_MAX;
+    const int R = ntiles - p.full_tiles;
+    const int b = blockIdx.x;
+    if (b >= R * p.nsplit) return false;
+    w.tile = p.full_tiles + b % R;
+    w.seg = b / R;
+    w.r0 = (int64_t)w.seg * B / p.nsplit;
+    w.r1 = (int64_t)(w.seg + 1) * B / p.nsplit;
+    return true;
 }
 
 // ============================================== clipped sum, per-record fold
@@ -84,8 +129,11 @@ struct FoldSmem {
     uint64_t p_full[2];
     uint64_t p_empty[2];
     uint64_t drain;
+    uint64_t fix_in;    // the epilogue threads' partial sums of a split tile are written
+    uint64_t fix_out;   // the arrival at the tile's counter is decided
     uint32_t tmem_base;
     int abort_flag;
+    int fix_last;       // this CTA completes the split tile
 };
 
 // z for 8 consecutive coordinates starting at kb
@@ -138,7 +186,10 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
             tc::mbar_init(&sh->p_empty[b], 32 * kEpiWarps);
         }
         tc::mbar_init(&sh->drain, 1);
+        tc::mbar_init(&sh->fix_in, 32 * kEpiWarps);
+        tc::mbar_init(&sh->fix_out, 1);
         sh->abort_flag = 0;
+        sh->fix_last = 0;
         tc::fence_barrier_init();
         tc::tma_prefetch_desc(&p.tmE);
         tc::tma_prefetch_desc(&p.tmA);
@@ -157,11 +208,13 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
     if (!skip && warp == 0) {
         if (lane == 0) {
             uint32_t it = 0;
-            const int nk = (int)(B * kpr);
-            for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            int cursor = blockIdx.x;
+            Work wk;
+            while (next_work(p, ntiles, B, cursor, wk)) {
                 int mb, nb;
-                tile_coords(tile, p.m_blocks, p.n_blocks, mb, nb);
-                for (int kt = 0; kt < nk; ++kt, ++it) {
+                tile_coords(wk.tile, p.m_blocks, p.n_blocks, mb, nb);
+                const int kt_end = (int)(wk.r1 * kpr);
+                for (int kt = (int)(wk.r0 * kpr); kt < kt_end; ++kt, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
                     if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort_flag, p.status)) goto fold_producer_done;
@@ -182,9 +235,11 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
     } else if (!skip && warp == 1) {
         if (lane == 0) {
             uint32_t it = 0, rc = 0;
-            for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            int cursor = blockIdx.x;
+            Work wk;
+            while (next_work(p, ntiles, B, cursor, wk)) {
                 bool ok = true;
-                for (int64_t i = 0; i < B && ok; ++i, ++rc) {
+                for (int64_t i = wk.r0; i < wk.r1 && ok; ++i, ++rc) {
                     const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
                     if (!tc::mbar_wait(&sh->p_empty[b], bph ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     tc::tc_fence_after();
@@ -263,17 +318,22 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
             tc::tc_fence_before();
             tc::mbar_arrive(&sh->p_empty[b]);
         }
-        for (int tile = blockIdx.x; tile < ntiles && kMulti; tile += gridDim.x) {
+        int cursor = blockIdx.x;
+        Work wk;
+        uint32_t fix_phase = 0;
+        while (kMulti && next_work(p, ntiles, B, cursor, wk)) {
             int mb, nb;
-            tile_coords(tile, p.m_blocks, p.n_blocks, mb, nb);
+            tile_coords(wk.tile, p.m_blocks, p.n_blocks, mb, nb);
             const int64_t m = (int64_t)mb * kBM + row;
             const int64_t n0 = (int64_t)nb * kBN + part * kColsPerWarp;
             const uint64_t k0 = (uint64_t)(p.coord_off + m * p.d_in + n0);   // this thread's first coordinate
+            // the range holding the tile's first record also carries its noise
+            const bool noisy = wk.r0 == 0 && m < p.d_out;
             float S[kColsPerWarp];
 #pragma unroll
             for (int j = 0; j < kColsPerWarp; ++j) S[j] = 0.f;
             bool ok = true;
-            for (int64_t i = 0; i < B; ++i, ++rc) {
+            for (int64_t i = wk.r0; i < wk.r1; ++i, ++rc) {
                 const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
                 if (!tc::mbar_wait(&sh->p_full[b], bph, abort_flag, p.status)) { ok = false; break; }
                 tc::tc_fence_after();
@@ -291,12 +351,56 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
                 tc::mbar_arrive(&sh->p_empty[b]);
                 // the noise joins the sum four columns at a time, one chunk after
                 // each of the first records, while the tensor cores work on the next
-                if (i < kNoiseChunks && m < p.d_out) add_noise_chunk(p, k0, (int)i, S);
+                if (noisy && i < kNoiseChunks) add_noise_chunk(p, k0, (int)i, S);
             }
             if (!ok) break;
-            if (m < p.d_out) {
-                for (int q = (int)(B < kNoiseChunks ? B : kNoiseChunks); q < kNoiseChunks; ++q)
+            if (noisy)
+                for (int q = (int)(wk.r1 < kNoiseChunks ? wk.r1 : kNoiseChunks); q < kNoiseChunks; ++q)
                     add_noise_chunk(p, k0, q, S);
+            if (wk.seg >= 0) {
+                // split tile: the range's partial sum to this CTA's slot, then the counter
+                const int R = ntiles - p.full_tiles;
+                const int r = wk.tile - p.full_tiles;
+                float* slot = p.scratch + (size_t)blockIdx.x * (kBM * kBN);
+#pragma unroll
+                for (int j = 0; j < kColsPerWarp; ++j) slot[(size_t)(part * kColsPerWarp + j) * kBM + row] = S[j];
+                __threadfence();
+                tc::mbar_arrive(&sh->fix_in);
+                if (warp == 2 && lane == 0) {
+                    int last = 0;
+                    if (tc::mbar_wait(&sh->fix_in, fix_phase, abort_flag, p.status)) {
+                        __threadfence();
+                        unsigned long long* cp = p.counters + r;
+                        unsigned long long seen = *(volatile unsigned long long*)cp, prev;
+                        do {
+                            prev = seen;
+                            const unsigned long long want = (unsigned)(prev >> 32) == p.epoch
+                                                                ? prev + 1
+                                                                : ((unsigned long long)p.epoch << 32) | 1ull;
+                            seen = atomicCAS(cp, prev, want);
+                        } while (seen != prev);
+                        const unsigned before = (unsigned)(prev >> 32) == p.epoch ? (unsigned)prev : 0u;
+                        last = before + 1 == (unsigned)p.nsplit ? 1 : 0;
+                        __threadfence();
+                    }
+                    *(volatile int*)&sh->fix_last = last;
+                    tc::mbar_arrive(&sh->fix_out);
+                }
+                const bool waited = tc::mbar_wait(&sh->fix_out, fix_phase, abort_flag, p.status);
+                fix_phase ^= 1u;
+                if (!waited) break;
+                if (!*(volatile int*)&sh->fix_last) continue;
+                // last arrival: the ranges' partial sums in range order
+#pragma unroll
+                for (int j = 0; j < kColsPerWarp; ++j) S[j] = 0.f;
+                for (int sg = 0; sg < p.nsplit; ++sg) {
+                    const float* src = p.scratch + (size_t)(r + sg * R) * (kBM * kBN);
+#pragma unroll
+                    for (int j = 0; j < kColsPerWarp; ++j)
+                        S[j] += __ldcg(src + (size_t)(part * kColsPerWarp + j) * kBM + row);
+                }
+            }
+            if (m < p.d_out) {
 #pragma unroll
                 for (int ch = 0; ch < kColsPerWarp / 8; ++ch) {
                     const int64_t n = n0 + ch * 8;
@@ -400,8 +504,12 @@ bool tc_encode_sum(const GradTask& t, int64_t B, CUtensorMap* maps2) {
            encode(&maps2[1], t.A, 2, da, sa, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+size_t fold_scratch_floats(int sms) { return (size_t)sms * kBM * kBN; }
+
+int device_sm_count() { return sm_count_cached(); }
+
 cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* status, const StepScalars& sc,
-                                  cudaStream_t s) {
+                                  const FoldWork* work, cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(k_clipped_sum_fold_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSumSmem);
@@ -433,7 +541,32 @@ cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* s
     p.seed = sc.seed;
     p.step = sc.step;
     const int ntiles = p.m_blocks * p.n_blocks;
-    const int grid = ntiles < sm_count_cached() ? ntiles : sm_count_cached();
+    const int sms = sm_count_cached();
+    int grid = ntiles < sms ? ntiles : sms;
+    p.full_tiles = ntiles;
+    p.nsplit = 1;
+    p.scratch = nullptr;
+    p.counters = nullptr;
+    p.epoch = 0;
+    if (work != nullptr && sc.B > 1) {
+        // split the R tiles of a partial last wave into grid / R record ranges
+        // (each at least 8 K tiles) when the wave would leave over 4% of the
+        // CTA slots idle
+        const int R = ntiles % sms;
+        const int waves = (ntiles + sms - 1) / sms;
+        const double idle = (double)((int64_t)waves * sms - ntiles) / ((double)waves * sms);
+        const int64_t kpr = (t.T + kBK - 1) / kBK;
+        int S = R > 0 ? sms / R : 1;
+        while (S > 1 && (sc.B / S) * kpr < 8) --S;
+        if (R > 0 && S >= 2 && idle > 0.04) {
+            p.full_tiles = ntiles - R;
+            p.nsplit = S;
+            p.scratch = work->scratch;
+            p.counters = work->counters;
+            p.epoch = work->epoch;
+            grid = sms;
+        }
+    }
     const cudaError_t e =
         sc.B > 1 ? launch_dependent(k_clipped_sum_fold_tc<true>, dim3(grid), dim3(kFoldThreads), kSumSmem, s, p)
                  : launch_dependent(k_clipped_sum_fold_tc<false>, dim3(grid), dim3(kFoldThreads), kSumSmem, s, p);
