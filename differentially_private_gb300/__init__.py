@@ -3,7 +3,10 @@
 The work is done by ``libdpclip.so`` (hand-written CUDA for sm_103a) behind
 the C ABI of ``include/dp_clip.h``; this package is its ctypes binding
 (``_binding``, same names as the C entry points), a convenience wrapper
-(``step.PrivateGradient``) and the in-tree build (``build``).
+(``step.PrivateGradient``), the in-tree build (``build``), the sensitivity
+audit of the computation (``audit``), and per-record activations and output
+gradients captured from a model's own forward and backward (``capture``,
+with an OPT-shaped LoRA producer in ``opt_lora``).
 """
 
 from ._binding import (  # noqa: F401
