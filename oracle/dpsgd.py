@@ -209,3 +209,68 @@ def step(layers: list[Layer], A_list, E_list, T_list, C: float, sigma: float,
         G = (flat + sigma * C * z[off:off + ly.ncoords]) / L
         res.grads.append(G)
     return res
+
+
+# ------------------------------------------------------------- user level
+@dataclass
+class UserStepResult:
+    user_sqnorm: np.ndarray      # [U] squared norm of each user's summed gradient
+    clip: np.ndarray             # [U]
+    noise: np.ndarray            # [P]
+    clipped: list = field(default_factory=list)   # per layer (S, sb) before noise and L
+    grads: list = field(default_factory=list)     # per layer G = (S + sigma C z) / L
+
+
+def user_step(layers: list[Layer], A_list, E_list, T_list, group_sizes, C: float, sigma: float,
+              seed: int, step_index: int, L: float | None = None) -> UserStepResult:
+    """User-level clipping ("Privacy-Preserving Machine Learning", section
+    "Differentially private stochastic gradient descent", the user-level
+    construction and its sum-then-user-clip example): the records are grouped
+    in order (user u owns the next group_sizes[u] records), each user's vector
+    is the sum of its records' gradients over all layers, that vector is
+    clipped to C, the clipped user vectors are summed, noise N(0, sigma^2 C^2)
+    is added once per coordinate, and the sum is divided by the public
+    normalizer L (default: the number of users).  Zero-record users are
+    allowed (their vector is zero)."""
+    C = check_clip_bound(C)
+    sizes = [int(k) for k in group_sizes]
+    if any(k < 0 for k in sizes):
+        raise ValueError("group sizes must be >= 0")
+    B = _f64(A_list[0]).shape[0]
+    if sum(sizes) != B:
+        raise ValueError("group sizes must add up to the number of records")
+    U = len(sizes)
+    L = float(U) if L is None else float(L)
+    check_noise_args(float(sigma), L)
+    starts = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    per_layer = []                       # per layer: list over users of (g_u, b_u)
+    n2 = np.zeros(U, dtype=np.float64)
+    for ly, A, E in zip(layers, A_list, E_list):
+        A, E = _f64(A), _f64(E)
+        users = []
+        for u in range(U):
+            g = np.zeros((ly.d_out, ly.d_in), dtype=np.float64)
+            b = np.zeros(ly.d_out, dtype=np.float64) if ly.has_bias else None
+            for i in range(starts[u], starts[u + 1]):
+                gi, bi = per_example_grad(A[i], E[i], ly.has_bias)
+                g += gi
+                if ly.has_bias:
+                    b += bi
+            users.append((g, b))
+            n2[u] += np.sum(g * g) + (np.sum(b * b) if b is not None else 0.0)
+        per_layer.append(users)
+    c = clip_factors(n2, C)
+    offs, P = coordinate_offsets(layers)
+    z = philox.normals(seed, step_index, 0, P)
+    res = UserStepResult(user_sqnorm=n2, clip=c, noise=z)
+    for ly, users, off in zip(layers, per_layer, offs):
+        S = np.zeros((ly.d_out, ly.d_in), dtype=np.float64)
+        sb = np.zeros(ly.d_out, dtype=np.float64) if ly.has_bias else None
+        for u, (g, b) in enumerate(users):
+            S += c[u] * g
+            if ly.has_bias:
+                sb += c[u] * b
+        res.clipped.append((S, sb))
+        flat = S.reshape(-1) if sb is None else np.concatenate([S.reshape(-1), sb])
+        res.grads.append((flat + sigma * C * z[off:off + ly.ncoords]) / L)
+    return res
