@@ -38,6 +38,7 @@ from ._binding import (  # noqa: F401
     dp_norm_accumulate,
     dp_norm_accumulate_batch,
     dp_num_coords,
+    dp_pack_groups,
     dp_philox_normals,
     dp_register_layer,
     dp_set_normalizer,

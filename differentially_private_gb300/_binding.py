@@ -35,7 +35,7 @@ EXPORTS = (
     "dp_version", "dp_kernel_launches", "dp_status_string", "dp_create", "dp_destroy", "dp_register_layer",
     "dp_layer_info", "dp_num_coords", "dp_choose_path", "dp_begin_step", "dp_set_normalizer",
     "dp_norm_accumulate", "dp_norm_accumulate_batch", "dp_clip_factors", "dp_clipped_noisy_grad",
-    "dp_step_status", "dp_last_error", "dp_philox_normals", "dp_layer_sqnorms_static",
+    "dp_step_status", "dp_last_error", "dp_philox_normals", "dp_layer_sqnorms_static", "dp_pack_groups",
 )
 
 
@@ -86,6 +86,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "dp_last_error": (c.c_char_p, [vp]),
         "dp_philox_normals": (i32, [u64, u64, u64, i64, vp, vp, vp]),
         "dp_layer_sqnorms_static": (i32, [vp, vp, i64, i64, i64, i64, i32, i32, vp, vp]),
+        "dp_pack_groups": (i32, [vp, vp, i64, i64, i64, i32, vp, i64, i64, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -224,3 +225,10 @@ def dp_layer_sqnorms_static(A, E, B: int, T: int, d_in: int, d_out: int, has_bia
     _check(load_library().dp_layer_sqnorms_static(_ptr(A), _ptr(E), int(B), int(T), int(d_in), int(d_out),
                                                   int(bool(has_bias)), int(dtype), _ptr(sqnorm_out),
                                                   _stream(stream)), "dp_layer_sqnorms_static")
+
+
+def dp_pack_groups(src, dst, B: int, T: int, d: int, dtype: int, group_starts, U: int, kmax: int,
+                   stream=None) -> None:
+    """Records grouped by user, laid out [U, kmax, T, d] with zero records where a user has fewer."""
+    _check(load_library().dp_pack_groups(_ptr(src), _ptr(dst), int(B), int(T), int(d), int(dtype),
+                                         _ptr(group_starts), int(U), int(kmax), _stream(stream)), "dp_pack_groups")

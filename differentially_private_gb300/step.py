@@ -55,6 +55,40 @@ class PrivateGradient:
         sq = torch.empty(B, dtype=torch.float32, device=self.device)
         return grads, clip, sq
 
+    def step_users(self, A_list, E_list, T_list, group_sizes, C: float, sigma: float, seed: int, step: int,
+                   L: float | None = None, outputs=None) -> StepOutput:
+        """User-level clipping: the records are grouped in order (user u owns
+        the next group_sizes[u] records); each user's vector, the sum of its
+        records' gradients, is clipped to C; noise is added once and the sum
+        divided by L (default: the number of users).  A user is handed to the
+        library as one record of its records stacked along T (users with
+        fewer records than the largest one padded with zero records by
+        dp_pack_groups).  The returned clip and sqnorm are per user."""
+        sizes = [int(k) for k in group_sizes]
+        B = int(A_list[0].shape[0])
+        if any(k < 0 for k in sizes) or sum(sizes) != B:
+            raise ValueError("group sizes must be >= 0 and add up to the number of records")
+        U, kmax = len(sizes), max(sizes, default=0)
+        if U == 0 or kmax == 0:
+            raise ValueError("at least one user with a record is needed")
+        if all(k == kmax for k in sizes):
+            A_u = [a.reshape(U, kmax * a.shape[1], a.shape[2]) for a in A_list]
+            E_u = [e.reshape(U, kmax * e.shape[1], e.shape[2]) for e in E_list]
+        else:
+            starts = torch.zeros(U + 1, dtype=torch.int64)
+            starts[1:] = torch.cumsum(torch.tensor(sizes, dtype=torch.int64), 0)
+            starts = starts.to(self.device)
+            dt = _DT[self.dtype]
+
+            def pack(x):
+                out = torch.empty(U, kmax * x.shape[1], x.shape[2], dtype=x.dtype, device=self.device)
+                b.dp_pack_groups(x, out, B, x.shape[1], x.shape[2], dt, starts, U, kmax, self.stream)
+                return out
+            A_u = [pack(a) for a in A_list]
+            E_u = [pack(e) for e in E_list]
+        T_u = [kmax * int(t) for t in T_list]
+        return self.step(A_u, E_u, T_u, C=C, sigma=sigma, seed=seed, step=step, L=L, outputs=outputs)
+
     def prepare(self, A_list, E_list, T_list, outputs=None, L: float | None = None,
                 layer_norms: bool = False) -> "PreparedStep":
         """Marshal the pointer arrays of a step once, for repeated steps on the same buffers."""

@@ -213,6 +213,30 @@ dp_status dp_step_status(dp_ctx* ctx);
 const char* dp_last_error(const dp_ctx* ctx);
 
 /*
+ * dp_pack_groups -- lay out records grouped by user for user-level clipping
+ * ("Privacy-Preserving Machine Learning", section "Differentially private
+ * stochastic gradient descent", the user-level construction: records are
+ * grouped, a vector is built per user and that vector is clipped).  A user's
+ * vector is the sum of its records' gradients, sum_i E_i^T A_i = E_u^T A_u
+ * with A_u, E_u the user's records stacked along T, so a user of k records is
+ * one record of length k*T for every other call of this library.
+ *
+ * src: device [B, T, d] row-major (dtype DP_F32 or DP_BF16), the records of
+ * user u being src records group_starts[u] .. group_starts[u+1]-1;
+ * group_starts: device int64 [U+1], non-decreasing, group_starts[U] <= B;
+ * dst: device [U, kmax, T, d] (= [U, kmax*T, d]), written in full: slot s of
+ * user u is record group_starts[u] + s when that is below group_starts[u+1],
+ * else zeros (a zero record adds nothing to a norm or a sum).  kmax must be at
+ * least the largest group; records beyond it are dropped.  Source indices
+ * outside [0, B) read as zeros.  Launches on `stream` (NULL = legacy default);
+ * src, dst and group_starts are caller-owned.  DP_ERR_INVALID_ARG for NULL
+ * pointers or an unknown dtype, DP_ERR_SHAPE for negative sizes or T, d < 1,
+ * DP_ERR_CUDA for a launch failure.
+ */
+dp_status dp_pack_groups(const void* src, void* dst, int64_t B, int64_t T, int64_t d, int dtype,
+                         const int64_t* group_starts, int64_t U, int64_t kmax, void* stream);
+
+/*
  * dp_philox_normals -- the noise generator on its own, for testing: for
  * coordinates k0 .. k0+n-1 of the (seed, step) stream write z (device float
  * [n], if z_out != NULL) and the raw Philox words of blocks k0/4 ..
