@@ -52,6 +52,7 @@ struct SumParams {
     float scale;       // sigma * C
     float inv_L;       // 1 / L
     uint64_t seed, step;
+    int box3d;                      // 1: one 3D TMA copy per operand tile (64-column chunks as the outer dimension)
     // split of the last partial wave (records mode only; see next_work)
     int full_tiles;                 // tiles done whole, strided over the grid
     int nsplit;                     // record ranges per remaining tile (1: no split)
@@ -221,11 +222,16 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
                     uint8_t* st = tiles + (size_t)s * kStageBytes;
                     tc::mbar_arrive_expect_tx(&sh->full[s], kStageBytes);
                     const int k0 = kt * kBK;
-                    tc::tma_load_2d(st, &p.tmE, &sh->full[s], mb * kBM, k0);
-                    tc::tma_load_2d(st + 8192, &p.tmE, &sh->full[s], mb * kBM + 64, k0);
+                    if (p.box3d) {
+                        tc::tma_load_3d(st, &p.tmE, &sh->full[s], 0, k0, mb * (kBM / 64));
+                        tc::tma_load_3d(st + kAStage, &p.tmA, &sh->full[s], 0, k0, nb * (kBN / 64));
+                    } else {
+                        tc::tma_load_2d(st, &p.tmE, &sh->full[s], mb * kBM, k0);
+                        tc::tma_load_2d(st + 8192, &p.tmE, &sh->full[s], mb * kBM + 64, k0);
 #pragma unroll
-                    for (int q = 0; q < kBN / 64; ++q)
-                        tc::tma_load_2d(st + kAStage + q * 8192, &p.tmA, &sh->full[s], nb * kBN + 64 * q, k0);
+                        for (int q = 0; q < kBN / 64; ++q)
+                            tc::tma_load_2d(st + kAStage + q * 8192, &p.tmA, &sh->full[s], nb * kBN + 64 * q, k0);
+                    }
                 }
             }
         fold_producer_done:
@@ -495,6 +501,17 @@ bool tc_sum_supported(int dtype, int64_t d_in, int64_t d_out, int has_bias) {
 
 bool tc_encode_sum(const GradTask& t, int64_t B, CUtensorMap* maps2) {
     const int64_t K = B * t.T;
+    if (t.d_in % 64 == 0 && t.d_out % 64 == 0) {
+        // {64 columns, K rows, 64-column chunks}: one copy brings a whole tile
+        const uint32_t be[3] = {64, (uint32_t)kBK, (uint32_t)(kBM / 64)};
+        const uint32_t ba[3] = {64, (uint32_t)kBK, (uint32_t)(kBN / 64)};
+        const uint64_t de[3] = {64, (uint64_t)K, (uint64_t)(t.d_out / 64)};
+        const uint64_t se[2] = {(uint64_t)t.d_out * 2, 128};
+        const uint64_t da[3] = {64, (uint64_t)K, (uint64_t)(t.d_in / 64)};
+        const uint64_t sa[2] = {(uint64_t)t.d_in * 2, 128};
+        return encode(&maps2[0], t.E, 3, de, se, be, CU_TENSOR_MAP_SWIZZLE_128B) &&
+               encode(&maps2[1], t.A, 3, da, sa, ba, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
     const uint32_t box[2] = {64, (uint32_t)kBK};
     const uint64_t de[2] = {(uint64_t)t.d_out, (uint64_t)K};
     const uint64_t se[1] = {(uint64_t)t.d_out * 2};
@@ -528,6 +545,7 @@ cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* s
     }
     p.K = sc.B * t.T;
     p.T = t.T;
+    p.box3d = (t.d_in % 64 == 0 && t.d_out % 64 == 0) ? 1 : 0;
     p.d_in = t.d_in;
     p.d_out = t.d_out;
     p.m_blocks = (int)((t.d_out + kBM - 1) / kBM);
