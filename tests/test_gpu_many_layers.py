@@ -1,0 +1,67 @@
+"""Layer counts above one launch's group limits, and the status word across
+a sequence of steps (two words that steps alternate between)."""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import differentially_private_gb300 as dp
+from gpu_harness import assert_step_parity
+
+pytestmark = pytest.mark.gpu
+
+
+def test_more_lora_factors_than_one_skinny_launch_holds():
+    # 60 materialized rank-8 factors: two skinny launches (48 + 12) and one
+    # grouped weighted sum per 64 layers
+    layers, A, E, T = [], [], [], []
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    for i in range(30):
+        for (d_in, d_out) in ((256, 8), (8, 256)):
+            layers.append((d_in, d_out, False))
+            A.append(torch.randn(3, 96, d_in, device="cuda", generator=g).bfloat16())
+            E.append((torch.randn(3, 96, d_out, device="cuda", generator=g) * 0.03).bfloat16())
+            T.append(96)
+    assert all(dp.dp_choose_path(t, a, b) == dp.DP_PATH_MATERIALIZE for (a, b, _), t in zip(layers, T))
+    assert_step_parity(layers, A, E, T, C=0.5, sigma=1.0, seed=3, step=1)
+
+
+def test_more_t1_layers_than_one_group_launch_holds():
+    # 70 bf16 T = 1 layers: two grouped norm launches (64 + 6)
+    layers, A, E, T = [], [], [], []
+    g = torch.Generator(device="cuda")
+    g.manual_seed(12)
+    for i in range(70):
+        d_in, d_out = 64 + 8 * (i % 5), 72 + 8 * (i % 3)
+        layers.append((d_in, d_out, i % 7 == 0))
+        A.append(torch.randn(5, 1, d_in, device="cuda", generator=g).bfloat16())
+        E.append((torch.randn(5, 1, d_out, device="cuda", generator=g) * 0.1).bfloat16())
+        T.append(1)
+    assert_step_parity(layers, A, E, T, C=0.8, sigma=0.7, seed=4, step=2)
+
+
+def test_status_across_a_sequence_of_steps():
+    A = torch.randn(3, 4, 32, device="cuda")
+    E = torch.randn(3, 4, 16, device="cuda")
+    pg = dp.PrivateGradient([(32, 16, True)], dtype=torch.float32)
+    bad = E.clone()
+    bad[0, 0, 0] = float("inf")
+    results = []
+    for inp in (E, bad, E, E, bad, bad, E):
+        try:
+            pg.step([A], [inp], [4], C=1.0, sigma=1.0, seed=0, step=0)
+            results.append(dp.DP_OK)
+        except dp.DPError as err:
+            results.append(err.status)
+    assert results == [dp.DP_OK, dp.DP_ERR_NONFINITE, dp.DP_OK, dp.DP_OK, dp.DP_ERR_NONFINITE,
+                       dp.DP_ERR_NONFINITE, dp.DP_OK]
+    # a step abandoned before its clip factors (begin twice), then a full one
+    dp.dp_begin_step(pg.ctx, 3)
+    dp.dp_norm_accumulate(pg.ctx, 0, A, bad, 4, None)
+    out = pg.step([A], [E], [4], C=1.0, sigma=1.0, seed=0, step=0)
+    assert bool(torch.isfinite(out.grads[0]).all())
+    assert dp.dp_step_status(pg.ctx) == dp.DP_OK
+    pg.close()
