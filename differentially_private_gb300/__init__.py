@@ -31,6 +31,9 @@ from ._binding import (  # noqa: F401
     dp_clipped_noisy_grad,
     dp_create,
     dp_destroy,
+    dp_int8_forward,
+    dp_int8_quantize_weight,
+    dp_int8_workspace_bytes,
     dp_kernel_launches,
     dp_last_error,
     dp_layer_info,

@@ -36,6 +36,7 @@ EXPORTS = (
     "dp_layer_info", "dp_num_coords", "dp_choose_path", "dp_begin_step", "dp_set_normalizer",
     "dp_norm_accumulate", "dp_norm_accumulate_batch", "dp_clip_factors", "dp_clipped_noisy_grad",
     "dp_step_status", "dp_last_error", "dp_philox_normals", "dp_layer_sqnorms_static", "dp_pack_groups",
+    "dp_int8_quantize_weight", "dp_int8_workspace_bytes", "dp_int8_forward",
 )
 
 
@@ -87,6 +88,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "dp_philox_normals": (i32, [u64, u64, u64, i64, vp, vp, vp]),
         "dp_layer_sqnorms_static": (i32, [vp, vp, i64, i64, i64, i64, i32, i32, vp, vp]),
         "dp_pack_groups": (i32, [vp, vp, i64, i64, i64, i32, vp, i64, i64, vp]),
+        "dp_int8_quantize_weight": (i32, [vp, i64, i64, vp, vp, vp, vp]),
+        "dp_int8_workspace_bytes": (i64, [i64, i64, i64]),
+        "dp_int8_forward": (i32, [vp, i64, i64, i64, vp, vp, vp, i64, c.c_float, i32, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -232,3 +236,19 @@ def dp_pack_groups(src, dst, B: int, T: int, d: int, dtype: int, group_starts, U
     """Records grouped by user, laid out [U, kmax, T, d] with zero records where a user has fewer."""
     _check(load_library().dp_pack_groups(_ptr(src), _ptr(dst), int(B), int(T), int(d), int(dtype),
                                          _ptr(group_starts), int(U), int(kmax), _stream(stream)), "dp_pack_groups")
+
+
+def dp_int8_quantize_weight(W, N: int, K: int, Wq, sW, What, stream=None) -> None:
+    _check(load_library().dp_int8_quantize_weight(_ptr(W), int(N), int(K), _ptr(Wq), _ptr(sW), _ptr(What),
+                                                  _stream(stream)), "dp_int8_quantize_weight")
+
+
+def dp_int8_workspace_bytes(n: int, K: int, rows_per_record: int) -> int:
+    return int(load_library().dp_int8_workspace_bytes(int(n), int(K), int(rows_per_record)))
+
+
+def dp_int8_forward(A, n: int, K: int, rows_per_record: int, Wq, sW, What, N: int, tau: float, record_owned: bool,
+                    Y, workspace, stream=None) -> None:
+    _check(load_library().dp_int8_forward(_ptr(A), int(n), int(K), int(rows_per_record), _ptr(Wq), _ptr(sW),
+                                          _ptr(What), int(N), float(tau), int(bool(record_owned)), _ptr(Y),
+                                          _ptr(workspace), _stream(stream)), "dp_int8_forward")

@@ -237,6 +237,44 @@ dp_status dp_pack_groups(const void* src, void* dst, int64_t B, int64_t T, int64
                          const int64_t* group_starts, int64_t U, int64_t kmax, void* stream);
 
 /*
+ * Record-owned LLM.int8 forward of a frozen layer ("Sensitivity Inflation
+ * from Cross-Record Precision Routing in Private Quantized Fine-Tuning",
+ * section 4.2, Eq. 6 and Algorithm 1; Appendix A).  A producer of the
+ * activations a private adapter sees, kept record-isolated: a row's output
+ * depends only on its own record's rows.
+ *
+ * dp_int8_quantize_weight -- W: device half [N, K] row-major (caller-owned).
+ * Writes Wq (device int8 [N, K]) = rint(127 W / sW_n), sW (device float [N])
+ * = max_j |W_nj|, What (device half [N, K]) = half(Wq sW_n / 127); a zero row
+ * gives zeros.  DP_ERR_INVALID_ARG for NULL pointers, DP_ERR_SHAPE for N or
+ * K < 1.
+ *
+ * dp_int8_workspace_bytes -- bytes of the device workspace dp_int8_forward
+ * needs for n rows of K columns in records of rows_per_record rows; -1 for
+ * invalid sizes (n not a multiple of rows_per_record, K or rows < 1).
+ *
+ * dp_int8_forward -- A: device half [n, K] row-major, rows r*rows_per_record
+ * .. (r+1)*rows_per_record-1 owned by record r.  With O_r the columns where
+ * some row of record r has |A| >= tau (tau > 0), U their union, s_i the
+ * largest |A_ij| below tau in row i, and O = O_r of the row's record
+ * (record_owned != 0) or U (record_owned == 0, batched LLM.int8):
+ *   Q_ij = rint((127 A_ij) / s_i) for j not in O (0 when s_i = 0), else 0;
+ *   Y_in = half( ((float(sum_j Q_ij Wq_nj) * s_i) * sW_n) / 16129
+ *                + sum over j in O ascending of fma(A_ij, What_nj, .) )
+ * written to Y (device half [n, N]).  The integer sum is exact (K below
+ * 133,000).  workspace: device, 16-byte aligned, dp_int8_workspace_bytes
+ * bytes, overwritten.  Launches on `stream`.  DP_ERR_INVALID_ARG for NULL
+ * pointers, tau <= 0 or a misaligned workspace; DP_ERR_SHAPE for invalid
+ * sizes; DP_ERR_CUDA for a launch failure.
+ */
+dp_status dp_int8_quantize_weight(const void* W, int64_t N, int64_t K, int8_t* Wq, float* sW, void* What,
+                                  void* stream);
+int64_t dp_int8_workspace_bytes(int64_t n, int64_t K, int64_t rows_per_record);
+dp_status dp_int8_forward(const void* A, int64_t n, int64_t K, int64_t rows_per_record, const int8_t* Wq,
+                          const float* sW, const void* What, int64_t N, float tau, int record_owned, void* Y,
+                          void* workspace, void* stream);
+
+/*
  * dp_philox_normals -- the noise generator on its own, for testing: for
  * coordinates k0 .. k0+n-1 of the (seed, step) stream write z (device float
  * [n], if z_out != NULL) and the raw Philox words of blocks k0/4 ..
