@@ -94,9 +94,6 @@ __device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t threads) 
 }
 
 // ------------------------------------------------------------ fences
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -244,8 +241,6 @@ __device__ __forceinline__ void tmem_ld16x4(uint32_t taddr, float (&v)[4][16]) {
         for (int i = 0; i < 16; ++i) v[b][i] = __uint_as_float(r[16 * b + i]);
 }
 
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31) == 0; }
 
 }  // namespace tc
