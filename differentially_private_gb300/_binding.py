@@ -36,7 +36,7 @@ EXPORTS = (
     "dp_layer_info", "dp_num_coords", "dp_choose_path", "dp_begin_step", "dp_set_normalizer",
     "dp_norm_accumulate", "dp_norm_accumulate_batch", "dp_clip_factors", "dp_clipped_noisy_grad",
     "dp_step_status", "dp_last_error", "dp_philox_normals", "dp_layer_sqnorms_static", "dp_pack_groups",
-    "dp_int8_quantize_weight", "dp_int8_workspace_bytes", "dp_int8_forward",
+    "dp_int8_quantize_weight", "dp_int8_workspace_bytes", "dp_int8_forward", "dp_check_wait_timeout",
 )
 
 
@@ -86,6 +86,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "dp_step_status": (i32, [vp]),
         "dp_last_error": (c.c_char_p, [vp]),
         "dp_philox_normals": (i32, [u64, u64, u64, i64, vp, vp, vp]),
+        "dp_check_wait_timeout": (i32, [vp, c.c_uint32]),
         "dp_layer_sqnorms_static": (i32, [vp, vp, i64, i64, i64, i64, i32, i32, vp, vp]),
         "dp_pack_groups": (i32, [vp, vp, i64, i64, i64, i32, vp, i64, i64, vp]),
         "dp_int8_quantize_weight": (i32, [vp, i64, i64, vp, vp, vp, vp]),
@@ -221,6 +222,11 @@ def dp_last_error(ctx) -> str:
 def dp_philox_normals(seed: int, step: int, k0: int, n: int, raw_out=None, z_out=None, stream=None) -> None:
     _check(load_library().dp_philox_normals(int(seed) & (2 ** 64 - 1), int(step) & (2 ** 64 - 1), int(k0), int(n),
                                             _ptr(raw_out), _ptr(z_out), _stream(stream)), "dp_philox_normals")
+
+
+def dp_check_wait_timeout(ctx, limit_ms: int) -> None:
+    """Enqueue the bounded wait that gives up (test hook of the timeout path)."""
+    _check(load_library().dp_check_wait_timeout(ctx, int(limit_ms)), "dp_check_wait_timeout", ctx)
 
 
 def dp_layer_sqnorms_static(A, E, B: int, T: int, d_in: int, d_out: int, has_bias: bool, dtype: int,

@@ -30,18 +30,34 @@ constexpr int kClipLoads = 8;
 constexpr int kClipMaxThreads = 512;
 constexpr int kClipWarpBlock = 256;   // warp-per-record mode: 8 records per block
 
+// G = smallest power of two with G * kClipLoads >= total_slots, at least a
+// warp and at most kClipMaxThreads; it depends on the shapes only
+int clip_group(int64_t total_slots) {
+    int G = 32;
+    while (G < kClipMaxThreads && (int64_t)G * kClipLoads < total_slots) G *= 2;
+    return G;
+}
+
 template <bool kWarpPerRecord>
 __global__ void __launch_bounds__(kClipMaxThreads) k_clip(const ClipParams p, float* __restrict__ n2_out,
                                                           float* __restrict__ c_out, float* __restrict__ n2_user,
                                                           float* __restrict__ c_user, unsigned* __restrict__ status) {
     __shared__ float red[32];
-    grid_dep_wait();
-    grid_dep_trigger();
-    if (p.status_next && blockIdx.x == 0 && threadIdx.x == 0) *p.status_next = 0u;
     const int64_t rec = kWarpPerRecord ? (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)
                                        : (int64_t)blockIdx.x;
     const int t = kWarpPerRecord ? (int)(threadIdx.x & 31) : (int)threadIdx.x;
     const int G = kWarpPerRecord ? 32 : (int)blockDim.x;
+    // the slot table comes from the host, never from an earlier kernel: the
+    // thread's first entries are fetched while the norm kernels still run
+    SlotRef first[kClipLoads];
+#pragma unroll
+    for (int u = 0; u < kClipLoads; ++u) {
+        const int64_t j = t + (int64_t)u * G;
+        first[u] = j < p.total_slots ? p.slots[j] : SlotRef{nullptr, 0};
+    }
+    grid_dep_wait();
+    grid_dep_trigger();
+    if (p.status_next && blockIdx.x == 0 && threadIdx.x == 0) *p.status_next = 0u;
     float s = 0.f;
     if (rec < p.B) {   // uniform per warp in warp mode; always true in block mode
         for (int64_t j0 = t; j0 < p.total_slots; j0 += (int64_t)G * kClipLoads) {
@@ -51,7 +67,7 @@ __global__ void __launch_bounds__(kClipMaxThreads) k_clip(const ClipParams p, fl
                 const int64_t j = j0 + (int64_t)u * G;
                 v[u] = 0.f;
                 if (j < p.total_slots) {
-                    const SlotRef r = p.slots[j];
+                    const SlotRef r = j0 == t ? first[u] : p.slots[j];
                     v[u] = __ldcg(r.base + rec * r.stride);
                 }
             }
@@ -88,6 +104,26 @@ struct WsumParams {
     GradTask t[kMaxGroup];
 };
 
+// acc += c_i g_i[p .. p+3] for records i .. i+N-1 in ascending order, all N loads issued first
+template <int N>
+__device__ __forceinline__ void wsum_round(const float4* g4, int64_t stride4, const float* c, int64_t i,
+                                           float4& acc) {
+    float4 v[N];
+    float cv[N];
+#pragma unroll
+    for (int u = 0; u < N; ++u) {
+        v[u] = __ldcg(g4 + (i + u) * stride4);
+        cv[u] = __ldca(c + i + u);
+    }
+#pragma unroll
+    for (int u = 0; u < N; ++u) {
+        acc.x = fmaf(cv[u], v[u].x, acc.x);
+        acc.y = fmaf(cv[u], v[u].y, acc.y);
+        acc.z = fmaf(cv[u], v[u].z, acc.z);
+        acc.w = fmaf(cv[u], v[u].w, acc.w);
+    }
+}
+
 // blockIdx.y = layer of the group; each thread owns one Philox block of the
 // layer's coordinates (up to 4 coordinates) and sums c_i g_i[p] over records
 // in ascending order.
@@ -113,23 +149,9 @@ __global__ void __launch_bounds__(256) k_grad_wsum(const WsumParams P, const flo
             const int64_t stride4 = ncl / 4;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             int64_t i = 0;
-            // records in ascending order; eight records' loads in flight per thread
-            for (; i + 8 <= sc.B; i += 8) {
-                float4 v[8];
-                float cv[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    v[u] = __ldcg(g4 + (i + u) * stride4);
-                    cv[u] = __ldca(c + i + u);
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    acc.x = fmaf(cv[u], v[u].x, acc.x);
-                    acc.y = fmaf(cv[u], v[u].y, acc.y);
-                    acc.z = fmaf(cv[u], v[u].z, acc.z);
-                    acc.w = fmaf(cv[u], v[u].w, acc.w);
-                }
-            }
+            // records in ascending order; sixteen (then eight) records' loads in flight per thread
+            for (; i + 16 <= sc.B; i += 16) wsum_round<16>(g4, stride4, c, i, acc);
+            for (; i + 8 <= sc.B; i += 8) wsum_round<8>(g4, stride4, c, i, acc);
             for (; i < sc.B; ++i) {
                 const float4 v = __ldcg(g4 + i * stride4);
                 const float ci = __ldca(c + i);
@@ -312,18 +334,20 @@ __global__ void k_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int6
 }  // namespace
 
 cudaError_t launch_clip(const ClipParams& p, float* n2, float* c, float* n2_user, float* c_user,
-                        unsigned* status, cudaStream_t s) {
-    // G = smallest power of two with G * kClipLoads >= total_slots, at least
-    // a warp and at most kClipMaxThreads; it depends on the shapes only
+                        unsigned* status, bool table_uploaded, cudaStream_t s) {
     cudaError_t e;
-    int G = 32;
-    while (G < kClipMaxThreads && (int64_t)G * kClipLoads < p.total_slots) G *= 2;
+    const int G = clip_group(p.total_slots);
+    // the kernel reads the slot table before its dependency wait: after a
+    // fresh upload it is launched as an ordinary (fully ordered) launch
+    const bool dep = !table_uploaded;
     if (G == 32) {
         const int per_block = kClipWarpBlock / 32;
         const unsigned grid = (unsigned)((p.B + per_block - 1) / per_block);
-        e = launch_dependent(k_clip<true>, dim3(grid), dim3(kClipWarpBlock), 0, s, p, n2, c, n2_user, c_user, status);
+        e = launch_maybe_dependent(dep, k_clip<true>, dim3(grid), dim3(kClipWarpBlock), 0, s, p, n2, c, n2_user,
+                                   c_user, status);
     } else {
-        e = launch_dependent(k_clip<false>, dim3((unsigned)p.B), dim3(G), 0, s, p, n2, c, n2_user, c_user, status);
+        e = launch_maybe_dependent(dep, k_clip<false>, dim3((unsigned)p.B), dim3(G), 0, s, p, n2, c, n2_user, c_user,
+                                   status);
     }
     count_launches(1);
     return e;

@@ -83,6 +83,10 @@ struct ClipParams {
     unsigned* status_next;     // status word of the next step, zeroed by the kernel (or nullptr)
 };
 
+// one-thread kernel whose bounded wait on a barrier nobody completes gives up
+// after limit_ns and sets the timeout bit of *status (waitcheck.cu)
+cudaError_t launch_wait_expiry(unsigned* status, uint64_t limit_ns, cudaStream_t s);
+
 // ---- every kernel launch of the library is counted here (dp_kernel_launches)
 void count_launches(int n);
 
@@ -101,7 +105,7 @@ cudaError_t launch_norm_ghost_cc(const NormTask& t, int64_t B, cudaStream_t s);
 cudaError_t launch_norm_mat_cc(const NormTask& t, int64_t B, cudaStream_t s);
 cudaError_t launch_layer_sqnorm(const float* partial, int nslots, int64_t B, float* out, cudaStream_t s);
 cudaError_t launch_clip(const ClipParams& p, float* n2, float* c, float* n2_user, float* c_user,
-                        unsigned* status, cudaStream_t s);
+                        unsigned* status, bool table_uploaded, cudaStream_t s);
 cudaError_t launch_grad_wsum(const GradTask* tasks, int n, const float* c, const unsigned* status,
                              const StepScalars& sc, cudaStream_t s);
 cudaError_t launch_grad_gemm_cc(const GradTask& t, const float* c, const unsigned* status,

@@ -595,7 +595,8 @@ dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnor
         key[l] = {ctx->layers[l].partial, (int64_t)ctx->layers[l].nslots};
         total += ctx->layers[l].nslots;
     }
-    if (key != ctx->slots_key) {
+    const bool upload = key != ctx->slots_key;
+    if (upload) {
         // the flat slot table changes only when the layer set or its scratch does
         if (ctx->d_slots_cap < (size_t)total) {
             cudaError_t e = cudaStreamSynchronize(ctx->stream);
@@ -625,7 +626,7 @@ dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnor
     // the clip kernel also zeroes the other status word for the next step
     // (every kernel that could write it belongs to an earlier, finished step)
     p.status_next = ctx->status_words + (ctx->slot ^ 1);
-    const cudaError_t e = launch_clip(p, ctx->n2, ctx->c, total_sqnorm_out, c_out, ctx->status, ctx->stream);
+    const cudaError_t e = launch_clip(p, ctx->n2, ctx->c, total_sqnorm_out, c_out, ctx->status, upload, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "clip kernel launch");
     ctx->clean[ctx->slot ^ 1] = true;
     ctx->C = C;
@@ -707,7 +708,17 @@ dp_status dp_step_status(dp_ctx* ctx) {
     e = cudaMemcpy(&word, ctx->status, sizeof word, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "status read");
     if (word & 1u) return fail(ctx, DP_ERR_NONFINITE, "a per-example gradient norm was not finite");
+    if (word) return fail(ctx, DP_ERR_CUDA, "a device-side wait timed out; the step's outputs were not written");
     return DP_OK;
+}
+
+dp_status dp_check_wait_timeout(dp_ctx* ctx, uint32_t limit_ms) {
+    if (!ctx) return DP_ERR_INVALID_ARG;
+    if (ctx->phase == IDLE) return fail(ctx, DP_ERR_STATE, "dp_check_wait_timeout needs an open step");
+    if (limit_ms < 1 || limit_ms > 2000) return fail(ctx, DP_ERR_INVALID_ARG, "limit_ms must be in 1..2000");
+    DeviceGuard g(ctx->device);
+    const cudaError_t e = launch_wait_expiry(ctx->status, (uint64_t)limit_ms * 1000000ull, ctx->stream);
+    return e == cudaSuccess ? DP_OK : cuda_fail(ctx, e, "wait check launch");
 }
 
 const char* dp_last_error(const dp_ctx* ctx) { return ctx ? ctx->err.c_str() : ""; }

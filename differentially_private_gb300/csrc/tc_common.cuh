@@ -57,21 +57,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete.  Returns false when
-// the CTA is aborting (flag already set, or this wait timed out).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned* status) {
+// Wait for the phase with the given parity to complete, at most limit_ns.
+// Returns false when the CTA is aborting (flag already set, or this wait
+// timed out: then the flag and the status word's timeout bit are set).
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              unsigned* status, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
         if (*abort_flag) return false;
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 > limit_ns) {
             *abort_flag = 1;
             atomicOr(status, kStatusTimeout);
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned* status) {
+    return mbar_wait_for(bar, parity, abort_flag, status, kWaitLimitNs);
 }
 
 // Wait used only while draining before exit: ignores the abort flag, gives

@@ -205,7 +205,9 @@ dp_status dp_clipped_noisy_grad(dp_ctx* ctx, float sigma, uint64_t seed, uint64_
 /*
  * dp_step_status -- synchronize the context's stream and return the deferred
  * device-side result of the step: DP_OK, DP_ERR_NONFINITE, or DP_ERR_CUDA for
- * an asynchronous CUDA error.
+ * an asynchronous CUDA error or a device-side wait that gave up (a kernel
+ * waits at most 2 s for its own copies and MMAs; the step's G is then not
+ * written).
  */
 dp_status dp_step_status(dp_ctx* ctx);
 
@@ -283,6 +285,19 @@ dp_status dp_int8_forward(const void* A, int64_t n, int64_t K, int64_t rows_per_
  */
 dp_status dp_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int64_t n,
                             uint32_t* raw_out, float* z_out, void* stream);
+
+/*
+ * dp_check_wait_timeout -- test hook for the failure path of the device-side
+ * waits.  Every wait of the tensor-core kernels on their own copies and MMAs
+ * is bounded; one that gives up sets the timeout bit of the step's status
+ * word, the gradient kernels then write nothing, and dp_step_status reports
+ * DP_ERR_CUDA.  This call enqueues, on the context's stream, a one-thread
+ * kernel whose wait on a barrier that nothing completes gives up after
+ * limit_ms milliseconds (1..2000, DP_ERR_INVALID_ARG otherwise) and takes
+ * that path.  Needs an open step (DP_ERR_STATE otherwise); the next step is
+ * not affected.
+ */
+dp_status dp_check_wait_timeout(dp_ctx* ctx, uint32_t limit_ms);
 
 /*
  * dp_layer_sqnorms_static -- per-example squared gradient norms of ONE layer

@@ -65,3 +65,27 @@ def test_status_across_a_sequence_of_steps():
     assert bool(torch.isfinite(out.grads[0]).all())
     assert dp.dp_step_status(pg.ctx) == dp.DP_OK
     pg.close()
+
+
+def test_device_wait_timeout_is_reported_and_skips_writes():
+    # a bounded device-side wait that gives up (a barrier nothing completes)
+    # takes the same path as a stuck copy or MMA in the tensor-core kernels
+    A = torch.randn(3, 4, 32, device="cuda")
+    E = torch.randn(3, 4, 16, device="cuda")
+    pg = dp.PrivateGradient([(32, 16, True)], dtype=torch.float32)
+    G = [torch.full((16 * 32 + 16,), 5.0, device="cuda")]
+    dp.dp_begin_step(pg.ctx, 3)
+    dp.dp_norm_accumulate(pg.ctx, 0, A, E, 4, None)
+    dp.dp_check_wait_timeout(pg.ctx, 20)
+    dp.dp_clip_factors(pg.ctx, 1.0, None, None)
+    dp.dp_clipped_noisy_grad(pg.ctx, 1.0, 0, 0, G)
+    assert dp.dp_step_status(pg.ctx) == dp.DP_ERR_CUDA
+    assert "timed out" in dp.dp_last_error(pg.ctx)
+    assert bool((G[0] == 5.0).all())
+    # outside a step the hook is refused; the next step is clean
+    with pytest.raises(dp.DPError) as err:
+        dp.dp_check_wait_timeout(pg.ctx, 20)
+    assert err.value.status == dp.DP_ERR_STATE
+    out = pg.step([A], [E], [4], C=1.0, sigma=1.0, seed=0, step=0)
+    assert bool(torch.isfinite(out.grads[0]).all())
+    pg.close()
