@@ -27,6 +27,7 @@ namespace {
 // reduction (G = blockDim) combines the threads.  G depends on total_slots
 // only, never on B, so a record's norm does not depend on the batch.
 constexpr int kClipLoads = 8;
+constexpr int kScalePre = 8;          // pre-scale units a thread fetches before the dependency wait
 constexpr int kClipMaxThreads = 512;
 constexpr int kClipWarpBlock = 256;   // warp-per-record mode: 8 records per block
 
@@ -38,6 +39,39 @@ int clip_group(int64_t total_slots) {
     return G;
 }
 
+// c * (8 bf16), rounded to bf16 (the pre-scaled operand of the tensor-core sum)
+__device__ __forceinline__ uint4 scale_bf16x8(uint4 v, float c) {
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w[i]);
+        const float2 f = __bfloat1622float2(h);
+        h = __floats2bfloat162_rn(f.x * c, f.y * c);
+        w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return v;
+}
+
+// Unit x (16 bytes) of record rec's rows over the pre-scale jobs, jobs in order.
+__device__ __forceinline__ bool scale_unit(const ClipParams& p, int64_t x, int64_t rec, const uint4** src,
+                                           uint4** dst) {
+    for (int j = 0; j < p.nscale; ++j) {
+        const int64_t n = p.scale[j].units;
+        if (x < n) {
+            *src = p.scale[j].src + rec * n + x;
+            *dst = p.scale[j].dst + rec * n + x;
+            return true;
+        }
+        x -= n;
+    }
+    return false;
+}
+
+// Besides n2 and c, the record's group of G threads writes the pre-scaled
+// copies c_i * X_i of the operands of the layers whose tensor-core sum runs
+// as one record (p.scale): those operands were written before the norm
+// kernels ran, so each thread fetches its first units of them before the
+// dependency wait and scales them as soon as c_i is known.
 template <bool kWarpPerRecord>
 __global__ void __launch_bounds__(kClipMaxThreads) k_clip(const ClipParams p, float* __restrict__ n2_out,
                                                           float* __restrict__ c_out, float* __restrict__ n2_user,
@@ -54,6 +88,15 @@ __global__ void __launch_bounds__(kClipMaxThreads) k_clip(const ClipParams p, fl
     for (int u = 0; u < kClipLoads; ++u) {
         const int64_t j = t + (int64_t)u * G;
         first[u] = j < p.total_slots ? p.slots[j] : SlotRef{nullptr, 0};
+    }
+    int64_t units = 0;
+    for (int j = 0; j < p.nscale; ++j) units += p.scale[j].units;
+    uint4 pre[kScalePre];
+#pragma unroll
+    for (int k = 0; k < kScalePre; ++k) {
+        const uint4* src;
+        uint4* dst;
+        if (rec < p.B && scale_unit(p, t + (int64_t)k * G, rec, &src, &dst)) pre[k] = __ldcs(src);
     }
     grid_dep_wait();
     grid_dep_trigger();
@@ -81,20 +124,28 @@ __global__ void __launch_bounds__(kClipMaxThreads) k_clip(const ClipParams p, fl
     } else {
         s = block_sum(s, red);
     }
+    // every thread of the group holds the same s, so the same c
+    const bool finite = isfinite(s);
+    // C / n rounded toward zero keeps c * n <= C in float arithmetic
+    const float c = !finite ? 0.f : (sqrtf(s) <= p.C ? 1.0f : __fdiv_rz(p.C, sqrtf(s)));
     if (t == 0) {
-        float c;
-        if (!isfinite(s)) {
-            atomicOr(status, 1u);
-            c = 0.f;
-        } else {
-            const float n = sqrtf(s);
-            // C / n rounded toward zero keeps c * n <= C in float arithmetic
-            c = (n <= p.C) ? 1.0f : __fdiv_rz(p.C, n);
-        }
+        if (!finite) atomicOr(status, 1u);
         n2_out[rec] = s;
         c_out[rec] = c;
         if (n2_user) n2_user[rec] = s;
         if (c_user) c_user[rec] = c;
+    }
+#pragma unroll
+    for (int k = 0; k < kScalePre; ++k) {
+        const uint4* src;
+        uint4* dst;
+        if (scale_unit(p, t + (int64_t)k * G, rec, &src, &dst)) *dst = scale_bf16x8(pre[k], c);
+    }
+    for (int64_t x = t + (int64_t)kScalePre * G; x < units; x += G) {
+        const uint4* src;
+        uint4* dst;
+        scale_unit(p, x, rec, &src, &dst);
+        *dst = scale_bf16x8(__ldcs(src), c);
     }
 }
 

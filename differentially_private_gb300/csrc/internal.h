@@ -75,12 +75,24 @@ struct SlotRef {
     int64_t stride;
 };
 
+// One operand the clip kernel copies scaled by c_i, row block by row block:
+// record i's rows are units [i * units, (i + 1) * units) of 16 bytes (8 bf16)
+// of src, written to the same place of dst.
+struct PrescaleJob {
+    const uint4* src;
+    uint4* dst;
+    int64_t units;
+};
+constexpr int kMaxPrescale = 4;
+
 struct ClipParams {
     int64_t B;
     float C;
     const SlotRef* slots;      // device array: layers in registration order, each layer's slots in order
     int64_t total_slots;
     unsigned* status_next;     // status word of the next step, zeroed by the kernel (or nullptr)
+    int nscale;                // pre-scaled operand copies made by the clip kernel
+    PrescaleJob scale[kMaxPrescale];
 };
 
 // one-thread kernel whose bounded wait on a barrier nobody completes gives up

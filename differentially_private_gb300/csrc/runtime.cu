@@ -53,6 +53,7 @@ struct Layer {
     bool prescale = false;     // clip factors folded into a bf16 copy of one operand
     bool prescale_A = false;   // that operand is A (fewer columns than E), else E
     float* escaled = nullptr;  // the pre-scaled copy
+    bool scaled_by_clip = false;   // this step's copy is written by the clip kernel
     size_t escaled_cap = 0;   // floats (two bf16 each)
     // TMA descriptors of the tensor-core kernels, encoded once per request
     // shape: reused while (A, E, T, B) stay the same from step to step
@@ -626,6 +627,15 @@ dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnor
     // the clip kernel also zeroes the other status word for the next step
     // (every kernel that could write it belongs to an earlier, finished step)
     p.status_next = ctx->status_words + (ctx->slot ^ 1);
+    // the clip kernel also writes the first kMaxPrescale pre-scaled operand copies
+    p.nscale = 0;
+    for (Layer& ly : ctx->layers) {
+        ly.scaled_by_clip = ly.grad_kernel == GK_GEMM_TC && ly.prescale && p.nscale < kMaxPrescale;
+        if (!ly.scaled_by_clip) continue;
+        const int64_t d = ly.prescale_A ? ly.d_in : ly.d_out;
+        p.scale[p.nscale++] = PrescaleJob{static_cast<const uint4*>(ly.prescale_A ? ly.A : ly.E),
+                                          reinterpret_cast<uint4*>(ly.escaled), ly.T * d / 8};
+    }
     const cudaError_t e = launch_clip(p, ctx->n2, ctx->c, total_sqnorm_out, c_out, ctx->status, upload, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "clip kernel launch");
     ctx->clean[ctx->slot ^ 1] = true;
@@ -672,8 +682,9 @@ dp_status dp_clipped_noisy_grad(dp_ctx* ctx, float sigma, uint64_t seed, uint64_
         if (ly.grad_kernel == GK_GEMM_TC && ly.prescale) {
             // c_i folded into a bf16 copy of the narrower operand, then one "record" of B*T rows with factor 1
             const int64_t K = ctx->B * ly.T;
-            e = ly.prescale_A ? launch_prescale_rows(ly.A, ly.escaled, ctx->c, K, ly.T, ly.d_in, ctx->stream)
-                              : launch_prescale_rows(ly.E, ly.escaled, ctx->c, K, ly.T, ly.d_out, ctx->stream);
+            e = ly.scaled_by_clip ? cudaSuccess
+                : ly.prescale_A   ? launch_prescale_rows(ly.A, ly.escaled, ctx->c, K, ly.T, ly.d_in, ctx->stream)
+                                  : launch_prescale_rows(ly.E, ly.escaled, ctx->c, K, ly.T, ly.d_out, ctx->stream);
             GradTask ts = t;
             if (ly.prescale_A) ts.A = ly.escaled;
             else ts.E = ly.escaled;
