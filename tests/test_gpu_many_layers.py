@@ -89,3 +89,33 @@ def test_device_wait_timeout_is_reported_and_skips_writes():
     out = pg.step([A], [E], [4], C=1.0, sigma=1.0, seed=0, step=0)
     assert bool(torch.isfinite(out.grads[0]).all())
     pg.close()
+
+
+def test_many_ragged_skinny_blocks_match_oracle_repeat_and_are_batch_invariant():
+    # 2880 128-column blocks (8 layers x 40 records x 9 blocks, D = 1088 and
+    # T = 140 both ragged) over the CTAs' ranges, ranges ending inside records
+    layers, A, E, T = [], [], [], []
+    g = torch.Generator(device="cuda")
+    g.manual_seed(13)
+    for i in range(4):
+        for (d_in, d_out) in ((1088, 16), (16, 1088)):
+            layers.append((d_in, d_out, False))
+            A.append(torch.randn(40, 140, d_in, device="cuda", generator=g).bfloat16())
+            E.append((torch.randn(40, 140, d_out, device="cuda", generator=g) * 0.02).bfloat16())
+            T.append(140)
+    assert all(dp.dp_choose_path(t, a, b) == dp.DP_PATH_MATERIALIZE for (a, b, _), t in zip(layers, T))
+    out, _, _ = assert_step_parity(layers, A, E, T, C=0.5, sigma=1.0, seed=5, step=3)
+    pg = dp.PrivateGradient(layers, dtype=torch.bfloat16)
+    runs = [pg.step(A, E, T, C=0.5, sigma=1.0, seed=5, step=3, layer_norms=True) for _ in range(3)]
+    torch.cuda.synchronize()
+    for r in runs:
+        assert torch.equal(r.sqnorm, out.sqnorm)
+        for a, b in zip(r.grads, out.grads):
+            assert torch.equal(a, b)
+    # a record's norms alone equal its norms inside the batch
+    one = pg.step([a[7:8].clone() for a in A], [e[7:8].clone() for e in E], T, C=0.5, sigma=1.0, seed=5, step=3,
+                  layer_norms=True)
+    torch.cuda.synchronize()
+    for l in range(len(layers)):
+        assert torch.equal(one.layer_sqnorm[l][0], out.layer_sqnorm[l][7])
+    pg.close()
