@@ -7,8 +7,9 @@ range writes a partial sum and the CTA that arrives last at the tile adds
 them in range order.  These cases put every tile, or the last wave, into
 that mode and check G tile by tile against the oracle at sigma = 0, that the
 noise of every coordinate is added exactly once, and that repeats are
-bitwise equal.  A single pre-scaled record (T not a multiple of 64) stays
-on whole tiles and is checked the same way.
+bitwise equal.  Layers of one pre-scaled record (T not a multiple of 64:
+the clip kernel writes c_i X_i, and the sum runs on whole tiles) are checked
+the same way, several layers and several row counts in one step.
 """
 
 from __future__ import annotations
@@ -85,3 +86,44 @@ def test_split_tiles_repeat_bitwise():
         torch.cuda.synchronize()
         runs.append(out.grads[0].clone())
     assert torch.equal(runs[0], runs[1]) and torch.equal(runs[0], runs[2])
+
+
+def test_prescaled_layers_match_oracle_noise_once_and_repeat():
+    """Four pre-scaled layers (all written by the clip kernel) of two row
+    counts, ragged shapes (2D tensor maps, partial tiles), at sigma = 0 tile
+    by tile, the noise once per coordinate, and bitwise repeats."""
+    from differentially_private_gb300 import PrivateGradient
+    B = 300
+    shapes = [(1024, 512, 3), (512, 1024, 3), (320, 200, 3), (640, 384, 5)]
+    layers = [(d_in, d_out, False) for (d_in, d_out, _) in shapes]
+    A, E, T = [], [], []
+    for i, (d_in, d_out, t) in enumerate(shapes):
+        a, e = _inputs(B, t, d_in, d_out, seed=40 + i)
+        A.append(a)
+        E.append(e)
+        T.append(t)
+    C, sigma, seed, step = 0.8, 1.1, 21, 6
+    out0, _ = gpu_step(layers, A, E, T, C, 0.0, seed, step, layer_norms=False)
+    outs, _ = gpu_step(layers, A, E, T, C, sigma, seed, step, layer_norms=False)
+    ref = oracle_step(layers, A, E, T, C, 0.0, seed, step)
+    off = 0
+    for l, (d_in, d_out, _) in enumerate(shapes):
+        S, _ = ref.clipped[l]
+        G0 = to64(out0.grads[l]).reshape(d_out, d_in)
+        errs = _tile_errors(G0, S / B, d_out, d_in)
+        assert np.all(errs <= G_RTOL), (l, errs.max(), int(errs.argmax()))
+        Gs = to64(outs.grads[l]).reshape(d_out, d_in)
+        z = philox.normals(seed, step, off, d_out * d_in).reshape(d_out, d_in)
+        tol = 1e-3 * sigma * C / B + 4e-7 * np.abs(G0) + 1e-5 * np.abs(S).max() / B
+        bad = np.abs(Gs - G0 - sigma * C * z / B) > tol
+        assert not bad.any(), (l, int(bad.sum()), np.argwhere(bad)[:4])
+        off += d_out * d_in
+    pg = PrivateGradient(layers, dtype=torch.bfloat16)
+    runs = []
+    for _ in range(3):
+        out = pg.step(A, E, T, C=C, sigma=sigma, seed=seed, step=step)
+        torch.cuda.synchronize()
+        runs.append([g.clone() for g in out.grads])
+    for r in runs[1:]:
+        assert all(torch.equal(a, b) for a, b in zip(runs[0], r))
+    pg.close()
