@@ -1,4 +1,5 @@
-// Clip factors, the reweighted clipped sum with its noise epilogue on the
+// Clip factors (with the pre-scaled operand copies of single-record
+// tensor-core sums), the reweighted clipped sum with its noise epilogue on the
 // CUDA cores, the weighted sum of stored per-example gradients, and the
 // standalone noise generator.
 //

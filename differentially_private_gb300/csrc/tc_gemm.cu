@@ -8,10 +8,10 @@
 //    stochastic gradient descent", phases 3-5; "Sensitivity Inflation from
 //    Cross-Record Precision Routing in Private Quantized Fine-Tuning", Eq. 3).
 //    When T is a multiple of 64 the clip factor is folded per record in fp32
-//    (below).  Otherwise the runtime first writes c_i A_i or c_i E_i (the
-//    operand with fewer columns) into scratch (k_prescale_rows, the clip
-//    factor folded into the staged operand) and runs this kernel as a single
-//    "record" of K rows with factor 1.
+//    (below).  Otherwise c_i A_i or c_i E_i (the operand with fewer columns)
+//    is first written into scratch -- by the clip kernel as soon as c_i is
+//    known (k_prescale_rows beyond four such layers) -- and this kernel runs
+//    as a single "record" of K rows with factor 1.
 //
 // Warp roles (one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer (one lane)
