@@ -233,15 +233,18 @@ __global__ void __launch_bounds__(256) k_grad_wsum(const WsumParams P, const flo
 }
 
 // ---------------------------------------- reweighted E^T diag(c) A (CUDA core)
-constexpr int kBM = 64, kBN = 64, kBK = 16;
+constexpr int kBM = 64, kBN = 64, kBK = 32;
+constexpr int kGemmLoads = kBK * kBM / 256;   // elements of each operand a thread stages per chunk
 
+// One 64 x 64 tile of G per block, K in chunks of 32 rows.  A and E were
+// written before the step's first kernel (at least two launches back), so
+// the block fetches its first chunk before the dependency wait, which guards
+// only c and the status word; each later chunk (with its clip factors) is
+// fetched into registers while the block computes on the one before.
 template <int DT>
 __global__ void __launch_bounds__(256) k_grad_gemm_cc(const GradTask t, const float* __restrict__ c,
                                                       const unsigned* __restrict__ status, StepScalars sc) {
     using Tt = typename Elem<DT>::T;
-    grid_dep_wait();
-    grid_dep_trigger();
-    if (status_bad(status)) return;
     __shared__ float Es[kBK][kBM];
     __shared__ float As[kBK][kBN];
     const int tid = threadIdx.x;
@@ -250,26 +253,42 @@ __global__ void __launch_bounds__(256) k_grad_gemm_cc(const GradTask t, const fl
     const int64_t K = sc.B * t.T;
     const Tt* E = (const Tt*)t.E;
     const Tt* A = (const Tt*)t.A;
+    // the thread's places of a chunk: row idx >> 6, column idx & 63, idx = tid + 256 r
+    float er[kGemmLoads], ar[kGemmLoads], cr[kGemmLoads];
+    auto fetch = [&](int64_t k0, bool with_c) {
+#pragma unroll
+        for (int r = 0; r < kGemmLoads; ++r) {
+            const int idx = tid + 256 * r;
+            const int64_t k = k0 + (idx >> 6);
+            const int col = idx & 63;
+            er[r] = (k < K && m0 + col < t.d_out) ? Elem<DT>::ld(E + k * t.d_out + m0 + col) : 0.f;
+            ar[r] = (k < K && n0 + col < t.d_in) ? Elem<DT>::ld(A + k * t.d_in + n0 + col) : 0.f;
+            if (with_c) cr[r] = k < K ? __ldca(c + k / t.T) : 0.f;
+        }
+    };
+    fetch(0, false);
+    grid_dep_wait();
+    grid_dep_trigger();
+    if (status_bad(status)) return;
+#pragma unroll
+    for (int r = 0; r < kGemmLoads; ++r) {
+        const int64_t k = (tid + 256 * r) >> 6;
+        cr[r] = k < K ? __ldca(c + k / t.T) : 0.f;
+    }
     float acc[4][4] = {};
     float bsum = 0.f;
     const bool do_bias = t.has_bias && blockIdx.x == 0;
     for (int64_t k0 = 0; k0 < K; k0 += kBK) {
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
+        for (int r = 0; r < kGemmLoads; ++r) {
             const int idx = tid + 256 * r;
             const int kk = idx >> 6, col = idx & 63;
-            const int64_t k = k0 + kk;
-            float e = 0.f, a = 0.f;
-            if (k < K) {
-                const float ck = __ldca(c + k / t.T);
-                if (m0 + col < t.d_out) e = ck * Elem<DT>::ld(E + k * t.d_out + m0 + col);
-                if (n0 + col < t.d_in) a = Elem<DT>::ld(A + k * t.d_in + n0 + col);
-            }
-            Es[kk][col] = e;
-            As[kk][col] = a;
+            Es[kk][col] = cr[r] * er[r];
+            As[kk][col] = ar[r];
         }
         __syncthreads();
-#pragma unroll
+        if (k0 + kBK < K) fetch(k0 + kBK, true);
+#pragma unroll 8
         for (int kk = 0; kk < kBK; ++kk) {
             float ev[4], av[4];
 #pragma unroll
@@ -286,18 +305,32 @@ __global__ void __launch_bounds__(256) k_grad_gemm_cc(const GradTask t, const fl
         }
         __syncthreads();
     }
+    // the epilogue stays rolled: small launches of this kernel run with a
+    // cold instruction cache, where code size is time
     const float scale = sc.sigma * sc.C;
-#pragma unroll
+#pragma unroll 1
     for (int i = 0; i < 4; ++i) {
         const int64_t m = m0 + tr * 4 + i;
         if (m >= t.d_out) continue;
+        const int64_t nb = n0 + tc * 4;
+        const uint64_t kb = (uint64_t)(t.coord_off + m * t.d_in + nb);
+        float z[4];
+        if ((kb & 3u) == 0 && nb + 4 <= t.d_in) {
+            // the four coordinates are one Philox block
+            const float4 z4 = noise4(sc.seed, sc.step, kb >> 2);
+            z[0] = z4.x;
+            z[1] = z4.y;
+            z[2] = z4.z;
+            z[3] = z4.w;
+        } else {
+#pragma unroll 1
+            for (int j = 0; j < 4; ++j) z[j] = nb + j < t.d_in ? noise_at(sc.seed, sc.step, kb + j) : 0.f;
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int64_t n = n0 + tc * 4 + j;
+            const int64_t n = nb + j;
             if (n >= t.d_in) continue;
-            const int64_t p = m * t.d_in + n;
-            const float z = noise_at(sc.seed, sc.step, (uint64_t)(t.coord_off + p));
-            t.G[p] = (acc[i][j] + scale * z) / sc.L;
+            t.G[m * t.d_in + n] = (acc[i][j] + scale * z[j]) / sc.L;
         }
     }
     if (do_bias && tid < kBM && m0 + tid < t.d_out) {
