@@ -26,6 +26,7 @@ from ._binding import (  # noqa: F401
     EXPORTS,
     LIB_PATH,
     dp_begin_step,
+    dp_box_muller,
     dp_check_wait_timeout,
     dp_choose_path,
     dp_clip_factors,

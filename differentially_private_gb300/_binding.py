@@ -36,7 +36,7 @@ EXPORTS = (
     "dp_layer_info", "dp_num_coords", "dp_choose_path", "dp_begin_step", "dp_set_normalizer",
     "dp_norm_accumulate", "dp_norm_accumulate_batch", "dp_clip_factors", "dp_clipped_noisy_grad",
     "dp_step_status", "dp_last_error", "dp_philox_normals", "dp_layer_sqnorms_static", "dp_pack_groups",
-    "dp_int8_quantize_weight", "dp_int8_workspace_bytes", "dp_int8_forward", "dp_check_wait_timeout",
+    "dp_int8_quantize_weight", "dp_int8_workspace_bytes", "dp_int8_forward", "dp_check_wait_timeout", "dp_box_muller",
 )
 
 
@@ -87,6 +87,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "dp_last_error": (c.c_char_p, [vp]),
         "dp_philox_normals": (i32, [u64, u64, u64, i64, vp, vp, vp]),
         "dp_check_wait_timeout": (i32, [vp, c.c_uint32]),
+        "dp_box_muller": (i32, [vp, i64, vp, vp]),
         "dp_layer_sqnorms_static": (i32, [vp, vp, i64, i64, i64, i64, i32, i32, vp, vp]),
         "dp_pack_groups": (i32, [vp, vp, i64, i64, i64, i32, vp, i64, i64, vp]),
         "dp_int8_quantize_weight": (i32, [vp, i64, i64, vp, vp, vp, vp]),
@@ -222,6 +223,11 @@ def dp_last_error(ctx) -> str:
 def dp_philox_normals(seed: int, step: int, k0: int, n: int, raw_out=None, z_out=None, stream=None) -> None:
     _check(load_library().dp_philox_normals(int(seed) & (2 ** 64 - 1), int(step) & (2 ** 64 - 1), int(k0), int(n),
                                             _ptr(raw_out), _ptr(z_out), _stream(stream)), "dp_philox_normals")
+
+
+def dp_box_muller(words, npairs: int, z_out, stream=None) -> None:
+    """The noise's Box-Muller map on given word pairs (test hook)."""
+    _check(load_library().dp_box_muller(_ptr(words), int(npairs), _ptr(z_out), _stream(stream)), "dp_box_muller")
 
 
 def dp_check_wait_timeout(ctx, limit_ms: int) -> None:

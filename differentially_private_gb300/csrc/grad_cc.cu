@@ -389,6 +389,16 @@ __global__ void __launch_bounds__(256) k_prescale_rows(const uint4* __restrict__
 }
 
 // ------------------------------------------------------- noise test hook
+// The Box-Muller map of the noise on given word pairs (words[2i], words[2i+1])
+// -> (z[2i], z[2i+1]): the same device function as every noise draw.
+__global__ void k_box_muller(const uint2* __restrict__ words, int64_t npairs, float2* __restrict__ z) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < npairs;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const uint2 w = words[i];
+        z[i] = box_muller(w.x, w.y);
+    }
+}
+
 __global__ void k_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int64_t n,
                                  uint32_t* __restrict__ raw, float* __restrict__ z) {
     const int64_t jb = (int64_t)(k0 >> 2);
@@ -490,6 +500,16 @@ cudaError_t launch_prescale_rows(const void* E, void* E2, const float* c, int64_
                                            (const uint4*)E, (uint4*)E2, c, K, T, d / 8);
     count_launches(1);
     return e;
+}
+
+cudaError_t launch_box_muller(const uint32_t* words, int64_t npairs, float* z, cudaStream_t s) {
+    if (npairs <= 0) return cudaSuccess;
+    int64_t grid = (npairs + 255) / 256;
+    if (grid > 152 * 64) grid = 152 * 64;
+    k_box_muller<<<(unsigned)grid, 256, 0, s>>>(reinterpret_cast<const uint2*>(words), npairs,
+                                                reinterpret_cast<float2*>(z));
+    count_launches(1);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int64_t n,

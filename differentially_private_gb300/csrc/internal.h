@@ -122,6 +122,7 @@ cudaError_t launch_grad_wsum(const GradTask* tasks, int n, const float* c, const
                              const StepScalars& sc, cudaStream_t s);
 cudaError_t launch_grad_gemm_cc(const GradTask& t, const float* c, const unsigned* status,
                                 const StepScalars& sc, cudaStream_t s);
+cudaError_t launch_box_muller(const uint32_t* words, int64_t npairs, float* z, cudaStream_t s);
 cudaError_t launch_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int64_t n,
                                   uint32_t* raw, float* z, cudaStream_t s);
 cudaError_t launch_bias_sum(const GradTask& t, const float* c, const unsigned* status,

@@ -734,6 +734,15 @@ dp_status dp_check_wait_timeout(dp_ctx* ctx, uint32_t limit_ms) {
 
 const char* dp_last_error(const dp_ctx* ctx) { return ctx ? ctx->err.c_str() : ""; }
 
+dp_status dp_box_muller(const uint32_t* words, int64_t npairs, float* z_out, void* stream) {
+    if (npairs < 0) return DP_ERR_SHAPE;
+    if (npairs == 0) return DP_OK;
+    if (!words || !z_out || (reinterpret_cast<uintptr_t>(words) & 7u) || (reinterpret_cast<uintptr_t>(z_out) & 7u))
+        return DP_ERR_INVALID_ARG;
+    const cudaError_t e = launch_box_muller(words, npairs, z_out, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DP_OK : DP_ERR_CUDA;
+}
+
 dp_status dp_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int64_t n, uint32_t* raw_out,
                             float* z_out, void* stream) {
     if (n < 0) return DP_ERR_SHAPE;

@@ -287,6 +287,16 @@ dp_status dp_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int64_t n
                             uint32_t* raw_out, float* z_out, void* stream);
 
 /*
+ * dp_box_muller -- the Box-Muller map of the noise on its own, for testing:
+ * for i < npairs, (z_out[2i], z_out[2i+1]) = (r cos 2 pi u2, r sin 2 pi u2)
+ * with u1, u2 and r from words[2i], words[2i+1] exactly as in
+ * dp_clipped_noisy_grad.  words: device uint32 [2 * npairs], z_out: device
+ * float [2 * npairs], both 8-byte aligned (DP_ERR_INVALID_ARG otherwise).
+ * Launches on `stream`.  npairs >= 0 (DP_ERR_SHAPE otherwise).
+ */
+dp_status dp_box_muller(const uint32_t* words, int64_t npairs, float* z_out, void* stream);
+
+/*
  * dp_check_wait_timeout -- test hook for the failure path of the device-side
  * waits.  Every wait of the tensor-core kernels on their own copies and MMAs
  * is bounded; one that gives up sets the timeout bit of the step's status

@@ -285,3 +285,31 @@ def test_batched_and_single_accumulate_agree():
     for g1, g2 in zip(x.grads, y.grads):
         assert torch.equal(g1, g2)
     assert torch.equal(x.sqnorm, y.sqnorm)
+
+
+@pytest.mark.parametrize("fixed", ["u1", "u2"])
+def test_box_muller_exhaustive_within_1e6(fixed):
+    """Every one of the 2^24 values of one uniform, with the other at the values
+    where the error is largest (u1 smallest: r = sqrt(48 ln 2), the longest
+    radius; u2 at the axes and the diagonals), against the float64 map."""
+    import differentially_private_gb300 as dp
+    grid = (np.arange(1 << 24, dtype=np.uint64) << np.uint64(8)).astype(np.uint32)
+    if fixed == "u1":
+        others = [0, 1 << 8, (1 << 23) << 8, 0xFFFFFFFF]          # u1 = 2^-24, 2 2^-24, 1/2 + 2^-24, 1
+    else:
+        others = [(q * (1 << 21)) << 8 for q in range(8)] + [0xFFFFFF00, 0x00000100]
+    worst = 0.0
+    for o in others:
+        w = np.empty((1 << 24, 2), dtype=np.uint32)
+        if fixed == "u1":
+            w[:, 0], w[:, 1] = np.uint32(o), grid
+        else:
+            w[:, 0], w[:, 1] = grid, np.uint32(o)
+        words = torch.from_numpy(w.view(np.int32)).cuda()
+        z = torch.empty((1 << 24, 2), dtype=torch.float32, device="cuda")
+        dp.dp_box_muller(words, 1 << 24, z)
+        torch.cuda.synchronize()
+        za, zb = philox.box_muller(w[:, 0], w[:, 1])
+        got = z.cpu().numpy().astype(np.float64)
+        worst = max(worst, float(np.abs(got[:, 0] - za).max()), float(np.abs(got[:, 1] - zb).max()))
+    assert worst <= Z_ATOL, worst
