@@ -313,3 +313,32 @@ def test_box_muller_exhaustive_within_1e6(fixed):
         got = z.cpu().numpy().astype(np.float64)
         worst = max(worst, float(np.abs(got[:, 0] - za).max()), float(np.abs(got[:, 1] - zb).max()))
     assert worst <= Z_ATOL, worst
+
+
+@pytest.mark.parametrize("kind", ["prescaled", "records", "stored"])
+def test_nonfinite_on_each_tensor_core_path(kind):
+    """A NaN in one record on each bf16 gradient path (pre-scaled single
+    record written by the clip kernel, per-record fold, stored per-example
+    gradients): the step reports it, no G is written, and the next clean step
+    of the same context matches the oracle."""
+    import differentially_private_gb300 as dp
+    B, T, d_in, d_out = {"prescaled": (33, 3, 256, 192), "records": (6, 64, 320, 256),
+                         "stored": (7, 96, 768, 8)}[kind]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(77)
+    A = torch.randn(B, T, d_in, device="cuda", generator=g).bfloat16()
+    E = (torch.randn(B, T, d_out, device="cuda", generator=g) * 0.05).bfloat16()
+    layers = [(d_in, d_out, True if kind == "prescaled" else False)]
+    pg = dp.PrivateGradient(layers, dtype=torch.bfloat16)
+    grads, clip, sq = pg.alloc_outputs(B)
+    grads[0].fill_(-3.0)
+    bad = E.clone()
+    bad[B // 2, T - 1, d_out - 1] = float("nan")
+    with pytest.raises(dp.DPError) as ei:
+        pg.step([A], [bad], [T], C=0.5, sigma=0.7, seed=1, step=2, outputs=(grads, clip, sq))
+    assert ei.value.status == dp.DP_ERR_NONFINITE
+    assert bool((grads[0] == -3.0).all())
+    out = pg.step([A], [E], [T], C=0.5, sigma=0.7, seed=1, step=2)
+    ref = oracle_step(layers, [A], [E], [T], 0.5, 0.7, 1, 2)
+    assert rel_fro(to64(out.grads[0]), ref.grads[0]) <= G_RTOL
+    pg.close()
