@@ -82,14 +82,6 @@ __global__ void __launch_bounds__(kClipMaxThreads) k_clip(const ClipParams p, fl
                                        : (int64_t)blockIdx.x;
     const int t = kWarpPerRecord ? (int)(threadIdx.x & 31) : (int)threadIdx.x;
     const int G = kWarpPerRecord ? 32 : (int)blockDim.x;
-    // the slot table comes from the host, never from an earlier kernel: the
-    // thread's first entries are fetched while the norm kernels still run
-    SlotRef first[kClipLoads];
-#pragma unroll
-    for (int u = 0; u < kClipLoads; ++u) {
-        const int64_t j = t + (int64_t)u * G;
-        first[u] = j < p.total_slots ? p.slots[j] : SlotRef{nullptr, 0};
-    }
     int64_t units = 0;
     for (int j = 0; j < p.nscale; ++j) units += p.scale[j].units;
     uint4 pre[kScalePre];
@@ -111,7 +103,7 @@ __global__ void __launch_bounds__(kClipMaxThreads) k_clip(const ClipParams p, fl
                 const int64_t j = j0 + (int64_t)u * G;
                 v[u] = 0.f;
                 if (j < p.total_slots) {
-                    const SlotRef r = j0 == t ? first[u] : p.slots[j];
+                    const SlotRef r = p.slots[j];
                     v[u] = __ldcg(r.base + rec * r.stride);
                 }
             }
@@ -429,20 +421,15 @@ __global__ void k_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int6
 }  // namespace
 
 cudaError_t launch_clip(const ClipParams& p, float* n2, float* c, float* n2_user, float* c_user,
-                        unsigned* status, bool table_uploaded, cudaStream_t s) {
+                        unsigned* status, cudaStream_t s) {
     cudaError_t e;
     const int G = clip_group(p.total_slots);
-    // the kernel reads the slot table before its dependency wait: after a
-    // fresh upload it is launched as an ordinary (fully ordered) launch
-    const bool dep = !table_uploaded;
     if (G == 32) {
         const int per_block = kClipWarpBlock / 32;
         const unsigned grid = (unsigned)((p.B + per_block - 1) / per_block);
-        e = launch_maybe_dependent(dep, k_clip<true>, dim3(grid), dim3(kClipWarpBlock), 0, s, p, n2, c, n2_user,
-                                   c_user, status);
+        e = launch_dependent(k_clip<true>, dim3(grid), dim3(kClipWarpBlock), 0, s, p, n2, c, n2_user, c_user, status);
     } else {
-        e = launch_maybe_dependent(dep, k_clip<false>, dim3((unsigned)p.B), dim3(G), 0, s, p, n2, c, n2_user, c_user,
-                                   status);
+        e = launch_dependent(k_clip<false>, dim3((unsigned)p.B), dim3(G), 0, s, p, n2, c, n2_user, c_user, status);
     }
     count_launches(1);
     return e;

@@ -117,7 +117,7 @@ cudaError_t launch_norm_ghost_cc(const NormTask& t, int64_t B, cudaStream_t s);
 cudaError_t launch_norm_mat_cc(const NormTask& t, int64_t B, cudaStream_t s);
 cudaError_t launch_layer_sqnorm(const float* partial, int nslots, int64_t B, float* out, cudaStream_t s);
 cudaError_t launch_clip(const ClipParams& p, float* n2, float* c, float* n2_user, float* c_user,
-                        unsigned* status, bool table_uploaded, cudaStream_t s);
+                        unsigned* status, cudaStream_t s);
 cudaError_t launch_grad_wsum(const GradTask* tasks, int n, const float* c, const unsigned* status,
                              const StepScalars& sc, cudaStream_t s);
 cudaError_t launch_grad_gemm_cc(const GradTask& t, const float* c, const unsigned* status,

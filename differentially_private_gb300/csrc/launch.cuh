@@ -6,10 +6,9 @@
 
 #include <cuda_runtime.h>
 
-// The same launch, with the overlap allowed only when dependent is true.
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_maybe_dependent(bool dependent, void (*kernel)(KArgs...), dim3 grid, dim3 block,
-                                          size_t smem, cudaStream_t s, Args&&... args) {
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                    Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -19,12 +18,6 @@ inline cudaError_t launch_maybe_dependent(bool dependent, void (*kernel)(KArgs..
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = dependent ? 1 : 0;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
-}
-
-template <typename... KArgs, typename... Args>
-inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                                    Args&&... args) {
-    return launch_maybe_dependent(true, kernel, grid, block, smem, s, static_cast<Args&&>(args)...);
 }

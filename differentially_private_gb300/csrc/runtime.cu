@@ -596,8 +596,7 @@ dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnor
         key[l] = {ctx->layers[l].partial, (int64_t)ctx->layers[l].nslots};
         total += ctx->layers[l].nslots;
     }
-    const bool upload = key != ctx->slots_key;
-    if (upload) {
+    if (key != ctx->slots_key) {
         // the flat slot table changes only when the layer set or its scratch does
         if (ctx->d_slots_cap < (size_t)total) {
             cudaError_t e = cudaStreamSynchronize(ctx->stream);
@@ -636,7 +635,7 @@ dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnor
         p.scale[p.nscale++] = PrescaleJob{static_cast<const uint4*>(ly.prescale_A ? ly.A : ly.E),
                                           reinterpret_cast<uint4*>(ly.escaled), ly.T * d / 8};
     }
-    const cudaError_t e = launch_clip(p, ctx->n2, ctx->c, total_sqnorm_out, c_out, ctx->status, upload, ctx->stream);
+    const cudaError_t e = launch_clip(p, ctx->n2, ctx->c, total_sqnorm_out, c_out, ctx->status, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "clip kernel launch");
     ctx->clean[ctx->slot ^ 1] = true;
     ctx->C = C;
