@@ -66,8 +66,8 @@ struct Layer {
             return A == o.A && E == o.E && T == o.T && B == o.B && kind == o.kind;
         }
     } nkey, gkey;
-    alignas(64) CUtensorMap nmaps[2];
-    alignas(64) CUtensorMap gmaps[2];
+    CUtensorMap nmaps[2];   // the type carries the alignment TMA needs
+    CUtensorMap gmaps[2];
 };
 
 }  // namespace

@@ -5,13 +5,12 @@ tiles and ragged tails; the five workloads appear at reduced size with their
 value distributions (full sizes are in test_gpu_fullsize.py).
 """
 
-import math
 
 import numpy as np
 import pytest
 import torch
 
-from gpu_harness import (G_RTOL, NORM_RTOL, Z_ATOL, assert_step_parity, gpu_step, oracle_step, rel_fro, to64)
+from gpu_harness import (G_RTOL, Z_ATOL, assert_step_parity, gpu_step, oracle_step, rel_fro, to64)
 from oracle import dpsgd, philox
 from synthetic import by_index, generate_layer
 

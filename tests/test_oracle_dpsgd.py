@@ -7,7 +7,6 @@ sensitivity bound the pages state.
 
 import itertools
 import json
-import math
 import os
 
 import numpy as np

@@ -8,7 +8,6 @@ import json
 import os
 
 import numpy as np
-import pytest
 
 from oracle import int8
 
