@@ -99,6 +99,17 @@ struct ClipParams {
 // after limit_ns and sets the timeout bit of *status (waitcheck.cu)
 cudaError_t launch_wait_expiry(unsigned* status, uint64_t limit_ns, cudaStream_t s);
 
+// ---- host helpers shared by the tensor-core launchers (runtime.cu)
+// cuTensorMapEncodeTiled, fetched once through the runtime (the library does
+// not link libcuda directly); nullptr when the driver does not provide it.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
+// The kernel's dynamic shared-memory limit raised to `bytes` on the current
+// device (once per device and kernel; safe from several host threads).
+cudaError_t ensure_smem_limit(const void* kernel, int bytes);
+
 // ---- every kernel launch of the library is counted here (dp_kernel_launches)
 void count_launches(int n);
 

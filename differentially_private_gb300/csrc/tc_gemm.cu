@@ -445,28 +445,9 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
 }
 
 // ============================================================ host side
-// driver entry point cuTensorMapEncodeTiled, fetched through the runtime so
-// that the library does not link libcuda directly
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
 bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
             const uint32_t* box, CUtensorMapSwizzle swz) {
-    auto fn = get_encode();
+    const EncodeTiledFn fn = tensor_map_encoder();
     if (!fn) return false;
     cuuint64_t gd[3], gs[2];
     cuuint32_t bd[3], es[3] = {1, 1, 1};
@@ -481,15 +462,12 @@ bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, co
     return r == CUDA_SUCCESS;
 }
 
+// SMs of the current device
 int sm_count_cached() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 1;
-    }
-    return n;
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
 }
 
 }  // namespace
@@ -527,11 +505,11 @@ int device_sm_count() { return sm_count_cached(); }
 
 cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* status, const StepScalars& sc,
                                   const FoldWork* work, cudaStream_t s) {
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_clipped_sum_fold_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSumSmem);
-        cudaFuncSetAttribute(k_clipped_sum_fold_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSumSmem);
-        attr = true;
+    {
+        const void* k = sc.B > 1 ? reinterpret_cast<const void*>(k_clipped_sum_fold_tc<true>)
+                                 : reinterpret_cast<const void*>(k_clipped_sum_fold_tc<false>);
+        const cudaError_t a = ensure_smem_limit(k, (int)kSumSmem);
+        if (a != cudaSuccess) return a;
     }
     SumParams p;
     if (t.maps) {

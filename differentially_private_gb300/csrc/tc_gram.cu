@@ -221,19 +221,8 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
 
 bool encode_bf16(CUtensorMap* m, const void* base, const uint64_t* dims, const uint64_t* strides,
                  const uint32_t* box) {
-    typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                      const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                      CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return false;
-        fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
+    const EncodeTiledFn fn = tensor_map_encoder();
+    if (!fn) return false;
     cuuint64_t gd[3] = {dims[0], dims[1], dims[2]};
     cuuint64_t gs[2] = {strides[0], strides[1]};
     cuuint32_t bd[3] = {box[0], box[1], box[2]};
@@ -268,10 +257,9 @@ bool tc_gram_supported(int dtype, int64_t T, int64_t d_in, int64_t d_out) {
 int nslots_gram(int64_t T) { return gram_tiles_per_rec(T) * 4; }
 
 cudaError_t launch_ghost_gram_tc(const NormTask& t, int64_t B, unsigned* status, cudaStream_t s) {
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_ghost_gram_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGramSmem);
-        attr = true;
+    {
+        const cudaError_t a = ensure_smem_limit(reinterpret_cast<const void*>(k_ghost_gram_tc), (int)kGramSmem);
+        if (a != cudaSuccess) return a;
     }
     GramParams p;
     if (t.maps) {

@@ -357,22 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
     }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
 bool encode3d(CUtensorMap* m, const void* base, const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
               CUtensorMapSwizzle swz) {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return false;
-        fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
+    const EncodeTiledFn fn = tensor_map_encoder();
+    if (!fn) return false;
     cuuint64_t gd[3] = {dims[0], dims[1], dims[2]};
     cuuint64_t gs[2] = {strides[0], strides[1]};
     cuuint32_t bd[3] = {box[0], box[1], box[2]};
@@ -427,10 +415,9 @@ bool tc_encode_skinny(const NormTask& t, int64_t B, CUtensorMap* maps2) {
 }
 
 cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsigned* status, cudaStream_t s) {
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_mat_skinny_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
-        attr = true;
+    {
+        const cudaError_t a = ensure_smem_limit(reinterpret_cast<const void*>(k_mat_skinny_tc), (int)kSmem);
+        if (a != cudaSuccess) return a;
     }
     thread_local SkinnyParams p;   // host staging of the parameter block; each launch copies it
     const int sms = sm_count();
