@@ -119,3 +119,49 @@ def test_many_ragged_skinny_blocks_match_oracle_repeat_and_are_batch_invariant()
     for l in range(len(layers)):
         assert torch.equal(one.layer_sqnorm[l][0], out.layer_sqnorm[l][7])
     pg.close()
+
+
+def test_two_contexts_from_two_host_threads():
+    # one context per host thread, each on its own stream, stepping at the
+    # same time: every result is bitwise the one of a lone run
+    import threading
+    g = torch.Generator(device="cuda")
+    g.manual_seed(21)
+    cases = []
+    for (d_in, d_out, T) in ((768, 8, 128), (512, 512, 64), (1024, 256, 3)):
+        A = torch.randn(6, T, d_in, device="cuda", generator=g).bfloat16()
+        E = (torch.randn(6, T, d_out, device="cuda", generator=g) * 0.05).bfloat16()
+        cases.append(([(d_in, d_out, False)], [A], [E], [T]))
+    lone = []
+    for layers, A, E, T in cases:
+        pg = dp.PrivateGradient(layers, dtype=torch.bfloat16)
+        out = pg.step(A, E, T, C=0.6, sigma=0.8, seed=9, step=4)
+        torch.cuda.synchronize()
+        lone.append(out.grads[0].clone())
+        pg.close()
+    results = [[None] * len(cases) for _ in range(2)]
+    errors = []
+
+    def worker(k):
+        try:
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                for i, (layers, A, E, T) in enumerate(cases):
+                    pg = dp.PrivateGradient(layers, dtype=torch.bfloat16, stream=stream)
+                    for _ in range(3):
+                        out = pg.step(A, E, T, C=0.6, sigma=0.8, seed=9, step=4)
+                    stream.synchronize()
+                    results[k][i] = out.grads[0].clone()
+                    pg.close()
+        except Exception as exc:   # surfaced in the main thread
+            errors.append(exc)
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for k in range(2):
+        for i in range(len(cases)):
+            assert torch.equal(results[k][i], lone[i]), (k, i)
