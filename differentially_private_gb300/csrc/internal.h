@@ -158,6 +158,12 @@ int nslots_skinny(int64_t d_in, int64_t d_out);
 // work == nullptr: every tile is done whole by one CTA
 cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* status,
                                   const StepScalars& sc, const FoldWork* work, cudaStream_t s);
+// Single-record sums of up to kMaxSumLayersLaunch layers sharing K = T rows
+// (tasks[i].T = K; factor 1: their clip factors are in the pre-scaled
+// operand) in one persistent launch, whole tiles strided over the CTAs.
+constexpr int kMaxSumLayersLaunch = 4;
+cudaError_t launch_sum_layers_tc(const GradTask* tasks, int n, unsigned* status, const StepScalars& sc,
+                                 cudaStream_t s);
 cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsigned* status, cudaStream_t s);
 // TMA descriptors of a layer, encoded once per (pointers, T, B) and cached by the runtime
 bool tc_encode_skinny(const NormTask& t, int64_t B, CUtensorMap* maps2);

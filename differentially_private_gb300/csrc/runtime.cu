@@ -686,7 +686,9 @@ dp_status dp_clipped_noisy_grad(dp_ctx* ctx, float sigma, uint64_t seed, uint64_
     sc.L = (float)ctx->L;
     sc.seed = seed;
     sc.step = step;
-    std::vector<GradTask> wsum;
+    // layers whose pre-scaled operand the clip kernel wrote are summed together
+    // (layers with the same K in one launch); their bias sums follow them
+    std::vector<GradTask> wsum, single, single_bias;
     for (size_t l = 0; l < ctx->layers.size(); ++l) {
         const Layer& ly = ctx->layers[l];
         GradTask t;
@@ -706,12 +708,20 @@ dp_status dp_clipped_noisy_grad(dp_ctx* ctx, float sigma, uint64_t seed, uint64_
             continue;
         }
         cudaError_t e;
+        if (ly.grad_kernel == GK_GEMM_TC && ly.prescale && ly.scaled_by_clip) {
+            GradTask ts = t;
+            if (ly.prescale_A) ts.A = ly.escaled;
+            else ts.E = ly.escaled;
+            ts.T = ctx->B * ly.T;
+            single.push_back(ts);
+            if (ly.has_bias) single_bias.push_back(t);
+            continue;
+        }
         if (ly.grad_kernel == GK_GEMM_TC && ly.prescale) {
             // c_i folded into a bf16 copy of the narrower operand, then one "record" of B*T rows with factor 1
             const int64_t K = ctx->B * ly.T;
-            e = ly.scaled_by_clip ? cudaSuccess
-                : ly.prescale_A   ? launch_prescale_rows(ly.A, ly.escaled, ctx->c, K, ly.T, ly.d_in, ctx->stream)
-                                  : launch_prescale_rows(ly.E, ly.escaled, ctx->c, K, ly.T, ly.d_out, ctx->stream);
+            e = ly.prescale_A ? launch_prescale_rows(ly.A, ly.escaled, ctx->c, K, ly.T, ly.d_in, ctx->stream)
+                              : launch_prescale_rows(ly.E, ly.escaled, ctx->c, K, ly.T, ly.d_out, ctx->stream);
             GradTask ts = t;
             if (ly.prescale_A) ts.A = ly.escaled;
             else ts.E = ly.escaled;
@@ -728,6 +738,27 @@ dp_status dp_clipped_noisy_grad(dp_ctx* ctx, float sigma, uint64_t seed, uint64_
             e = launch_grad_gemm_cc(t, ctx->c, ctx->status, sc, ctx->stream);
         }
         if (e != cudaSuccess) return cuda_fail(ctx, e, "clipped-sum kernel launch");
+    }
+    {
+        StepScalars s1 = sc;
+        s1.B = 1;
+        std::vector<bool> done(single.size(), false);
+        for (size_t i = 0; i < single.size(); ++i) {
+            if (done[i]) continue;
+            GradTask group[kMaxSumLayersLaunch];
+            int n = 0;
+            for (size_t j = i; j < single.size() && n < kMaxSumLayersLaunch; ++j)
+                if (!done[j] && single[j].T == single[i].T) {
+                    group[n++] = single[j];
+                    done[j] = true;
+                }
+            const cudaError_t e = launch_sum_layers_tc(group, n, ctx->status, s1, ctx->stream);
+            if (e != cudaSuccess) return cuda_fail(ctx, e, "clipped-sum kernel launch");
+        }
+        for (const GradTask& t : single_bias) {
+            const cudaError_t e = launch_bias_sum(t, ctx->c, ctx->status, sc, ctx->stream);
+            if (e != cudaSuccess) return cuda_fail(ctx, e, "bias-sum kernel launch");
+        }
     }
     if (!wsum.empty()) {
         const cudaError_t e = launch_grad_wsum(wsum.data(), (int)wsum.size(), ctx->c, ctx->status, sc, ctx->stream);

@@ -444,6 +444,207 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
     }
 }
 
+// ================================= single-record sums of several layers
+// Layers whose clip factors the clip kernel folded into a pre-scaled operand
+// are sums over K = B*T rows with factor 1 (as k_clipped_sum_fold_tc<false>).
+// Layers sharing K are summed in one persistent launch: their output tiles
+// form one index space, strided over the CTAs, so a layer's tiles fill the
+// SMs another layer's partial wave leaves idle, and the launch boundary
+// between the layers is gone.  Per tile the work is that of
+// k_clipped_sum_fold_tc<false>: the whole K in TMEM (two buffers, so a
+// tile's epilogue overlaps the next tile's MMAs), the noise drawn while the
+// tensor cores accumulate, G = (S + sigma C z) / L.
+constexpr int kMaxSumLayers = 4;
+
+struct SumLayer {
+    CUtensorMap tmE;   // the layer's operands over the K rows (as SumParams)
+    CUtensorMap tmA;
+    int64_t d_in, d_out;
+    int m_blocks, n_blocks;
+    int box3d;
+    float* G;
+    int64_t coord_off;
+};
+
+struct LayersParams {
+    int nlayers;
+    int nk;                          // K tiles of every tile
+    int tile_begin[kMaxSumLayers + 1];
+    unsigned* status;
+    float scale, inv_L;              // sigma * C, 1 / L
+    uint64_t seed, step;
+    SumLayer L[kMaxSumLayers];
+};
+
+// layer and tile within it of tile g of the launch
+__device__ __forceinline__ int layer_of(const LayersParams& p, int g) {
+    int l = 0;
+    while (l + 1 < p.nlayers && p.tile_begin[l + 1] <= g) ++l;
+    return l;
+}
+
+__global__ void __launch_bounds__(kFoldThreads, 1) k_sum_layers_tc(const __grid_constant__ LayersParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    FoldSmem* sh = reinterpret_cast<FoldSmem*>(tiles + (size_t)kStages * kStageBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntiles = p.tile_begin[p.nlayers];
+    volatile int* abort_flag = &sh->abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            tc::mbar_init(&sh->full[s], 1);
+            tc::mbar_init(&sh->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&sh->p_full[b], 1);
+            tc::mbar_init(&sh->p_empty[b], 32 * kEpiWarps);
+        }
+        tc::mbar_init(&sh->drain, 1);
+        sh->abort_flag = 0;
+        tc::fence_barrier_init();
+        for (int l = 0; l < p.nlayers; ++l) {
+            tc::tma_prefetch_desc(&p.L[l].tmE);
+            tc::tma_prefetch_desc(&p.L[l].tmA);
+        }
+    }
+    if (warp == 1) tc::tmem_alloc(&sh->tmem_base, kTmemCols);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+    // the pre-scaled operands (written by the clip kernel) and the status
+    // word are read only after the previous kernel completed
+    grid_dep_wait();
+    grid_dep_trigger();
+    const bool skip = status_bad(p.status);
+
+    if (!skip && warp == 0) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int g = blockIdx.x; g < ntiles; g += gridDim.x) {
+                const int l = layer_of(p, g);
+                const SumLayer& ly = p.L[l];
+                int mb, nb;
+                tile_coords(g - p.tile_begin[l], ly.m_blocks, ly.n_blocks, mb, nb);
+                for (int kt = 0; kt < p.nk; ++kt, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort_flag, p.status)) goto layers_producer_done;
+                    uint8_t* st = tiles + (size_t)s * kStageBytes;
+                    tc::mbar_arrive_expect_tx(&sh->full[s], kStageBytes);
+                    const int k0 = kt * kBK;
+                    if (ly.box3d) {
+                        tc::tma_load_3d(st, &ly.tmE, &sh->full[s], 0, k0, mb * (kBM / 64));
+                        tc::tma_load_3d(st + kAStage, &ly.tmA, &sh->full[s], 0, k0, nb * (kBN / 64));
+                    } else {
+                        tc::tma_load_2d(st, &ly.tmE, &sh->full[s], mb * kBM, k0);
+                        tc::tma_load_2d(st + 8192, &ly.tmE, &sh->full[s], mb * kBM + 64, k0);
+#pragma unroll
+                        for (int q = 0; q < kBN / 64; ++q)
+                            tc::tma_load_2d(st + kAStage + q * 8192, &ly.tmA, &sh->full[s], nb * kBN + 64 * q, k0);
+                    }
+                }
+            }
+        layers_producer_done:
+            for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j)
+                tc::mbar_wait_drain(&sh->full[j % kStages], (j / kStages) & 1u);
+        }
+    } else if (!skip && warp == 1) {
+        if (lane == 0) {
+            uint32_t it = 0, rc = 0;
+            bool ok = true;
+            for (int g = blockIdx.x; g < ntiles && ok; g += gridDim.x, ++rc) {
+                const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
+                if (!tc::mbar_wait(&sh->p_empty[b], bph ^ 1u, abort_flag, p.status)) break;
+                tc::tc_fence_after();
+                const uint32_t d_tmem = tmem + b * kAccCols;
+                for (int kt = 0; kt < p.nk; ++kt, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    const uint32_t sa = tc::smem_u32(tiles + (size_t)s * kStageBytes);
+                    const uint32_t sb = sa + kAStage;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t ad = tc::smem_desc(sa + kk * 2048, 8192, 1024, tc::SW_128B);
+                        const uint64_t bd = tc::smem_desc(sb + kk * 2048, 8192, 1024, tc::SW_128B);
+                        tc::mma_bf16(d_tmem, ad, bd, kIdescSum, (kt | kk) != 0);
+                    }
+                    tc::mma_commit(&sh->empty[s]);
+                }
+                if (!ok) break;
+                tc::mma_commit(&sh->p_full[b]);
+            }
+        }
+    } else if (!skip && warp >= 2) {
+        const int quarter = warp & 3;
+        const int part = (warp - 2) >> 2;          // columns part*64 .. +63
+        const int row = quarter * 32 + lane;
+        uint32_t rc = 0;
+        for (int g = blockIdx.x; g < ntiles; g += gridDim.x, ++rc) {
+            const int l = layer_of(p, g);
+            const SumLayer& ly = p.L[l];
+            int mb, nb;
+            tile_coords(g - p.tile_begin[l], ly.m_blocks, ly.n_blocks, mb, nb);
+            const int64_t m = (int64_t)mb * kBM + row;
+            const int64_t n0 = (int64_t)nb * kBN + part * kColsPerWarp;
+            // the noise does not depend on the sum: drawn while the tensor cores accumulate
+            float z[kColsPerWarp];
+            if (m < ly.d_out) {
+#pragma unroll
+                for (int ch = 0; ch < kColsPerWarp / 8; ++ch) {
+                    float zc[8];
+                    noise8(p.seed, p.step, (uint64_t)(ly.coord_off + m * ly.d_in + n0 + ch * 8), zc);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) z[ch * 8 + j] = zc[j];
+                }
+            }
+            const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
+            if (!tc::mbar_wait(&sh->p_full[b], bph, abort_flag, p.status)) break;
+            tc::tc_fence_after();
+            const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + part * kColsPerWarp;
+            float* out = ly.G + m * ly.d_in + n0;
+#pragma unroll
+            for (int ch = 0; ch < kColsPerWarp / 16; ++ch) {
+                float v[16];
+                tc::tmem_ld16(tb + ch * 16, v);
+                if (m >= ly.d_out) continue;
+                const int64_t n = n0 + ch * 16;
+                if (n + 16 <= ly.d_in) {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) {
+                        float4 o;
+                        o.x = (v[j] + p.scale * z[ch * 16 + j]) * p.inv_L;
+                        o.y = (v[j + 1] + p.scale * z[ch * 16 + j + 1]) * p.inv_L;
+                        o.z = (v[j + 2] + p.scale * z[ch * 16 + j + 2]) * p.inv_L;
+                        o.w = (v[j + 3] + p.scale * z[ch * 16 + j + 3]) * p.inv_L;
+                        *reinterpret_cast<float4*>(out + ch * 16 + j) = o;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (n + j < ly.d_in) out[ch * 16 + j] = (v[j] + p.scale * z[ch * 16 + j]) * p.inv_L;
+                }
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&sh->p_empty[b]);
+        }
+    }
+
+    if (!skip && warp == 1 && lane == 0) {
+        tc::mma_commit(&sh->drain);
+        tc::mbar_wait_drain(&sh->drain, 0);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
 // ============================================================ host side
 bool encode(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
             const uint32_t* box, CUtensorMapSwizzle swz) {
@@ -566,6 +767,54 @@ cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* s
     const cudaError_t e =
         sc.B > 1 ? launch_dependent(k_clipped_sum_fold_tc<true>, dim3(grid), dim3(kFoldThreads), kSumSmem, s, p)
                  : launch_dependent(k_clipped_sum_fold_tc<false>, dim3(grid), dim3(kFoldThreads), kSumSmem, s, p);
+    count_launches(1);
+    return e;
+}
+
+cudaError_t launch_sum_layers_tc(const GradTask* tasks, int n, unsigned* status, const StepScalars& sc,
+                                 cudaStream_t s) {
+    if (n < 1 || n > kMaxSumLayers) return cudaErrorInvalidValue;
+    {
+        const cudaError_t a = ensure_smem_limit(reinterpret_cast<const void*>(k_sum_layers_tc), (int)kSumSmem);
+        if (a != cudaSuccess) return a;
+    }
+    LayersParams p;
+    p.nlayers = n;
+    const int64_t K = tasks[0].T;   // one record of K rows with factor 1
+    p.nk = (int)((K + kBK - 1) / kBK);
+    int tiles = 0;
+    for (int l = 0; l < n; ++l) {
+        const GradTask& t = tasks[l];
+        if (t.T != K) return cudaErrorInvalidValue;
+        SumLayer& L = p.L[l];
+        if (t.maps) {
+            L.tmE = t.maps[0];
+            L.tmA = t.maps[1];
+        } else {
+            CUtensorMap m[2];
+            if (!tc_encode_sum(t, 1, m)) return cudaErrorInvalidValue;
+            L.tmE = m[0];
+            L.tmA = m[1];
+        }
+        L.d_in = t.d_in;
+        L.d_out = t.d_out;
+        L.m_blocks = (int)((t.d_out + kBM - 1) / kBM);
+        L.n_blocks = (int)((t.d_in + kBN - 1) / kBN);
+        L.box3d = (t.d_in % 64 == 0 && t.d_out % 64 == 0) ? 1 : 0;
+        L.G = t.G;
+        L.coord_off = t.coord_off;
+        p.tile_begin[l] = tiles;
+        tiles += L.m_blocks * L.n_blocks;
+    }
+    p.tile_begin[n] = tiles;
+    p.status = status;
+    p.scale = sc.sigma * sc.C;
+    p.inv_L = 1.0f / sc.L;
+    p.seed = sc.seed;
+    p.step = sc.step;
+    const int sms = sm_count_cached();
+    const int grid = tiles < sms ? tiles : sms;
+    const cudaError_t e = launch_dependent(k_sum_layers_tc, dim3(grid), dim3(kFoldThreads), kSumSmem, s, p);
     count_launches(1);
     return e;
 }
