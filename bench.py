@@ -402,9 +402,9 @@ def run_ours(args, w):
                        else "k_norm_t1_group" if ghost_T and all(t == 1 for t in ghost_T) else "k_mat_skinny_tc")
     else:
         # layers whose T is not a multiple of 64 are summed as one pre-scaled record,
-        # the layers sharing K in one launch of k_sum_layers_tc
+        # the layers sharing K in one launch of k_sum_layers_pair_tc
         kernel_name = ("k_grad_wsum" if roof["bound"] == "hbm"
-                       else "k_sum_layers_tc" if ghost_T and all(t % 64 for t in ghost_T)
+                       else "k_sum_layers_pair_tc" if ghost_T and all(t % 64 for t in ghost_T)
                        else "k_clipped_sum_fold_tc")
     roof["traffic"] = kernel_traffic(f"{kernel_name}@{w.name}")
     roof["kernel"] = kernel_name

@@ -55,7 +55,7 @@ struct GradTask {
     const float* gstore;   // stored per-example gradients (GK_WSUM)
     float* G;              // output, d_out*d_in (+ d_out)
     int64_t coord_off;     // first noise coordinate of the layer
-    const CUtensorMap* maps;  // two pre-encoded TMA descriptors (tensor-core kernels), or nullptr
+    const CUtensorMap* maps;  // pre-encoded TMA descriptors (tc_encode_sum: three), or nullptr
 };
 
 struct StepScalars {
@@ -167,7 +167,8 @@ cudaError_t launch_sum_layers_tc(const GradTask* tasks, int n, unsigned* status,
 cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsigned* status, cudaStream_t s);
 // TMA descriptors of a layer, encoded once per (pointers, T, B) and cached by the runtime
 bool tc_encode_skinny(const NormTask& t, int64_t B, CUtensorMap* maps2);
-bool tc_encode_sum(const GradTask& t, int64_t B, CUtensorMap* maps2);
+// maps3: E, A in 256-column tiles, A in 128-column halves (CTA pairs)
+bool tc_encode_sum(const GradTask& t, int64_t B, CUtensorMap* maps3);
 bool tc_encode_gram(const NormTask& t, int64_t B, CUtensorMap* maps2);
 
 // ---- tcgen05 ghost Gram (tc_gram.cu)

@@ -69,7 +69,7 @@ struct Layer {
         }
     } nkey, gkey;
     CUtensorMap nmaps[2];   // the type carries the alignment TMA needs
-    CUtensorMap gmaps[2];
+    CUtensorMap gmaps[3];
 };
 
 }  // namespace

@@ -19,6 +19,7 @@
 //   warps 2-17  fold S += c_i P_i, then the noise epilogue
 #include <cuda_bf16.h>
 
+#include <atomic>
 #include <climits>
 
 #include "common.cuh"
@@ -447,13 +448,10 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
 // ================================= single-record sums of several layers
 // Layers whose clip factors the clip kernel folded into a pre-scaled operand
 // are sums over K = B*T rows with factor 1 (as k_clipped_sum_fold_tc<false>).
-// Layers sharing K are summed in one persistent launch: their output tiles
-// form one index space, strided over the CTAs, so a layer's tiles fill the
-// SMs another layer's partial wave leaves idle, and the launch boundary
-// between the layers is gone.  Per tile the work is that of
-// k_clipped_sum_fold_tc<false>: the whole K in TMEM (two buffers, so a
-// tile's epilogue overlaps the next tile's MMAs), the noise drawn while the
-// tensor cores accumulate, G = (S + sigma C z) / L.
+// Layers sharing K are summed in one persistent launch, k_sum_layers_pair_tc:
+// their output tiles form one index space, strided over the CTA pairs, so a
+// layer's tiles fill the SMs another layer's partial wave leaves idle, and
+// the launch boundary between the layers is gone.
 constexpr int kMaxSumLayers = 4;
 
 struct SumLayer {
@@ -483,22 +481,64 @@ __device__ __forceinline__ int layer_of(const LayersParams& p, int g) {
     return l;
 }
 
-__global__ void __launch_bounds__(kFoldThreads, 1) k_sum_layers_tc(const __grid_constant__ LayersParams p) {
+// ==================================== single-record sums on CTA pairs
+// A 256 x 256 output tile per cluster of two CTAs and one
+// tcgen05.mma.cta_group::2 per K step: CTA r stages columns [128 r, 128 r +
+// 128) of the tile's E and A blocks (its half of M and of N), rank 0 issues
+// the MMAs, and each CTA's TMEM receives its 128 rows of the tile (two
+// buffers, so a tile's epilogue overlaps the next tile's MMAs).  Per SM the
+// tensor cores do the same work per K step as a 128 x 256 tile of one CTA
+// but stage two thirds of its bytes, which leaves room for six stages and a
+// 2 KB staging block per epilogue warp.  The epilogue draws the tile's noise
+// while the tensor cores accumulate, then writes G = (S + sigma C z) / L
+// through its staging block: a store instruction covers 8 rows x 64
+// contiguous bytes instead of 32 rows x 16 bytes, four times fewer (and
+// whole-sector) L2 writes.
+//
+// Barriers: rank 0's full[s] counts both CTAs' copies (its producer expects
+// the bytes of both halves); the MMA commits arrive on empty[s], p_full[b]
+// and drain of both CTAs; the epilogue warps of both CTAs arrive on rank 0's
+// p_empty[b].
+constexpr int kPairStages = 6;
+constexpr int kHalf = 128;                    // M rows and N columns staged per CTA
+constexpr int kPairTile = 2 * kHalf;          // output tile of the pair: 256 x 256
+constexpr int kPairEStage = kHalf * kBK * 2;  // 2 boxes of 64 columns x 64 rows
+constexpr int kPairStageBytes = 2 * kPairEStage;
+constexpr uint32_t kIdescPair = tc::idesc_bf16_f32(kPairTile, kPairTile, 1, 1);
+constexpr int kStagingBytes = kEpiWarps * 32 * 16 * 4;  // 32 rows x 16 fp32 per epilogue warp
+constexpr size_t kPairSmem = 1024 + (size_t)kPairStages * kPairStageBytes + kStagingBytes + 256;
+
+struct PairSmem {
+    uint64_t full[kPairStages];
+    uint64_t empty[kPairStages];
+    uint64_t p_full[2];
+    uint64_t p_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+static_assert(sizeof(PairSmem) <= 256, "pair barriers exceed their shared-memory slot");
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
+    k_sum_layers_pair_tc(const __grid_constant__ LayersParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    FoldSmem* sh = reinterpret_cast<FoldSmem*>(tiles + (size_t)kStages * kStageBytes);
+    uint8_t* staging = tiles + (size_t)kPairStages * kPairStageBytes;
+    PairSmem* sh = reinterpret_cast<PairSmem*>(staging + kStagingBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = tc::cluster_ctarank();
+    const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
     const int ntiles = p.tile_begin[p.nlayers];
     volatile int* abort_flag = &sh->abort_flag;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kPairStages; ++s) {
             tc::mbar_init(&sh->full[s], 1);
             tc::mbar_init(&sh->empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&sh->p_full[b], 1);
-            tc::mbar_init(&sh->p_empty[b], 32 * kEpiWarps);
+            tc::mbar_init(&sh->p_empty[b], 2 * kEpiWarps);
         }
         tc::mbar_init(&sh->drain, 1);
         sh->abort_flag = 0;
@@ -508,89 +548,95 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_sum_layers_tc(const __grid_
             tc::tma_prefetch_desc(&p.L[l].tmA);
         }
     }
-    if (warp == 1) tc::tmem_alloc(&sh->tmem_base, kTmemCols);
+    if (warp == 1) tc::tmem_alloc_pair(&sh->tmem_base, 2 * kAccCols);
     tc::tc_fence_before();
     __syncthreads();
+    // both CTAs' barriers are initialised before either signals the other
+    tc::cluster_sync();
     tc::tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
-    // the pre-scaled operands (written by the clip kernel) and the status
-    // word are read only after the previous kernel completed
     grid_dep_wait();
     grid_dep_trigger();
     const bool skip = status_bad(p.status);
 
     if (!skip && warp == 0) {
         if (lane == 0) {
+            const uint32_t full0 = tc::mapa_shared(tc::smem_u32(&sh->full[0]), 0);
             uint32_t it = 0;
-            for (int g = blockIdx.x; g < ntiles; g += gridDim.x) {
+            for (int g = pair; g < ntiles; g += npairs) {
                 const int l = layer_of(p, g);
                 const SumLayer& ly = p.L[l];
                 int mb, nb;
                 tile_coords(g - p.tile_begin[l], ly.m_blocks, ly.n_blocks, mb, nb);
                 for (int kt = 0; kt < p.nk; ++kt, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1u;
-                    if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort_flag, p.status)) goto layers_producer_done;
-                    uint8_t* st = tiles + (size_t)s * kStageBytes;
-                    tc::mbar_arrive_expect_tx(&sh->full[s], kStageBytes);
+                    const int s = it % kPairStages;
+                    const uint32_t ph = (it / kPairStages) & 1u;
+                    if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort_flag, p.status)) goto pair_producer_done;
+                    uint8_t* st = tiles + (size_t)s * kPairStageBytes;
+                    if (rank == 0) tc::mbar_arrive_expect_tx(&sh->full[s], 2 * kPairStageBytes);
+                    const uint32_t fb = full0 + (uint32_t)(s * sizeof(uint64_t));
                     const int k0 = kt * kBK;
                     if (ly.box3d) {
-                        tc::tma_load_3d(st, &ly.tmE, &sh->full[s], 0, k0, mb * (kBM / 64));
-                        tc::tma_load_3d(st + kAStage, &ly.tmA, &sh->full[s], 0, k0, nb * (kBN / 64));
+                        tc::tma_load_3d_pair(st, &ly.tmE, fb, 0, k0, mb * (kPairTile / 64) + (int)rank * (kHalf / 64));
+                        tc::tma_load_3d_pair(st + kPairEStage, &ly.tmA, fb, 0, k0,
+                                             nb * (kPairTile / 64) + (int)rank * (kHalf / 64));
                     } else {
-                        tc::tma_load_2d(st, &ly.tmE, &sh->full[s], mb * kBM, k0);
-                        tc::tma_load_2d(st + 8192, &ly.tmE, &sh->full[s], mb * kBM + 64, k0);
-#pragma unroll
-                        for (int q = 0; q < kBN / 64; ++q)
-                            tc::tma_load_2d(st + kAStage + q * 8192, &ly.tmA, &sh->full[s], nb * kBN + 64 * q, k0);
+                        const int xe = mb * kPairTile + (int)rank * kHalf, xa = nb * kPairTile + (int)rank * kHalf;
+                        tc::tma_load_2d_pair(st, &ly.tmE, fb, xe, k0);
+                        tc::tma_load_2d_pair(st + 8192, &ly.tmE, fb, xe + 64, k0);
+                        tc::tma_load_2d_pair(st + kPairEStage, &ly.tmA, fb, xa, k0);
+                        tc::tma_load_2d_pair(st + kPairEStage + 8192, &ly.tmA, fb, xa + 64, k0);
                     }
                 }
             }
-        layers_producer_done:
-            for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j)
-                tc::mbar_wait_drain(&sh->full[j % kStages], (j / kStages) & 1u);
+        pair_producer_done:
+            // rank 0 waits for the copies of both CTAs still in flight; rank 1's
+            // copies complete on rank 0's barriers before the final cluster barrier
+            if (rank == 0)
+                for (uint32_t j = it > kPairStages ? it - kPairStages : 0; j < it; ++j)
+                    tc::mbar_wait_drain(&sh->full[j % kPairStages], (j / kPairStages) & 1u);
         }
     } else if (!skip && warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             uint32_t it = 0, rc = 0;
             bool ok = true;
-            for (int g = blockIdx.x; g < ntiles && ok; g += gridDim.x, ++rc) {
+            for (int g = pair; g < ntiles && ok; g += npairs, ++rc) {
                 const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
                 if (!tc::mbar_wait(&sh->p_empty[b], bph ^ 1u, abort_flag, p.status)) break;
                 tc::tc_fence_after();
                 const uint32_t d_tmem = tmem + b * kAccCols;
                 for (int kt = 0; kt < p.nk; ++kt, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1u;
+                    const int s = it % kPairStages;
+                    const uint32_t ph = (it / kPairStages) & 1u;
                     if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) { ok = false; break; }
                     tc::tc_fence_after();
-                    const uint32_t sa = tc::smem_u32(tiles + (size_t)s * kStageBytes);
-                    const uint32_t sb = sa + kAStage;
+                    const uint32_t sa = tc::smem_u32(tiles + (size_t)s * kPairStageBytes);
+                    const uint32_t sb = sa + kPairEStage;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint64_t ad = tc::smem_desc(sa + kk * 2048, 8192, 1024, tc::SW_128B);
                         const uint64_t bd = tc::smem_desc(sb + kk * 2048, 8192, 1024, tc::SW_128B);
-                        tc::mma_bf16(d_tmem, ad, bd, kIdescSum, (kt | kk) != 0);
+                        tc::mma_bf16_pair(d_tmem, ad, bd, kIdescPair, (kt | kk) != 0);
                     }
-                    tc::mma_commit(&sh->empty[s]);
+                    tc::mma_commit_pair(&sh->empty[s], 0x3);
                 }
                 if (!ok) break;
-                tc::mma_commit(&sh->p_full[b]);
+                tc::mma_commit_pair(&sh->p_full[b], 0x3);
             }
         }
     } else if (!skip && warp >= 2) {
         const int quarter = warp & 3;
         const int part = (warp - 2) >> 2;          // columns part*64 .. +63
         const int row = quarter * 32 + lane;
+        const uint32_t pe0 = tc::mapa_shared(tc::smem_u32(&sh->p_empty[0]), 0);
         uint32_t rc = 0;
-        for (int g = blockIdx.x; g < ntiles; g += gridDim.x, ++rc) {
+        for (int g = pair; g < ntiles; g += npairs, ++rc) {
             const int l = layer_of(p, g);
             const SumLayer& ly = p.L[l];
             int mb, nb;
             tile_coords(g - p.tile_begin[l], ly.m_blocks, ly.n_blocks, mb, nb);
-            const int64_t m = (int64_t)mb * kBM + row;
-            const int64_t n0 = (int64_t)nb * kBN + part * kColsPerWarp;
-            // the noise does not depend on the sum: drawn while the tensor cores accumulate
+            const int64_t m = (int64_t)mb * kPairTile + (int64_t)rank * kHalf + row;
+            const int64_t n0 = (int64_t)nb * kPairTile + part * kColsPerWarp;
             float z[kColsPerWarp];
             if (m < ly.d_out) {
 #pragma unroll
@@ -605,43 +651,61 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_sum_layers_tc(const __grid_
             if (!tc::mbar_wait(&sh->p_full[b], bph, abort_flag, p.status)) break;
             tc::tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + part * kColsPerWarp;
-            float* out = ly.G + m * ly.d_in + n0;
+            // the warp's 32 rows x 16 columns pass through its staging block so
+            // that each store instruction writes 8 rows x 64 contiguous bytes
+            const int64_t m_top = m - lane;
+            float4* stg = reinterpret_cast<float4*>(staging) + (warp - 2) * 128;
 #pragma unroll
             for (int ch = 0; ch < kColsPerWarp / 16; ++ch) {
                 float v[16];
                 tc::tmem_ld16(tb + ch * 16, v);
-                if (m >= ly.d_out) continue;
-                const int64_t n = n0 + ch * 16;
-                if (n + 16 <= ly.d_in) {
 #pragma unroll
-                    for (int j = 0; j < 16; j += 4) {
-                        float4 o;
-                        o.x = (v[j] + p.scale * z[ch * 16 + j]) * p.inv_L;
-                        o.y = (v[j + 1] + p.scale * z[ch * 16 + j + 1]) * p.inv_L;
-                        o.z = (v[j + 2] + p.scale * z[ch * 16 + j + 2]) * p.inv_L;
-                        o.w = (v[j + 3] + p.scale * z[ch * 16 + j + 3]) * p.inv_L;
-                        *reinterpret_cast<float4*>(out + ch * 16 + j) = o;
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (n + j < ly.d_in) out[ch * 16 + j] = (v[j] + p.scale * z[ch * 16 + j]) * p.inv_L;
+                for (int j4 = 0; j4 < 4; ++j4) {
+                    float4 o;
+                    o.x = (v[4 * j4] + p.scale * z[ch * 16 + 4 * j4]) * p.inv_L;
+                    o.y = (v[4 * j4 + 1] + p.scale * z[ch * 16 + 4 * j4 + 1]) * p.inv_L;
+                    o.z = (v[4 * j4 + 2] + p.scale * z[ch * 16 + 4 * j4 + 2]) * p.inv_L;
+                    o.w = (v[4 * j4 + 3] + p.scale * z[ch * 16 + 4 * j4 + 3]) * p.inv_L;
+                    stg[lane * 4 + (j4 ^ ((lane >> 1) & 3))] = o;
                 }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = i * 8 + (lane >> 2), q = lane & 3;
+                    const float4 o = stg[r * 4 + (q ^ ((r >> 1) & 3))];
+                    const int64_t mr = m_top + r;
+                    const int64_t n = n0 + ch * 16 + q * 4;
+                    if (mr < ly.d_out) {
+                        float* dst = ly.G + mr * ly.d_in + n;
+                        if (n + 4 <= ly.d_in) {
+                            *reinterpret_cast<float4*>(dst) = o;
+                        } else {
+                            if (n < ly.d_in) dst[0] = o.x;
+                            if (n + 1 < ly.d_in) dst[1] = o.y;
+                            if (n + 2 < ly.d_in) dst[2] = o.z;
+                        }
+                    }
+                }
+                __syncwarp();
             }
             tc::tc_fence_before();
-            tc::mbar_arrive(&sh->p_empty[b]);
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive_cluster(pe0 + (uint32_t)(b * sizeof(uint64_t)));
         }
     }
 
     if (!skip && warp == 1 && lane == 0) {
-        tc::mma_commit(&sh->drain);
+        if (rank == 0) tc::mma_commit_pair(&sh->drain, 0x3);
         tc::mbar_wait_drain(&sh->drain, 0);
     }
     tc::tc_fence_before();
     __syncthreads();
+    // neither CTA leaves (nor frees its TMEM) while the pair's MMAs, copies or
+    // arrivals may still touch it
+    tc::cluster_sync();
     if (warp == 1) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, kTmemCols);
+        tc::tmem_dealloc_pair(tmem, 2 * kAccCols);
     }
 }
 
@@ -678,31 +742,61 @@ bool tc_sum_supported(int dtype, int64_t d_in, int64_t d_out, int has_bias) {
     return dtype == DT_BF16 && d_in % 8 == 0 && d_out % 8 == 0 && d_in >= 64 && d_out >= 64;
 }
 
-bool tc_encode_sum(const GradTask& t, int64_t B, CUtensorMap* maps2) {
+bool tc_encode_sum(const GradTask& t, int64_t B, CUtensorMap* maps3) {
     const int64_t K = B * t.T;
     if (t.d_in % 64 == 0 && t.d_out % 64 == 0) {
-        // {64 columns, K rows, 64-column chunks}: one copy brings a whole tile
+        // {64 columns, K rows, 64-column chunks}: one copy brings a whole
+        // tile (E: 128 columns; A: 256 columns, or 128 for a CTA of a pair)
         const uint32_t be[3] = {64, (uint32_t)kBK, (uint32_t)(kBM / 64)};
         const uint32_t ba[3] = {64, (uint32_t)kBK, (uint32_t)(kBN / 64)};
+        const uint32_t bh[3] = {64, (uint32_t)kBK, (uint32_t)(kHalf / 64)};
         const uint64_t de[3] = {64, (uint64_t)K, (uint64_t)(t.d_out / 64)};
         const uint64_t se[2] = {(uint64_t)t.d_out * 2, 128};
         const uint64_t da[3] = {64, (uint64_t)K, (uint64_t)(t.d_in / 64)};
         const uint64_t sa[2] = {(uint64_t)t.d_in * 2, 128};
-        return encode(&maps2[0], t.E, 3, de, se, be, CU_TENSOR_MAP_SWIZZLE_128B) &&
-               encode(&maps2[1], t.A, 3, da, sa, ba, CU_TENSOR_MAP_SWIZZLE_128B);
+        return encode(&maps3[0], t.E, 3, de, se, be, CU_TENSOR_MAP_SWIZZLE_128B) &&
+               encode(&maps3[1], t.A, 3, da, sa, ba, CU_TENSOR_MAP_SWIZZLE_128B) &&
+               encode(&maps3[2], t.A, 3, da, sa, bh, CU_TENSOR_MAP_SWIZZLE_128B);
     }
     const uint32_t box[2] = {64, (uint32_t)kBK};
     const uint64_t de[2] = {(uint64_t)t.d_out, (uint64_t)K};
     const uint64_t se[1] = {(uint64_t)t.d_out * 2};
     const uint64_t da[2] = {(uint64_t)t.d_in, (uint64_t)K};
     const uint64_t sa[1] = {(uint64_t)t.d_in * 2};
-    return encode(&maps2[0], t.E, 2, de, se, box, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           encode(&maps2[1], t.A, 2, da, sa, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!encode(&maps3[0], t.E, 2, de, se, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode(&maps3[1], t.A, 2, da, sa, box, CU_TENSOR_MAP_SWIZZLE_128B))
+        return false;
+    maps3[2] = maps3[1];
+    return true;
 }
 
 size_t fold_scratch_floats(int sms) { return (size_t)sms * kBM * kBN; }
 
 int device_sm_count() { return sm_count_cached(); }
+
+// Clusters of two CTAs of the pair kernel resident at once on the current
+// device (queried once per device; half the SM count if the query fails).
+static int pair_clusters_cached(const void* kern, int smem) {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (unsigned)sm_count_cached());
+    cfg.blockDim = dim3(kFoldThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = sm_count_cached() / 2;
+        if (n < 1) n = 1;
+    }
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
 
 cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* status, const StepScalars& sc,
                                   const FoldWork* work, cudaStream_t s) {
@@ -717,7 +811,7 @@ cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* s
         p.tmE = t.maps[0];
         p.tmA = t.maps[1];
     } else {
-        CUtensorMap m[2];
+        CUtensorMap m[3];
         if (!tc_encode_sum(t, sc.B, m)) return cudaErrorInvalidValue;
         p.tmE = m[0];
         p.tmA = m[1];
@@ -774,8 +868,9 @@ cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* s
 cudaError_t launch_sum_layers_tc(const GradTask* tasks, int n, unsigned* status, const StepScalars& sc,
                                  cudaStream_t s) {
     if (n < 1 || n > kMaxSumLayers) return cudaErrorInvalidValue;
+    const void* kern = reinterpret_cast<const void*>(k_sum_layers_pair_tc);
     {
-        const cudaError_t a = ensure_smem_limit(reinterpret_cast<const void*>(k_sum_layers_tc), (int)kSumSmem);
+        const cudaError_t a = ensure_smem_limit(kern, (int)kPairSmem);
         if (a != cudaSuccess) return a;
     }
     LayersParams p;
@@ -789,17 +884,17 @@ cudaError_t launch_sum_layers_tc(const GradTask* tasks, int n, unsigned* status,
         SumLayer& L = p.L[l];
         if (t.maps) {
             L.tmE = t.maps[0];
-            L.tmA = t.maps[1];
+            L.tmA = t.maps[2];
         } else {
-            CUtensorMap m[2];
+            CUtensorMap m[3];
             if (!tc_encode_sum(t, 1, m)) return cudaErrorInvalidValue;
             L.tmE = m[0];
-            L.tmA = m[1];
+            L.tmA = m[2];
         }
         L.d_in = t.d_in;
         L.d_out = t.d_out;
-        L.m_blocks = (int)((t.d_out + kBM - 1) / kBM);
-        L.n_blocks = (int)((t.d_in + kBN - 1) / kBN);
+        L.m_blocks = (int)((t.d_out + kPairTile - 1) / kPairTile);
+        L.n_blocks = (int)((t.d_in + kPairTile - 1) / kPairTile);
         L.box3d = (t.d_in % 64 == 0 && t.d_out % 64 == 0) ? 1 : 0;
         L.G = t.G;
         L.coord_off = t.coord_off;
@@ -812,9 +907,9 @@ cudaError_t launch_sum_layers_tc(const GradTask* tasks, int n, unsigned* status,
     p.inv_L = 1.0f / sc.L;
     p.seed = sc.seed;
     p.step = sc.step;
-    const int sms = sm_count_cached();
-    const int grid = tiles < sms ? tiles : sms;
-    const cudaError_t e = launch_dependent(k_sum_layers_tc, dim3(grid), dim3(kFoldThreads), kSumSmem, s, p);
+    const int pairs = pair_clusters_cached(kern, (int)kPairSmem);
+    const int grid = 2 * (tiles < pairs ? tiles : pairs);
+    const cudaError_t e = launch_dependent(k_sum_layers_pair_tc, dim3(grid), dim3(kFoldThreads), kPairSmem, s, p);
     count_launches(1);
     return e;
 }
