@@ -405,7 +405,7 @@ def run_ours(args, w):
         # the layers sharing K in one launch of k_sum_layers_pair_tc
         kernel_name = ("k_grad_wsum" if roof["bound"] == "hbm"
                        else "k_sum_layers_pair_tc" if ghost_T and all(t % 64 for t in ghost_T)
-                       else "k_clipped_sum_fold_tc")
+                       else "k_clipped_sum_fold_pair_tc")
     roof["traffic"] = kernel_traffic(f"{kernel_name}@{w.name}")
     roof["kernel"] = kernel_name
     roof["phase"] = phase

@@ -155,7 +155,9 @@ int device_sm_count();
 bool tc_sum_supported(int dtype, int64_t d_in, int64_t d_out, int has_bias);
 bool tc_skinny_supported(int dtype, int64_t d_in, int64_t d_out, int has_bias);
 int nslots_skinny(int64_t d_in, int64_t d_out);
-// work == nullptr: every tile is done whole by one CTA
+// B > 1 (T % 64 == 0): the per-record fold on CTA pairs, the tiles of a
+// partial last wave cut into record ranges when work != nullptr; B == 1: one
+// record of T rows with factor c[0], one CTA per tile
 cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* status,
                                   const StepScalars& sc, const FoldWork* work, cudaStream_t s);
 // Single-record sums of up to kMaxSumLayersLaunch layers sharing K = T rows

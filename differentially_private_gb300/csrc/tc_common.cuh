@@ -80,6 +80,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     return mbar_wait_for(bar, parity, abort_flag, status, kWaitLimitNs);
 }
 
+// mbar_wait by all 32 lanes of a warp with one outcome for the warp: when
+// one lane gives up, every lane leaves, even one whose own wait succeeded,
+// so the warp stays converged for the .sync.aligned TMEM loads and warp
+// barriers that follow (a lane left behind at one of them would never be
+// joined).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                               unsigned* status) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status));
+}
+
 // Wait used only while draining before exit: ignores the abort flag, gives
 // up silently after the same wall-clock limit.
 __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) {

@@ -1,22 +1,26 @@
 // tcgen05 / TMA kernels for the reweighted clipped sum, whose operands are
 // both "row = contraction index" (MN-major) arrays:
 //
-//  * k_clipped_sum_fold_tc: the reweighted clipped sum of one layer,
+// The reweighted clipped sum of a layer,
 //        S = E^T diag(c) A = sum_i c_i E_i^T A_i     (K = B*T rows),
-//    and the noise epilogue G = (S + sigma C z) / L computed from TMEM
-//    ("Privacy-Preserving Machine Learning", section "Differentially private
-//    stochastic gradient descent", phases 3-5; "Sensitivity Inflation from
-//    Cross-Record Precision Routing in Private Quantized Fine-Tuning", Eq. 3).
-//    When T is a multiple of 64 the clip factor is folded per record in fp32
-//    (below).  Otherwise c_i A_i or c_i E_i (the operand with fewer columns)
-//    is first written into scratch -- by the clip kernel as soon as c_i is
-//    known (k_prescale_rows beyond four such layers) -- and this kernel runs
-//    as a single "record" of K rows with factor 1.
+// and the noise epilogue G = (S + sigma C z) / L computed from TMEM
+// ("Privacy-Preserving Machine Learning", section "Differentially private
+// stochastic gradient descent", phases 3-5; "Sensitivity Inflation from
+// Cross-Record Precision Routing in Private Quantized Fine-Tuning", Eq. 3):
+//
+//  * k_clipped_sum_fold_pair_tc: T a multiple of 64 and B > 1, the clip
+//    factor folded per record in fp32 by the epilogue warps, on CTA pairs.
+//  * otherwise c_i A_i or c_i E_i (the operand with fewer columns) is first
+//    written into scratch -- by the clip kernel as soon as c_i is known
+//    (k_prescale_rows beyond four such layers) -- and the sum runs as a
+//    single "record" of K rows with factor 1: k_sum_layers_pair_tc for the
+//    layers whose copy the clip kernel wrote (several layers per launch, CTA
+//    pairs), k_clipped_sum_tc for the others (one CTA per tile).
 //
 // Warp roles (one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer (one lane)
-//   warp 1      TMEM owner and MMA issuer (one lane)
-//   warps 2-17  fold S += c_i P_i, then the noise epilogue
+//   warp 1      TMEM owner and MMA issuer (one lane; rank 0 of a pair)
+//   warps 2-17  the epilogue: fold S += c_i P_i, noise, G
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -76,51 +80,29 @@ __device__ __forceinline__ void tile_coords(int tile, int m_blocks, int n_blocks
 }
 
 // ------------------------------------------------------------ work split
-// With records (B > 1), a CTA does the whole tiles blockIdx.x, + grid, ...
-// below full_tiles.  When the tile count leaves a partial last wave of R
-// tiles, the remaining tiles are each cut into nsplit = grid / R ranges of
-// records, all run at once: CTA b < R * nsplit takes tile full_tiles + b % R,
-// records of range b / R.  The CTAs working on one range read the same K rows
-// of E and A at the same time, as a whole wave would.  Every range writes its
-// partial sum to the CTA's scratch slot; the CTA that arrives last at the
-// tile's counter adds the slots in range order and writes G (a fixed order,
-// so the result does not depend on timing).
+// With records (B > 1), a CTA pair does the whole tiles pair, pair + npairs,
+// ... below full_tiles.  When the tile count leaves a partial last wave of R
+// tiles, the remaining tiles are each cut into nsplit = npairs / R ranges of
+// records, all run at once: pair b < R * nsplit takes tile full_tiles + b % R,
+// records of range b / R.  The pairs working on one range read the same K
+// rows of E and A at the same time, as a whole wave would.  Every range
+// writes its partial sum to the CTA's scratch slot; the CTA that arrives last
+// at the counter of its half of the tile adds the slots in range order and
+// writes G (a fixed order, so the result does not depend on timing).
 struct Work {
     int tile;
     int seg;            // record range of a split tile, -1 for a whole tile
     int64_t r0, r1;     // records [r0, r1)
 };
 
-__device__ __forceinline__ bool next_work(const SumParams& p, int ntiles, int64_t B, int& cursor, Work& w) {
-    if (cursor < p.full_tiles) {
-        w.tile = cursor;
-        w.seg = -1;
-        w.r0 = 0;
-        w.r1 = B;
-        cursor += gridDim.x;
-        return true;
-    }
-    if (cursor == INT_MAX || p.nsplit < 2) return false;
-    cursor = INT_MAX;
-    const int R = ntiles - p.full_tiles;
-    const int b = blockIdx.x;
-    if (b >= R * p.nsplit) return false;
-    w.tile = p.full_tiles + b % R;
-    w.seg = b / R;
-    w.r0 = (int64_t)w.seg * B / p.nsplit;
-    w.r1 = (int64_t)(w.seg + 1) * B / p.nsplit;
-    return true;
-}
-
-// ============================================== clipped sum, per-record fold
-// Requires T % 64 == 0 (every record spans whole 64-row K tiles) or a single
-// record (B = K / T = 1; a partial last K tile is zero-filled by TMA).  The
-// tensor cores accumulate each record's unscaled partial P_i = E_i^T A_i in
-// TMEM (two buffers) and the epilogue warps fold S += c_i * P_i in fp32
-// registers: the clip factor is applied exactly, without rounding a scaled
-// operand back to bf16.  Warps 2-17: four per TMEM lane quarter, each owning
-// 64 of the 256 columns (sixteen epilogue warps keep enough chains in flight
-// for the Philox / Box-Muller epilogue).
+// ====================================================== single-record sum
+// One record of K rows with factor 1 (the clip factors are in the pre-scaled
+// operand; a partial last K tile is zero-filled by TMA), one CTA per 128 x
+// 256 tile, tiles strided over the CTAs, the whole K accumulated in TMEM (two
+// buffers, so a tile's epilogue overlaps the next tile's MMAs).  Warps 2-17:
+// four per TMEM lane quarter, each owning 64 of the 256 columns (sixteen
+// epilogue warps keep enough chains in flight for the Philox / Box-Muller
+// epilogue).
 constexpr int kEpiWarps = 16;
 constexpr int kColsPerWarp = kBN / (kEpiWarps / 4);
 constexpr int kFoldThreads = 32 * (2 + kEpiWarps);
@@ -131,11 +113,8 @@ struct FoldSmem {
     uint64_t p_full[2];
     uint64_t p_empty[2];
     uint64_t drain;
-    uint64_t fix_in;    // the epilogue threads' partial sums of a split tile are written
-    uint64_t fix_out;   // the arrival at the tile's counter is decided
     uint32_t tmem_base;
     int abort_flag;
-    int fix_last;       // this CTA completes the split tile
 };
 
 // z for 8 consecutive coordinates starting at kb
@@ -167,15 +146,13 @@ __device__ __forceinline__ void add_noise_chunk(const SumParams& p, uint64_t k0,
         }
 }
 
-template <bool kMulti>
-__global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const __grid_constant__ SumParams p) {
+__global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_tc(const __grid_constant__ SumParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     FoldSmem* sh = reinterpret_cast<FoldSmem*>(tiles + (size_t)kStages * kStageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ntiles = p.m_blocks * p.n_blocks;
-    const int kpr = (int)((p.T + kBK - 1) / kBK);  // K tiles per record (zero-filled past K)
-    const int64_t B = p.K / p.T;
+    const int nk = (int)((p.K + kBK - 1) / kBK);  // K tiles (zero-filled past K)
     volatile int* abort_flag = &sh->abort_flag;
 
     if (threadIdx.x == 0) {
@@ -188,10 +165,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
             tc::mbar_init(&sh->p_empty[b], 32 * kEpiWarps);
         }
         tc::mbar_init(&sh->drain, 1);
-        tc::mbar_init(&sh->fix_in, 32 * kEpiWarps);
-        tc::mbar_init(&sh->fix_out, 1);
         sh->abort_flag = 0;
-        sh->fix_last = 0;
         tc::fence_barrier_init();
         tc::tma_prefetch_desc(&p.tmE);
         tc::tma_prefetch_desc(&p.tmA);
@@ -210,16 +184,13 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
     if (!skip && warp == 0) {
         if (lane == 0) {
             uint32_t it = 0;
-            int cursor = blockIdx.x;
-            Work wk;
-            while (next_work(p, ntiles, B, cursor, wk)) {
+            for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
                 int mb, nb;
-                tile_coords(wk.tile, p.m_blocks, p.n_blocks, mb, nb);
-                const int kt_end = (int)(wk.r1 * kpr);
-                for (int kt = (int)(wk.r0 * kpr); kt < kt_end; ++kt, ++it) {
+                tile_coords(tile, p.m_blocks, p.n_blocks, mb, nb);
+                for (int kt = 0; kt < nk; ++kt, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
-                    if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort_flag, p.status)) goto fold_producer_done;
+                    if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort_flag, p.status)) goto sum_producer_done;
                     uint8_t* st = tiles + (size_t)s * kStageBytes;
                     tc::mbar_arrive_expect_tx(&sh->full[s], kStageBytes);
                     const int k0 = kt * kBK;
@@ -235,41 +206,36 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
                     }
                 }
             }
-        fold_producer_done:
+        sum_producer_done:
             for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j)
                 tc::mbar_wait_drain(&sh->full[j % kStages], (j / kStages) & 1u);
         }
     } else if (!skip && warp == 1) {
         if (lane == 0) {
             uint32_t it = 0, rc = 0;
-            int cursor = blockIdx.x;
-            Work wk;
-            while (next_work(p, ntiles, B, cursor, wk)) {
+            for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++rc) {
+                const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
+                if (!tc::mbar_wait(&sh->p_empty[b], bph ^ 1u, abort_flag, p.status)) break;
+                tc::tc_fence_after();
+                const uint32_t d_tmem = tmem + b * kAccCols;
                 bool ok = true;
-                for (int64_t i = wk.r0; i < wk.r1 && ok; ++i, ++rc) {
-                    const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
-                    if (!tc::mbar_wait(&sh->p_empty[b], bph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                for (int kt = 0; kt < nk; ++kt, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1u;
+                    if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) { ok = false; break; }
                     tc::tc_fence_after();
-                    const uint32_t d_tmem = tmem + b * kAccCols;
-                    for (int kt = 0; kt < kpr; ++kt, ++it) {
-                        const int s = it % kStages;
-                        const uint32_t ph = (it / kStages) & 1u;
-                        if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) { ok = false; break; }
-                        tc::tc_fence_after();
-                        const uint32_t sa = tc::smem_u32(tiles + (size_t)s * kStageBytes);
-                        const uint32_t sb = sa + kAStage;
+                    const uint32_t sa = tc::smem_u32(tiles + (size_t)s * kStageBytes);
+                    const uint32_t sb = sa + kAStage;
 #pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk) {
-                            const uint64_t ad = tc::smem_desc(sa + kk * 2048, 8192, 1024, tc::SW_128B);
-                            const uint64_t bd = tc::smem_desc(sb + kk * 2048, 8192, 1024, tc::SW_128B);
-                            tc::mma_bf16(d_tmem, ad, bd, kIdescSum, (kt | kk) != 0);
-                        }
-                        tc::mma_commit(&sh->empty[s]);
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t ad = tc::smem_desc(sa + kk * 2048, 8192, 1024, tc::SW_128B);
+                        const uint64_t bd = tc::smem_desc(sb + kk * 2048, 8192, 1024, tc::SW_128B);
+                        tc::mma_bf16(d_tmem, ad, bd, kIdescSum, (kt | kk) != 0);
                     }
-                    if (!ok) break;
-                    tc::mma_commit(&sh->p_full[b]);
+                    tc::mma_commit(&sh->empty[s]);
                 }
                 if (!ok) break;
+                tc::mma_commit(&sh->p_full[b]);
             }
         }
     } else if (!skip && warp >= 2) {
@@ -277,9 +243,9 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
         const int part = (warp - 2) >> 2;          // columns part*64 .. +63
         const int row = quarter * 32 + lane;
         uint32_t rc = 0;
-        for (int tile = blockIdx.x; tile < ntiles && !kMulti; tile += gridDim.x, ++rc) {
-            // one record: the noise does not depend on the sum, so it is drawn
-            // while the tensor cores are still accumulating this tile
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++rc) {
+            // the noise does not depend on the sum: drawn while the tensor
+            // cores are still accumulating this tile
             int mb, nb;
             tile_coords(tile, p.m_blocks, p.n_blocks, mb, nb);
             const int64_t m = (int64_t)mb * kBM + row;
@@ -295,7 +261,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
                 }
             }
             const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
-            if (!tc::mbar_wait(&sh->p_full[b], bph, abort_flag, p.status)) break;
+            if (!tc::mbar_wait_warp(&sh->p_full[b], bph, abort_flag, p.status)) break;
             tc::tc_fence_after();
             const float c0 = __ldca(p.c);
             const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + part * kColsPerWarp;
@@ -325,112 +291,6 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
             tc::tc_fence_before();
             tc::mbar_arrive(&sh->p_empty[b]);
         }
-        int cursor = blockIdx.x;
-        Work wk;
-        uint32_t fix_phase = 0;
-        while (kMulti && next_work(p, ntiles, B, cursor, wk)) {
-            int mb, nb;
-            tile_coords(wk.tile, p.m_blocks, p.n_blocks, mb, nb);
-            const int64_t m = (int64_t)mb * kBM + row;
-            const int64_t n0 = (int64_t)nb * kBN + part * kColsPerWarp;
-            const uint64_t k0 = (uint64_t)(p.coord_off + m * p.d_in + n0);   // this thread's first coordinate
-            // the range holding the tile's first record also carries its noise
-            const bool noisy = wk.r0 == 0 && m < p.d_out;
-            float S[kColsPerWarp];
-#pragma unroll
-            for (int j = 0; j < kColsPerWarp; ++j) S[j] = 0.f;
-            bool ok = true;
-            for (int64_t i = wk.r0; i < wk.r1; ++i, ++rc) {
-                const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
-                if (!tc::mbar_wait(&sh->p_full[b], bph, abort_flag, p.status)) { ok = false; break; }
-                tc::tc_fence_after();
-                const float ci = __ldca(p.c + i);
-                const uint32_t tb =
-                    tmem + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + part * kColsPerWarp;
-#pragma unroll
-                for (int ch = 0; ch < kColsPerWarp / 16; ++ch) {
-                    float v[16];
-                    tc::tmem_ld16(tb + ch * 16, v);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) S[ch * 16 + j] = fmaf(ci, v[j], S[ch * 16 + j]);
-                }
-                tc::tc_fence_before();
-                tc::mbar_arrive(&sh->p_empty[b]);
-                // the noise joins the sum four columns at a time, one chunk after
-                // each of the first records, while the tensor cores work on the next
-                if (noisy && i < kNoiseChunks) add_noise_chunk(p, k0, (int)i, S);
-            }
-            if (!ok) break;
-            if (noisy)
-                for (int q = (int)(wk.r1 < kNoiseChunks ? wk.r1 : kNoiseChunks); q < kNoiseChunks; ++q)
-                    add_noise_chunk(p, k0, q, S);
-            if (wk.seg >= 0) {
-                // split tile: the range's partial sum to this CTA's slot, then the counter
-                const int R = ntiles - p.full_tiles;
-                const int r = wk.tile - p.full_tiles;
-                float* slot = p.scratch + (size_t)blockIdx.x * (kBM * kBN);
-#pragma unroll
-                for (int j = 0; j < kColsPerWarp; ++j) slot[(size_t)(part * kColsPerWarp + j) * kBM + row] = S[j];
-                __threadfence();
-                tc::mbar_arrive(&sh->fix_in);
-                if (warp == 2 && lane == 0) {
-                    int last = 0;
-                    if (tc::mbar_wait(&sh->fix_in, fix_phase, abort_flag, p.status)) {
-                        __threadfence();
-                        unsigned long long* cp = p.counters + r;
-                        unsigned long long seen = *(volatile unsigned long long*)cp, prev;
-                        do {
-                            prev = seen;
-                            const unsigned long long want = (unsigned)(prev >> 32) == p.epoch
-                                                                ? prev + 1
-                                                                : ((unsigned long long)p.epoch << 32) | 1ull;
-                            seen = atomicCAS(cp, prev, want);
-                        } while (seen != prev);
-                        const unsigned before = (unsigned)(prev >> 32) == p.epoch ? (unsigned)prev : 0u;
-                        last = before + 1 == (unsigned)p.nsplit ? 1 : 0;
-                        __threadfence();
-                    }
-                    *(volatile int*)&sh->fix_last = last;
-                    tc::mbar_arrive(&sh->fix_out);
-                }
-                const bool waited = tc::mbar_wait(&sh->fix_out, fix_phase, abort_flag, p.status);
-                fix_phase ^= 1u;
-                if (!waited) break;
-                if (!*(volatile int*)&sh->fix_last) continue;
-                // last arrival: the ranges' partial sums in range order
-#pragma unroll
-                for (int j = 0; j < kColsPerWarp; ++j) S[j] = 0.f;
-                for (int sg = 0; sg < p.nsplit; ++sg) {
-                    const float* src = p.scratch + (size_t)(r + sg * R) * (kBM * kBN);
-#pragma unroll
-                    for (int j = 0; j < kColsPerWarp; ++j)
-                        S[j] += __ldcg(src + (size_t)(part * kColsPerWarp + j) * kBM + row);
-                }
-            }
-            if (m < p.d_out) {
-#pragma unroll
-                for (int ch = 0; ch < kColsPerWarp / 8; ++ch) {
-                    const int64_t n = n0 + ch * 8;
-                    if (n >= p.d_in) continue;
-                    float* out = p.G + m * p.d_in + n;
-                    if (n + 8 <= p.d_in) {
-#pragma unroll
-                        for (int j = 0; j < 8; j += 4) {
-                            float4 o;
-                            o.x = S[ch * 8 + j] * p.inv_L;
-                            o.y = S[ch * 8 + j + 1] * p.inv_L;
-                            o.z = S[ch * 8 + j + 2] * p.inv_L;
-                            o.w = S[ch * 8 + j + 3] * p.inv_L;
-                            *reinterpret_cast<float4*>(out + j) = o;
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (n + j < p.d_in) out[j] = S[ch * 8 + j] * p.inv_L;
-                    }
-                }
-            }
-        }
     }
 
     if (!skip && warp == 1 && lane == 0) {
@@ -447,7 +307,7 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_fold_tc(const _
 
 // ================================= single-record sums of several layers
 // Layers whose clip factors the clip kernel folded into a pre-scaled operand
-// are sums over K = B*T rows with factor 1 (as k_clipped_sum_fold_tc<false>).
+// are sums over K = B*T rows with factor 1 (as k_clipped_sum_tc).
 // Layers sharing K are summed in one persistent launch, k_sum_layers_pair_tc:
 // their output tiles form one index space, strided over the CTA pairs, so a
 // layer's tiles fill the SMs another layer's partial wave leaves idle, and
@@ -648,7 +508,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
                 }
             }
             const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
-            if (!tc::mbar_wait(&sh->p_full[b], bph, abort_flag, p.status)) break;
+            if (!tc::mbar_wait_warp(&sh->p_full[b], bph, abort_flag, p.status)) break;
             tc::tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + part * kColsPerWarp;
             // the warp's 32 rows x 16 columns pass through its staging block so
@@ -702,6 +562,295 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
     __syncthreads();
     // neither CTA leaves (nor frees its TMEM) while the pair's MMAs, copies or
     // arrivals may still touch it
+    tc::cluster_sync();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc_pair(tmem, 2 * kAccCols);
+    }
+}
+
+// ============================================== per-record fold on CTA pairs
+// T % 64 == 0 and B > 1: every record spans whole 64-row K tiles.  The tensor
+// cores accumulate each record's unscaled partial P_i = E_i^T A_i in TMEM
+// (two buffers) and the epilogue warps fold S += c_i * P_i in fp32
+// registers: the clip factor is applied exactly, without rounding a scaled
+// operand back to bf16.  Clusters of two CTAs with the operand staging and
+// MMAs of k_sum_layers_pair_tc: 256 x 256 output tiles, each CTA staging its
+// 128 columns of E and A per K step, its TMEM receiving its 128 rows of every
+// record's partial, its epilogue warps folding those rows.  The record-range
+// split of the last partial wave (see "work split") works per pair tile; each
+// CTA of a pair keeps its half's partial sum in its own scratch slot, and the
+// arrival counters are per (tile, half), so the CTA arriving last among the
+// ranges of a half adds that half's slots in range order.
+constexpr int kFoldPairStages = 6;
+
+struct FoldPairSmem {
+    uint64_t full[kFoldPairStages];
+    uint64_t empty[kFoldPairStages];
+    uint64_t p_full[2];
+    uint64_t p_empty[2];
+    uint64_t drain;
+    uint64_t fix_in;
+    uint64_t fix_out;
+    uint32_t tmem_base;
+    int abort_flag;
+    int fix_last;
+};
+static_assert(sizeof(FoldPairSmem) <= 256, "pair fold barriers exceed their shared-memory slot");
+constexpr size_t kFoldPairSmem = 1024 + (size_t)kFoldPairStages * kPairStageBytes + 256;
+
+// next_work over CTA pairs: whole pair tiles pair, pair + npairs, ... below
+// full_tiles, then (with nsplit > 1) pair < R * nsplit takes record range
+// pair / R of the remaining tile full_tiles + pair % R
+__device__ __forceinline__ bool next_pair_work(const SumParams& p, int ntiles, int64_t B, int pair, int npairs,
+                                               int& cursor, Work& w) {
+    if (cursor < p.full_tiles) {
+        w.tile = cursor;
+        w.seg = -1;
+        w.r0 = 0;
+        w.r1 = B;
+        cursor += npairs;
+        return true;
+    }
+    if (cursor == INT_MAX || p.nsplit < 2) return false;
+    cursor = INT_MAX;
+    const int R = ntiles - p.full_tiles;
+    if (pair >= R * p.nsplit) return false;
+    w.tile = p.full_tiles + pair % R;
+    w.seg = pair / R;
+    w.r0 = (int64_t)w.seg * B / p.nsplit;
+    w.r1 = (int64_t)(w.seg + 1) * B / p.nsplit;
+    return true;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
+    k_clipped_sum_fold_pair_tc(const __grid_constant__ SumParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    FoldPairSmem* sh = reinterpret_cast<FoldPairSmem*>(tiles + (size_t)kFoldPairStages * kPairStageBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = tc::cluster_ctarank();
+    const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+    const int ntiles = p.m_blocks * p.n_blocks;
+    const int kpr = (int)((p.T + kBK - 1) / kBK);
+    const int64_t B = p.K / p.T;
+    volatile int* abort_flag = &sh->abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kFoldPairStages; ++s) {
+            tc::mbar_init(&sh->full[s], 1);
+            tc::mbar_init(&sh->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&sh->p_full[b], 1);
+            tc::mbar_init(&sh->p_empty[b], 2 * kEpiWarps);
+        }
+        tc::mbar_init(&sh->drain, 1);
+        tc::mbar_init(&sh->fix_in, 32 * kEpiWarps);
+        tc::mbar_init(&sh->fix_out, 1);
+        sh->abort_flag = 0;
+        sh->fix_last = 0;
+        tc::fence_barrier_init();
+        tc::tma_prefetch_desc(&p.tmE);
+        tc::tma_prefetch_desc(&p.tmA);
+    }
+    if (warp == 1) tc::tmem_alloc_pair(&sh->tmem_base, 2 * kAccCols);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::cluster_sync();
+    tc::tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+    grid_dep_wait();
+    grid_dep_trigger();
+    const bool skip = status_bad(p.status);
+
+    if (!skip && warp == 0) {
+        if (lane == 0) {
+            const uint32_t full0 = tc::mapa_shared(tc::smem_u32(&sh->full[0]), 0);
+            uint32_t it = 0;
+            int cursor = pair;
+            Work wk;
+            while (next_pair_work(p, ntiles, B, pair, npairs, cursor, wk)) {
+                int mb, nb;
+                tile_coords(wk.tile, p.m_blocks, p.n_blocks, mb, nb);
+                const int kt_end = (int)(wk.r1 * kpr);
+                for (int kt = (int)(wk.r0 * kpr); kt < kt_end; ++kt, ++it) {
+                    const int s = it % kFoldPairStages;
+                    const uint32_t ph = (it / kFoldPairStages) & 1u;
+                    if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort_flag, p.status)) goto fold_pair_producer_done;
+                    uint8_t* st = tiles + (size_t)s * kPairStageBytes;
+                    if (rank == 0) tc::mbar_arrive_expect_tx(&sh->full[s], 2 * kPairStageBytes);
+                    const uint32_t fb = full0 + (uint32_t)(s * sizeof(uint64_t));
+                    const int k0 = kt * kBK;
+                    if (p.box3d) {
+                        tc::tma_load_3d_pair(st, &p.tmE, fb, 0, k0, mb * (kPairTile / 64) + (int)rank * (kHalf / 64));
+                        tc::tma_load_3d_pair(st + kPairEStage, &p.tmA, fb, 0, k0,
+                                             nb * (kPairTile / 64) + (int)rank * (kHalf / 64));
+                    } else {
+                        const int xe = mb * kPairTile + (int)rank * kHalf, xa = nb * kPairTile + (int)rank * kHalf;
+                        tc::tma_load_2d_pair(st, &p.tmE, fb, xe, k0);
+                        tc::tma_load_2d_pair(st + 8192, &p.tmE, fb, xe + 64, k0);
+                        tc::tma_load_2d_pair(st + kPairEStage, &p.tmA, fb, xa, k0);
+                        tc::tma_load_2d_pair(st + kPairEStage + 8192, &p.tmA, fb, xa + 64, k0);
+                    }
+                }
+            }
+        fold_pair_producer_done:
+            if (rank == 0)
+                for (uint32_t j = it > kFoldPairStages ? it - kFoldPairStages : 0; j < it; ++j)
+                    tc::mbar_wait_drain(&sh->full[j % kFoldPairStages], (j / kFoldPairStages) & 1u);
+        }
+    } else if (!skip && warp == 1) {
+        if (lane == 0 && rank == 0) {
+            uint32_t it = 0, rc = 0;
+            int cursor = pair;
+            Work wk;
+            while (next_pair_work(p, ntiles, B, pair, npairs, cursor, wk)) {
+                bool ok = true;
+                for (int64_t i = wk.r0; i < wk.r1 && ok; ++i, ++rc) {
+                    const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
+                    if (!tc::mbar_wait(&sh->p_empty[b], bph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    const uint32_t d_tmem = tmem + b * kAccCols;
+                    for (int kt = 0; kt < kpr; ++kt, ++it) {
+                        const int s = it % kFoldPairStages;
+                        const uint32_t ph = (it / kFoldPairStages) & 1u;
+                        if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) { ok = false; break; }
+                        tc::tc_fence_after();
+                        const uint32_t sa = tc::smem_u32(tiles + (size_t)s * kPairStageBytes);
+                        const uint32_t sb = sa + kPairEStage;
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            const uint64_t ad = tc::smem_desc(sa + kk * 2048, 8192, 1024, tc::SW_128B);
+                            const uint64_t bd = tc::smem_desc(sb + kk * 2048, 8192, 1024, tc::SW_128B);
+                            tc::mma_bf16_pair(d_tmem, ad, bd, kIdescPair, (kt | kk) != 0);
+                        }
+                        tc::mma_commit_pair(&sh->empty[s], 0x3);
+                    }
+                    if (!ok) break;
+                    tc::mma_commit_pair(&sh->p_full[b], 0x3);
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (!skip && warp >= 2) {
+        const int quarter = warp & 3;
+        const int part = (warp - 2) >> 2;          // columns part*64 .. +63
+        const int row = quarter * 32 + lane;
+        const uint32_t pe0 = tc::mapa_shared(tc::smem_u32(&sh->p_empty[0]), 0);
+        uint32_t rc = 0, fix_phase = 0;
+        int cursor = pair;
+        Work wk;
+        while (next_pair_work(p, ntiles, B, pair, npairs, cursor, wk)) {
+            int mb, nb;
+            tile_coords(wk.tile, p.m_blocks, p.n_blocks, mb, nb);
+            const int64_t m = (int64_t)mb * kPairTile + (int64_t)rank * kHalf + row;
+            const int64_t n0 = (int64_t)nb * kPairTile + part * kColsPerWarp;
+            const uint64_t k0 = (uint64_t)(p.coord_off + m * p.d_in + n0);   // this thread's first coordinate
+            // the range holding the tile's first record also carries its noise
+            const bool noisy = wk.r0 == 0 && m < p.d_out;
+            float S[kColsPerWarp];
+#pragma unroll
+            for (int j = 0; j < kColsPerWarp; ++j) S[j] = 0.f;
+            bool ok = true;
+            for (int64_t i = wk.r0; i < wk.r1; ++i, ++rc) {
+                const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
+                if (!tc::mbar_wait_warp(&sh->p_full[b], bph, abort_flag, p.status)) { ok = false; break; }
+                tc::tc_fence_after();
+                const float ci = __ldca(p.c + i);
+                const uint32_t tb =
+                    tmem + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + part * kColsPerWarp;
+#pragma unroll
+                for (int ch = 0; ch < kColsPerWarp / 16; ++ch) {
+                    float v[16];
+                    tc::tmem_ld16(tb + ch * 16, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) S[ch * 16 + j] = fmaf(ci, v[j], S[ch * 16 + j]);
+                }
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive_cluster(pe0 + (uint32_t)(b * sizeof(uint64_t)));
+                if (noisy && i < kNoiseChunks) add_noise_chunk(p, k0, (int)i, S);
+            }
+            if (!ok) break;
+            if (noisy)
+                for (int q = (int)(wk.r1 < kNoiseChunks ? wk.r1 : kNoiseChunks); q < kNoiseChunks; ++q)
+                    add_noise_chunk(p, k0, q, S);
+            if (wk.seg >= 0) {
+                // split tile: this half's partial sum to the CTA's slot, then the half's counter
+                const int R = ntiles - p.full_tiles;
+                const int r = wk.tile - p.full_tiles;
+                float* slot = p.scratch + (size_t)blockIdx.x * (kBM * kBN);
+#pragma unroll
+                for (int j = 0; j < kColsPerWarp; ++j) slot[(size_t)(part * kColsPerWarp + j) * kBM + row] = S[j];
+                __threadfence();
+                tc::mbar_arrive(&sh->fix_in);
+                if (warp == 2 && lane == 0) {
+                    int last = 0;
+                    if (tc::mbar_wait(&sh->fix_in, fix_phase, abort_flag, p.status)) {
+                        __threadfence();
+                        unsigned long long* cp = p.counters + 2 * r + (int)rank;
+                        unsigned long long seen = *(volatile unsigned long long*)cp, prev;
+                        do {
+                            prev = seen;
+                            const unsigned long long want = (unsigned)(prev >> 32) == p.epoch
+                                                                ? prev + 1
+                                                                : ((unsigned long long)p.epoch << 32) | 1ull;
+                            seen = atomicCAS(cp, prev, want);
+                        } while (seen != prev);
+                        const unsigned before = (unsigned)(prev >> 32) == p.epoch ? (unsigned)prev : 0u;
+                        last = before + 1 == (unsigned)p.nsplit ? 1 : 0;
+                        __threadfence();
+                    }
+                    *(volatile int*)&sh->fix_last = last;
+                    tc::mbar_arrive(&sh->fix_out);
+                }
+                const bool waited = tc::mbar_wait_warp(&sh->fix_out, fix_phase, abort_flag, p.status);
+                fix_phase ^= 1u;
+                if (!waited) break;
+                if (!*(volatile int*)&sh->fix_last) continue;
+                // last arrival for this half: the ranges' partial sums in range order
+#pragma unroll
+                for (int j = 0; j < kColsPerWarp; ++j) S[j] = 0.f;
+                for (int sg = 0; sg < p.nsplit; ++sg) {
+                    const float* src = p.scratch + (size_t)(2 * (r + sg * R) + (int)rank) * (kBM * kBN);
+#pragma unroll
+                    for (int j = 0; j < kColsPerWarp; ++j)
+                        S[j] += __ldcg(src + (size_t)(part * kColsPerWarp + j) * kBM + row);
+                }
+            }
+            if (m < p.d_out) {
+#pragma unroll
+                for (int ch = 0; ch < kColsPerWarp / 8; ++ch) {
+                    const int64_t n = n0 + ch * 8;
+                    if (n >= p.d_in) continue;
+                    float* out = p.G + m * p.d_in + n;
+                    if (n + 8 <= p.d_in) {
+#pragma unroll
+                        for (int j = 0; j < 8; j += 4) {
+                            float4 o;
+                            o.x = S[ch * 8 + j] * p.inv_L;
+                            o.y = S[ch * 8 + j + 1] * p.inv_L;
+                            o.z = S[ch * 8 + j + 2] * p.inv_L;
+                            o.w = S[ch * 8 + j + 3] * p.inv_L;
+                            *reinterpret_cast<float4*>(out + j) = o;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (n + j < p.d_in) out[j] = S[ch * 8 + j] * p.inv_L;
+                    }
+                }
+            }
+        }
+    }
+
+    if (!skip && warp == 1 && lane == 0) {
+        if (rank == 0) tc::mma_commit_pair(&sh->drain, 0x3);
+        tc::mbar_wait_drain(&sh->drain, 0);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
     tc::cluster_sync();
     if (warp == 1) {
         tc::tc_fence_after();
@@ -774,10 +923,10 @@ size_t fold_scratch_floats(int sms) { return (size_t)sms * kBM * kBN; }
 
 int device_sm_count() { return sm_count_cached(); }
 
-// Clusters of two CTAs of the pair kernel resident at once on the current
-// device (queried once per device; half the SM count if the query fails).
-static int pair_clusters_cached(const void* kern, int smem) {
-    static std::atomic<int> cache[64];
+// Clusters of two CTAs of a pair kernel resident at once on the current
+// device (queried once per device and kernel, kept in `cache`; half the SM
+// count if the query fails).
+static int pair_clusters_cached(const void* kern, int smem, std::atomic<int> (&cache)[64]) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64) {
@@ -798,12 +947,80 @@ static int pair_clusters_cached(const void* kern, int smem) {
     return n;
 }
 
+// records mode (B > 1, T % 64 == 0) on CTA pairs; work == nullptr: every
+// tile is done whole by one pair
+static cudaError_t launch_fold_pair(const GradTask& t, const float* c, unsigned* status, const StepScalars& sc,
+                                   const FoldWork* work, cudaStream_t s) {
+    const void* kern = reinterpret_cast<const void*>(k_clipped_sum_fold_pair_tc);
+    {
+        const cudaError_t a = ensure_smem_limit(kern, (int)kFoldPairSmem);
+        if (a != cudaSuccess) return a;
+    }
+    SumParams p;
+    if (t.maps) {
+        p.tmE = t.maps[0];
+        p.tmA = t.maps[2];
+    } else {
+        CUtensorMap m[3];
+        if (!tc_encode_sum(t, sc.B, m)) return cudaErrorInvalidValue;
+        p.tmE = m[0];
+        p.tmA = m[2];
+    }
+    p.K = sc.B * t.T;
+    p.T = t.T;
+    p.box3d = (t.d_in % 64 == 0 && t.d_out % 64 == 0) ? 1 : 0;
+    p.d_in = t.d_in;
+    p.d_out = t.d_out;
+    p.m_blocks = (int)((t.d_out + kPairTile - 1) / kPairTile);
+    p.n_blocks = (int)((t.d_in + kPairTile - 1) / kPairTile);
+    p.c = c;
+    p.status = status;
+    p.G = t.G;
+    p.coord_off = t.coord_off;
+    p.scale = sc.sigma * sc.C;
+    p.inv_L = 1.0f / sc.L;
+    p.seed = sc.seed;
+    p.step = sc.step;
+    const int ntiles = p.m_blocks * p.n_blocks;
+    static std::atomic<int> clusters[64];
+    const int pairs = pair_clusters_cached(kern, (int)kFoldPairSmem, clusters);
+    int npairs = ntiles < pairs ? ntiles : pairs;
+    p.full_tiles = ntiles;
+    p.nsplit = 1;
+    p.scratch = nullptr;
+    p.counters = nullptr;
+    p.epoch = 0;
+    if (work != nullptr && 2 * pairs <= sm_count_cached()) {
+        // split the R pair tiles of a partial last wave into pairs / R record
+        // ranges (each at least 8 K tiles) when the wave would leave over 4%
+        // of the pair slots idle; a CTA's scratch slot and a (tile, half)
+        // counter are indexed below the SM count
+        const int R = ntiles % pairs;
+        const int waves = (ntiles + pairs - 1) / pairs;
+        const double idle = (double)((int64_t)waves * pairs - ntiles) / ((double)waves * pairs);
+        const int64_t kpr = (t.T + kBK - 1) / kBK;
+        int S = R > 0 ? pairs / R : 1;
+        while (S > 1 && (sc.B / S) * kpr < 8) --S;
+        if (R > 0 && S >= 2 && idle > 0.04) {
+            p.full_tiles = ntiles - R;
+            p.nsplit = S;
+            p.scratch = work->scratch;
+            p.counters = work->counters;
+            p.epoch = work->epoch;
+            npairs = pairs;
+        }
+    }
+    const cudaError_t e = launch_dependent(k_clipped_sum_fold_pair_tc, dim3(2 * npairs), dim3(kFoldThreads), kFoldPairSmem, s, p);
+    count_launches(1);
+    return e;
+}
+
 cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* status, const StepScalars& sc,
                                   const FoldWork* work, cudaStream_t s) {
+    if (sc.B > 1) return launch_fold_pair(t, c, status, sc, work, s);
+    // one record of t.T rows (with factor c[0])
     {
-        const void* k = sc.B > 1 ? reinterpret_cast<const void*>(k_clipped_sum_fold_tc<true>)
-                                 : reinterpret_cast<const void*>(k_clipped_sum_fold_tc<false>);
-        const cudaError_t a = ensure_smem_limit(k, (int)kSumSmem);
+        const cudaError_t a = ensure_smem_limit(reinterpret_cast<const void*>(k_clipped_sum_tc), (int)kSumSmem);
         if (a != cudaSuccess) return a;
     }
     SumParams p;
@@ -812,11 +1029,11 @@ cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* s
         p.tmA = t.maps[1];
     } else {
         CUtensorMap m[3];
-        if (!tc_encode_sum(t, sc.B, m)) return cudaErrorInvalidValue;
+        if (!tc_encode_sum(t, 1, m)) return cudaErrorInvalidValue;
         p.tmE = m[0];
         p.tmA = m[1];
     }
-    p.K = sc.B * t.T;
+    p.K = t.T;
     p.T = t.T;
     p.box3d = (t.d_in % 64 == 0 && t.d_out % 64 == 0) ? 1 : 0;
     p.d_in = t.d_in;
@@ -831,36 +1048,15 @@ cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* s
     p.inv_L = 1.0f / sc.L;
     p.seed = sc.seed;
     p.step = sc.step;
-    const int ntiles = p.m_blocks * p.n_blocks;
-    const int sms = sm_count_cached();
-    int grid = ntiles < sms ? ntiles : sms;
-    p.full_tiles = ntiles;
+    p.full_tiles = p.m_blocks * p.n_blocks;
     p.nsplit = 1;
     p.scratch = nullptr;
     p.counters = nullptr;
     p.epoch = 0;
-    if (work != nullptr && sc.B > 1) {
-        // split the R tiles of a partial last wave into grid / R record ranges
-        // (each at least 8 K tiles) when the wave would leave over 4% of the
-        // CTA slots idle
-        const int R = ntiles % sms;
-        const int waves = (ntiles + sms - 1) / sms;
-        const double idle = (double)((int64_t)waves * sms - ntiles) / ((double)waves * sms);
-        const int64_t kpr = (t.T + kBK - 1) / kBK;
-        int S = R > 0 ? sms / R : 1;
-        while (S > 1 && (sc.B / S) * kpr < 8) --S;
-        if (R > 0 && S >= 2 && idle > 0.04) {
-            p.full_tiles = ntiles - R;
-            p.nsplit = S;
-            p.scratch = work->scratch;
-            p.counters = work->counters;
-            p.epoch = work->epoch;
-            grid = sms;
-        }
-    }
-    const cudaError_t e =
-        sc.B > 1 ? launch_dependent(k_clipped_sum_fold_tc<true>, dim3(grid), dim3(kFoldThreads), kSumSmem, s, p)
-                 : launch_dependent(k_clipped_sum_fold_tc<false>, dim3(grid), dim3(kFoldThreads), kSumSmem, s, p);
+    const int ntiles = p.full_tiles;
+    const int sms = sm_count_cached();
+    const int grid = ntiles < sms ? ntiles : sms;
+    const cudaError_t e = launch_dependent(k_clipped_sum_tc, dim3(grid), dim3(kFoldThreads), kSumSmem, s, p);
     count_launches(1);
     return e;
 }
@@ -907,7 +1103,8 @@ cudaError_t launch_sum_layers_tc(const GradTask* tasks, int n, unsigned* status,
     p.inv_L = 1.0f / sc.L;
     p.seed = sc.seed;
     p.step = sc.step;
-    const int pairs = pair_clusters_cached(kern, (int)kPairSmem);
+    static std::atomic<int> clusters[64];
+    const int pairs = pair_clusters_cached(kern, (int)kPairSmem, clusters);
     const int grid = 2 * (tiles < pairs ? tiles : pairs);
     const cudaError_t e = launch_dependent(k_sum_layers_pair_tc, dim3(grid), dim3(kFoldThreads), kPairSmem, s, p);
     count_launches(1);

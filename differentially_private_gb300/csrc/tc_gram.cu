@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
             const int tl = item % p.tiles_per_rec;
             int pb, qb;
             gram_tile(tl, p.np, p.nq, pb, qb);
-            if (!tc::mbar_wait(&sh->acc_full, lt & 1u, abort_flag, p.status)) break;
+            if (!tc::mbar_wait_warp(&sh->acc_full, lt & 1u, abort_flag, p.status)) break;
             tc::tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16);
             const float bias = p.has_bias ? 1.f : 0.f;

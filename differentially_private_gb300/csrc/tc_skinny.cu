@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_mat_skinny_tc(const __grid_cons
             const SkinnyLayer& ly = p.L[cur];
             const uint32_t a = lt % kAccSets, aph = (lt / kAccSets) & 1u;
             ++lt;
-            if (!tc::mbar_wait(&sh->acc_full[a], aph, abort_flag, p.status)) break;
+            if (!tc::mbar_wait_warp(&sh->acc_full[a], aph, abort_flag, p.status)) break;
             tc::tc_fence_after();
             const int64_t ncl = ly.r * ly.D;
             float* g = ly.gstore ? ly.gstore + (int64_t)in.rec * ncl : nullptr;

@@ -23,7 +23,9 @@ from oracle import philox
 
 pytestmark = pytest.mark.gpu
 
-TILE_M, TILE_N = 128, 256   # output tile of the kernel: rows of d_out x columns of d_in
+# errors are checked per 128 x 256 block (rows of d_out x columns of d_in); the
+# per-record fold runs on 256 x 256 tiles of CTA pairs, each CTA folding 128 rows
+TILE_M, TILE_N = 128, 256
 
 
 def _inputs(B, T, d_in, d_out, seed):
@@ -48,8 +50,8 @@ def _tile_errors(got, want, d_out, d_in):
 
 
 @pytest.mark.parametrize("B,T,d_in,d_out", [
-    (40, 512, 512, 256),    # 4 tiles of 40 records, each cut into 38 ranges
-    (20, 512, 2560, 2048),  # 160 tiles: one full wave, then 8 tiles cut into 19 ranges
+    (40, 512, 512, 256),    # 2 pair tiles of 40 records, each cut into 38 ranges (76 pairs)
+    (20, 512, 2560, 2048),  # 80 pair tiles: one full wave of 76, then 4 tiles cut into 19 ranges
     (6500, 3, 256, 512),    # one pre-scaled record of 19500 rows: whole tiles
 ])
 def test_split_tiles_match_oracle(B, T, d_in, d_out):
