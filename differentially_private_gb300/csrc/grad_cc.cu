@@ -332,6 +332,78 @@ __global__ void __launch_bounds__(256) k_grad_gemm_cc(const GradTask t, const fl
     }
 }
 
+// The same sum for outputs too small to occupy the GPU with 64 x 64 tiles:
+// one 16 x 16 tile per block, one output per thread, K in chunks of 64 rows
+// (the first fetched before the dependency wait, as above).  A block whose
+// tile starts the row holds the bias sums of its 16 rows.
+constexpr int kSmallTile = 16, kSmallBK = 64;
+constexpr int kSmallLoads = kSmallBK * kSmallTile / 256;   // elements of each operand a thread stages per chunk
+
+template <int DT>
+__global__ void __launch_bounds__(256) k_grad_gemm_small(const GradTask t, const float* __restrict__ c,
+                                                         const unsigned* __restrict__ status, StepScalars sc) {
+    using Tt = typename Elem<DT>::T;
+    __shared__ float Es[kSmallBK][kSmallTile];
+    __shared__ float As[kSmallBK][kSmallTile];
+    const int tid = threadIdx.x;
+    const int tr = tid >> 4, tc = tid & 15;   // output row and column within the tile
+    const int64_t m0 = (int64_t)blockIdx.y * kSmallTile, n0 = (int64_t)blockIdx.x * kSmallTile;
+    const int64_t K = sc.B * t.T;
+    const Tt* E = (const Tt*)t.E;
+    const Tt* A = (const Tt*)t.A;
+    // the thread's places of a chunk: row idx >> 4, column idx & 15, idx = tid + 256 r
+    float er[kSmallLoads], ar[kSmallLoads], cr[kSmallLoads];
+    auto fetch = [&](int64_t k0, bool with_c) {
+#pragma unroll
+        for (int r = 0; r < kSmallLoads; ++r) {
+            const int idx = tid + 256 * r;
+            const int64_t k = k0 + (idx >> 4);
+            const int col = idx & 15;
+            er[r] = (k < K && m0 + col < t.d_out) ? Elem<DT>::ld(E + k * t.d_out + m0 + col) : 0.f;
+            ar[r] = (k < K && n0 + col < t.d_in) ? Elem<DT>::ld(A + k * t.d_in + n0 + col) : 0.f;
+            if (with_c) cr[r] = k < K ? __ldca(c + k / t.T) : 0.f;
+        }
+    };
+    fetch(0, false);
+    grid_dep_wait();
+    grid_dep_trigger();
+    if (status_bad(status)) return;
+#pragma unroll
+    for (int r = 0; r < kSmallLoads; ++r) {
+        const int64_t k = (tid + 256 * r) >> 4;
+        cr[r] = k < K ? __ldca(c + k / t.T) : 0.f;
+    }
+    float acc = 0.f, bsum = 0.f;
+    const bool do_bias = t.has_bias && blockIdx.x == 0;
+    for (int64_t k0 = 0; k0 < K; k0 += kSmallBK) {
+#pragma unroll
+        for (int r = 0; r < kSmallLoads; ++r) {
+            const int idx = tid + 256 * r;
+            Es[idx >> 4][idx & 15] = cr[r] * er[r];
+            As[idx >> 4][idx & 15] = ar[r];
+        }
+        __syncthreads();
+        if (k0 + kSmallBK < K) fetch(k0 + kSmallBK, true);
+#pragma unroll 16
+        for (int kk = 0; kk < kSmallBK; ++kk) acc = fmaf(Es[kk][tr], As[kk][tc], acc);
+        if (do_bias && tid < kSmallTile) {
+            for (int kk = 0; kk < kSmallBK; ++kk) bsum += Es[kk][tid];
+        }
+        __syncthreads();
+    }
+    const float scale = sc.sigma * sc.C;
+    const int64_t m = m0 + tr, n = n0 + tc;
+    if (m < t.d_out && n < t.d_in) {
+        const float z = noise_at(sc.seed, sc.step, (uint64_t)(t.coord_off + m * t.d_in + n));
+        t.G[m * t.d_in + n] = (acc + scale * z) / sc.L;
+    }
+    if (do_bias && tid < kSmallTile && m0 + tid < t.d_out) {
+        const int64_t p = t.d_out * t.d_in + m0 + tid;
+        const float z = noise_at(sc.seed, sc.step, (uint64_t)(t.coord_off + p));
+        t.G[p] = (bsum + scale * z) / sc.L;
+    }
+}
+
 // --------------------------------------------- bias part of the clipped sum
 // sb[m] = sum_k c[k / T] E[k, m] (ascending k), then G = (sb + sigma C z) / L
 // at the layer's bias coordinates.  Used beside the tensor-core weight sum.
@@ -461,6 +533,16 @@ cudaError_t launch_grad_wsum(const GradTask* tasks, int n, const float* c, const
 cudaError_t launch_grad_gemm_cc(const GradTask& t, const float* c, const unsigned* status,
                                 const StepScalars& sc, cudaStream_t s) {
     const dim3 grid((unsigned)((t.d_in + kBN - 1) / kBN), (unsigned)((t.d_out + kBM - 1) / kBM));
+    if (grid.x * grid.y < 16) {
+        // too few 64 x 64 tiles to spread over the SMs: 16 x 16 tiles
+        const dim3 g16((unsigned)((t.d_in + kSmallTile - 1) / kSmallTile),
+                       (unsigned)((t.d_out + kSmallTile - 1) / kSmallTile));
+        const cudaError_t e =
+            t.dtype == DT_F32 ? launch_dependent(k_grad_gemm_small<DT_F32>, g16, dim3(256), 0, s, t, c, status, sc)
+                              : launch_dependent(k_grad_gemm_small<DT_BF16>, g16, dim3(256), 0, s, t, c, status, sc);
+        count_launches(1);
+        return e;
+    }
     const cudaError_t e = t.dtype == DT_F32
                               ? launch_dependent(k_grad_gemm_cc<DT_F32>, grid, dim3(256), 0, s, t, c, status, sc)
                               : launch_dependent(k_grad_gemm_cc<DT_BF16>, grid, dim3(256), 0, s, t, c, status, sc);
