@@ -53,6 +53,10 @@ def _tile_errors(got, want, d_out, d_in):
     (40, 512, 512, 256),    # 2 pair tiles of 40 records, each cut into 38 ranges (76 pairs)
     (20, 512, 2560, 2048),  # 80 pair tiles: one full wave of 76, then 4 tiles cut into 19 ranges
     (6500, 3, 256, 512),    # one pre-scaled record of 19500 rows: whole tiles
+    (40, 128, 328, 200),    # widths not multiples of 64 (2D tensor maps), ragged in both
+                            # directions: 2 pair tiles, each cut into 10 ranges of 4 records
+    (12, 64, 640, 384),     # 3D maps, partial pair tiles: the second CTA of the last row
+                            # block lies wholly past d_out (zero-filled loads, no stores)
 ])
 def test_split_tiles_match_oracle(B, T, d_in, d_out):
     A, E = _inputs(B, T, d_in, d_out, seed=B * 7 + T)
