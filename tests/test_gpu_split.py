@@ -133,3 +133,34 @@ def test_prescaled_layers_match_oracle_noise_once_and_repeat():
     for r in runs[1:]:
         assert all(torch.equal(a, b) for a, b in zip(runs[0], r))
     pg.close()
+
+
+def test_two_split_layers_in_one_step():
+    """Two per-record layers whose last waves are both split into record
+    ranges (one with 3D, one with 2D tensor maps) in one step: the second
+    launch reuses the context's arrival counters under a new tag, and each
+    layer's G matches the oracle tile by tile with its own noise once."""
+    B, T = 40, 64
+    shapes = [(512, 256), (328, 200)]
+    layers = [(d_in, d_out, False) for d_in, d_out in shapes]
+    A, E = [], []
+    for i, (d_in, d_out) in enumerate(shapes):
+        a, e = _inputs(B, T, d_in, d_out, seed=70 + i)
+        A.append(a)
+        E.append(e)
+    C, sigma, seed, step = 0.6, 1.3, 8, 3
+    out0, _ = gpu_step(layers, A, E, [T, T], C, 0.0, seed, step, layer_norms=False)
+    outs, _ = gpu_step(layers, A, E, [T, T], C, sigma, seed, step, layer_norms=False)
+    ref = oracle_step(layers, A, E, [T, T], C, 0.0, seed, step)
+    off = 0
+    for l, (d_in, d_out) in enumerate(shapes):
+        S, _ = ref.clipped[l]
+        G0 = to64(out0.grads[l]).reshape(d_out, d_in)
+        errs = _tile_errors(G0, S / B, d_out, d_in)
+        assert np.all(errs <= G_RTOL), (l, errs.max(), int(errs.argmax()))
+        Gs = to64(outs.grads[l]).reshape(d_out, d_in)
+        z = philox.normals(seed, step, off, d_out * d_in).reshape(d_out, d_in)
+        tol = 1e-3 * sigma * C / B + 4e-7 * np.abs(G0) + 1e-5 * np.abs(S).max() / B
+        bad = np.abs(Gs - G0 - sigma * C * z / B) > tol
+        assert not bad.any(), (l, int(bad.sum()), np.argwhere(bad)[:4])
+        off += d_out * d_in
