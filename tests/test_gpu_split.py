@@ -164,3 +164,35 @@ def test_two_split_layers_in_one_step():
         bad = np.abs(Gs - G0 - sigma * C * z / B) > tol
         assert not bad.any(), (l, int(bad.sum()), np.argwhere(bad)[:4])
         off += d_out * d_in
+
+
+def test_four_layers_in_one_sum_launch_and_a_fifth_beside():
+    """Five pre-scaled layers of one row count: the clip kernel scales the
+    first four, which are summed in one launch of four layers (the most one
+    launch carries); the fifth is scaled by its own kernel and summed alone.
+    Each G matches the oracle tile by tile at sigma = 0 and carries its own
+    noise once at sigma."""
+    B, T = 200, 3
+    shapes = [(256, 512), (512, 256), (320, 200), (136, 264), (384, 640)]
+    layers = [(d_in, d_out, False) for d_in, d_out in shapes]
+    A, E = [], []
+    for i, (d_in, d_out) in enumerate(shapes):
+        a, e = _inputs(B, T, d_in, d_out, seed=90 + i)
+        A.append(a)
+        E.append(e)
+    C, sigma, seed, step = 0.9, 0.8, 13, 5
+    out0, _ = gpu_step(layers, A, E, [T] * 5, C, 0.0, seed, step, layer_norms=False)
+    outs, _ = gpu_step(layers, A, E, [T] * 5, C, sigma, seed, step, layer_norms=False)
+    ref = oracle_step(layers, A, E, [T] * 5, C, 0.0, seed, step)
+    off = 0
+    for l, (d_in, d_out) in enumerate(shapes):
+        S, _ = ref.clipped[l]
+        G0 = to64(out0.grads[l]).reshape(d_out, d_in)
+        errs = _tile_errors(G0, S / B, d_out, d_in)
+        assert np.all(errs <= G_RTOL), (l, errs.max(), int(errs.argmax()))
+        Gs = to64(outs.grads[l]).reshape(d_out, d_in)
+        z = philox.normals(seed, step, off, d_out * d_in).reshape(d_out, d_in)
+        tol = 1e-3 * sigma * C / B + 4e-7 * np.abs(G0) + 1e-5 * np.abs(S).max() / B
+        bad = np.abs(Gs - G0 - sigma * C * z / B) > tol
+        assert not bad.any(), (l, int(bad.sum()), np.argwhere(bad)[:4])
+        off += d_out * d_in
