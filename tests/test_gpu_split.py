@@ -196,3 +196,26 @@ def test_four_layers_in_one_sum_launch_and_a_fifth_beside():
         bad = np.abs(Gs - G0 - sigma * C * z / B) > tol
         assert not bad.any(), (l, int(bad.sum()), np.argwhere(bad)[:4])
         off += d_out * d_in
+
+
+def test_batch_of_one_record_applies_its_clip_factor():
+    """B = 1 with T a multiple of 64: the sum runs as one record of T rows
+    with the record's own clip factor c_0 applied in the epilogue (no
+    pre-scaled copy); the record is clipped (its norm is far above C)."""
+    B, T, d_in, d_out = 1, 128, 320, 256
+    A, E = _inputs(B, T, d_in, d_out, seed=123)
+    layers = [(d_in, d_out, False)]
+    C, sigma, seed, step = 0.05, 0.5, 2, 9
+    out0, _ = gpu_step(layers, [A], [E], [T], C, 0.0, seed, step, layer_norms=False)
+    ref = oracle_step(layers, [A], [E], [T], C, 0.0, seed, step)
+    assert float(ref.clip[0]) < 0.5
+    S, _ = ref.clipped[0]
+    G0 = to64(out0.grads[0]).reshape(d_out, d_in)
+    errs = _tile_errors(G0, S / B, d_out, d_in)
+    assert np.all(errs <= G_RTOL), (errs.max(), int(errs.argmax()))
+    outs, _ = gpu_step(layers, [A], [E], [T], C, sigma, seed, step, layer_norms=False)
+    Gs = to64(outs.grads[0]).reshape(d_out, d_in)
+    z = philox.normals(seed, step, 0, d_out * d_in).reshape(d_out, d_in)
+    tol = 1e-3 * sigma * C / B + 4e-7 * np.abs(G0) + 1e-5 * np.abs(S).max() / B
+    bad = np.abs(Gs - G0 - sigma * C * z / B) > tol
+    assert not bad.any(), (int(bad.sum()), np.argwhere(bad)[:4])
