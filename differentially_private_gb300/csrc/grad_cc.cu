@@ -333,10 +333,10 @@ __global__ void __launch_bounds__(256) k_grad_gemm_cc(const GradTask t, const fl
 }
 
 // The same sum for outputs too small to occupy the GPU with 64 x 64 tiles:
-// one 16 x 16 tile per block, one output per thread, K in chunks of 64 rows
+// one 16 x 16 tile per block, one output per thread, K in chunks of 128 rows
 // (the first fetched before the dependency wait, as above).  A block whose
 // tile starts the row holds the bias sums of its 16 rows.
-constexpr int kSmallTile = 16, kSmallBK = 64;
+constexpr int kSmallTile = 16, kSmallBK = 128;
 constexpr int kSmallLoads = kSmallBK * kSmallTile / 256;   // elements of each operand a thread stages per chunk
 
 template <int DT>
