@@ -190,6 +190,33 @@ def work_model(w):
     return {"norm_flops": norm_flops, "norm_bytes": norm_bytes, "grad_flops": grad_flops, "grad_bytes": grad_bytes}
 
 
+def dominant_kernel(w, phase: str, bound: str) -> str:
+    """The library kernel that dominates a phase of one step of workload w,
+    given the bound the work model assigns to that phase (the runtime's own
+    kernel choice restated from the layers' dtype and shapes)."""
+    import torch
+    import differentially_private_gb300 as dp
+    ghost_T = [ly.T for ly in w.layers if dp.dp_choose_path(ly.T, ly.d_in, ly.d_out) == dp.DP_PATH_GHOST]
+    if w.torch_dtype == torch.float32:
+        # fp32 layers take the CUDA-core kernels: ghost or materialized norms, and
+        # the reweighted sum (16 x 16 tiles below sixteen 64 x 64 tiles) or the
+        # weighted sum of the stored per-example gradients
+        ly = max(w.layers, key=lambda l: l.d_in * l.d_out)
+        ghost = dp.dp_choose_path(ly.T, ly.d_in, ly.d_out) == dp.DP_PATH_GHOST
+        tiles64 = -(-ly.d_in // 64) * -(-ly.d_out // 64)
+        if phase == "norm":
+            return "k_norm_ghost_cc" if ghost else "k_norm_mat_cc"
+        return "k_grad_wsum" if not ghost else "k_grad_gemm_small" if tiles64 < 16 else "k_grad_gemm_cc"
+    if phase == "norm":
+        return ("k_ghost_gram_tc" if bound == "tensor"
+                else "k_norm_t1_group" if ghost_T and all(t == 1 for t in ghost_T) else "k_mat_skinny_tc")
+    # layers whose T is not a multiple of 64 are summed as one pre-scaled record,
+    # the layers sharing K in one launch of k_sum_layers_pair_tc
+    return ("k_grad_wsum" if bound == "hbm"
+            else "k_sum_layers_pair_tc" if ghost_T and all(t % 64 for t in ghost_T)
+            else "k_clipped_sum_fold_pair_tc")
+
+
 # ------------------------------------------------------------ CPU oracle leg
 def oracle_sample_rate(w, A_host, E_host, budget_s: float):
     """Oracle throughput (examples/s) on a bounded sample of the workload.
@@ -400,27 +427,7 @@ def run_ours(args, w):
         ach = bytes_ / (t_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / peaks["hbm_gbs"]}
-    # the kernel that dominates that phase for this workload's layer shapes
-    ghost_T = [ly.T for ly in w.layers if dp.dp_choose_path(ly.T, ly.d_in, ly.d_out) == dp.DP_PATH_GHOST]
-    if w.torch_dtype == torch.float32:
-        # fp32 layers take the CUDA-core kernels: ghost or materialized norms, and
-        # the reweighted sum (16 x 16 tiles below sixteen 64 x 64 tiles) or the
-        # weighted sum of the stored per-example gradients
-        ly = max(w.layers, key=lambda l: l.d_in * l.d_out)
-        ghost = dp.dp_choose_path(ly.T, ly.d_in, ly.d_out) == dp.DP_PATH_GHOST
-        tiles64 = -(-ly.d_in // 64) * -(-ly.d_out // 64)
-        kernel_name = (("k_norm_ghost_cc" if ghost else "k_norm_mat_cc") if phase == "norm"
-                       else "k_grad_wsum" if not ghost
-                       else "k_grad_gemm_small" if tiles64 < 16 else "k_grad_gemm_cc")
-    elif phase == "norm":
-        kernel_name = ("k_ghost_gram_tc" if roof["bound"] == "tensor"
-                       else "k_norm_t1_group" if ghost_T and all(t == 1 for t in ghost_T) else "k_mat_skinny_tc")
-    else:
-        # layers whose T is not a multiple of 64 are summed as one pre-scaled record,
-        # the layers sharing K in one launch of k_sum_layers_pair_tc
-        kernel_name = ("k_grad_wsum" if roof["bound"] == "hbm"
-                       else "k_sum_layers_pair_tc" if ghost_T and all(t % 64 for t in ghost_T)
-                       else "k_clipped_sum_fold_pair_tc")
+    kernel_name = dominant_kernel(w, phase, roof["bound"])
     roof["traffic"] = kernel_traffic(f"{kernel_name}@{w.name}")
     roof["kernel"] = kernel_name
     roof["phase"] = phase

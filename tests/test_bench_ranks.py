@@ -75,3 +75,29 @@ def test_reference_arm_under_torchrun_prints_once():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_dominant_kernel_names_the_runtime_choice():
+    """The kernel each bench line names for its dominant phase is the one the
+    runtime launches for that workload's dtype and shapes, and a kernel that
+    exists in the CUDA sources."""
+    import glob
+    import re
+
+    from synthetic import by_index
+
+    src = "".join(open(f).read() for f in glob.glob(os.path.join(ROOT, "differentially_private_gb300", "csrc", "*.cu")))
+    defined = set(re.findall(r"__global__\s+void\s+(?:__\w+__\([^)]*\)\s+)*(\w+)\s*\(", src))
+    expected = {
+        1: {("norm", "alu"): "k_norm_ghost_cc", ("grad", "alu"): "k_grad_gemm_small"},
+        2: {("norm", "hbm"): "k_mat_skinny_tc", ("grad", "hbm"): "k_grad_wsum"},
+        3: {("norm", "tensor"): "k_ghost_gram_tc", ("grad", "tensor"): "k_clipped_sum_fold_pair_tc"},
+        4: {("norm", "hbm"): "k_norm_t1_group", ("grad", "tensor"): "k_sum_layers_pair_tc"},
+        5: {("norm", "tensor"): "k_ghost_gram_tc", ("grad", "tensor"): "k_clipped_sum_fold_pair_tc"},
+    }
+    for i, cases in expected.items():
+        w = by_index(i)
+        for (phase, bound), name in cases.items():
+            got = bench.dominant_kernel(w, phase, bound)
+            assert got == name, (i, phase, bound, got)
+            assert got in defined, (got, sorted(defined))
