@@ -1,7 +1,7 @@
 """Throughput of the DP-SGD private-gradient step (norms -> clip -> clipped sum
 -> noise -> /L) on GB300, through the library's C ABI.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 5] [--impl ours|reference]
 
 Prints ONE JSON line (rank 0).  A step is one pass of the whole path over one
 batch of synthetic records already resident in HBM: every
@@ -9,6 +9,10 @@ dp_norm_accumulate (one batched call), dp_clip_factors and
 dp_clipped_noisy_grad.  The metric is clipped+noised examples per second over
 all ranks.  Under torchrun each rank processes its own batch (weak scaling,
 no collective on the data path of the timed step).
+
+The default workload is the largest single-GPU configuration: one
+Llama-3-8B-shaped decoder layer (LoRA rank 16 on q/k/v/o and gate/up, the
+full-weight down_proj), B = 32 records of T = 2048 tokens.
 """
 
 from __future__ import annotations
@@ -37,7 +41,9 @@ def parse():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", type=int, default=2, help="workload index 1..5 (default: 2)")
+    p.add_argument("--workload", type=int, default=5, help="workload index 1..5 (default: 5, the largest)")
+    p.add_argument("--batch", type=int, default=None,
+                   help="override the workload's B (smaller cases for profiler captures)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget-s", type=float, default=12.0)
@@ -218,52 +224,135 @@ def dominant_kernel(w, phase: str, bound: str) -> str:
 
 
 # ------------------------------------------------------------ CPU oracle leg
-def oracle_sample_rate(w, A_host, E_host, budget_s: float):
+def oracle_sample_rate(w, record, n_avail: int, budget_s: float):
     """Oracle throughput (examples/s) on a bounded sample of the workload.
 
     The oracle materializes every per-example gradient in float64.  Its
-    per-record work is timed on the first b records (b grows until the budget
-    is used or the batch is exhausted) and the noise of all P coordinates is
-    timed on a sample of coordinates; the full-batch step time is
-    t_records * B / b + t_noise * P / p."""
+    per-record work (the record's norm over all layers, its clip factor and
+    its clipped gradient added to the running sum S of every layer) is timed
+    on the first b records, b growing until the budget is used or the n_avail
+    records given are exhausted; the noise and the division,
+    G = (S + sigma C z) / L, are timed on a sample of coordinates.  The
+    full-batch step time is t_records * B / b + t_noise * P / p.
+    record(l, i) returns record i of layer l as float64 arrays (A_i, E_i);
+    fetching it is not timed."""
     import numpy as np
     from oracle import dpsgd, philox
 
     layers = [dpsgd.Layer(ly.d_in, ly.d_out, ly.has_bias) for ly in w.layers]
+    t_rec = 0.0
     t0 = time.perf_counter()
+    S = [np.zeros((ly.d_out, ly.d_in)) for ly in layers]
+    Sb = [np.zeros(ly.d_out) if ly.has_bias else None for ly in layers]
+    t_rec += time.perf_counter() - t0
     b = 0
-    while b < w.B and time.perf_counter() - t0 < budget_s * 0.8:
+    while b < min(w.B, n_avail) and (b == 0 or t_rec < budget_s * 0.8):
+        rec = [record(l, b) for l in range(len(layers))]
+        t0 = time.perf_counter()
         n2 = 0.0
-        for ly, A, E in zip(layers, A_host, E_host):
-            n2 += dpsgd.record_sqnorm(A[b], E[b], ly.has_bias)
+        for ly, (A, E) in zip(layers, rec):
+            n2 += dpsgd.record_sqnorm(A, E, ly.has_bias)
         c = dpsgd.clip_factors(np.array([n2]), w.C)[0]
-        for ly, A, E in zip(layers, A_host, E_host):
-            g, bb = dpsgd.per_example_grad(A[b], E[b], ly.has_bias)
-            _ = c * g
+        for l, (ly, (A, E)) in enumerate(zip(layers, rec)):
+            g, bb = dpsgd.per_example_grad(A, E, ly.has_bias)
+            S[l] += c * g
+            if bb is not None:
+                Sb[l] += c * bb
+        t_rec += time.perf_counter() - t0
         b += 1
-    t_rec = time.perf_counter() - t0
     P = w.ncoords
     p = min(P, 1 << 22)
-    t1 = time.perf_counter()
-    philox.normals(w.noise_seed, w.step, 0, p)
-    t_noise = (time.perf_counter() - t1) * P / p
+    t0 = time.perf_counter()
+    z = philox.normals(w.noise_seed, w.step, 0, p)
+    done = 0
+    for l, ly in enumerate(layers):
+        if done >= p:
+            break
+        flat = S[l].reshape(-1) if Sb[l] is None else np.concatenate([S[l].reshape(-1), Sb[l]])
+        m = min(flat.size, p - done)
+        _ = (flat[:m] + w.sigma * w.C * z[done:done + m]) / float(w.B)
+        done += m
+    t_noise = (time.perf_counter() - t0) * P / p
     t_full = t_rec * w.B / b + t_noise
     cores = len(os.sched_getaffinity(0))
-    sample = (f"oracle float64 on {b} of {w.B} records (materialize, clip, scale) timed, scaled to B; "
-              f"noise timed on {p} of {P} coordinates, scaled to P")
+    sample = (f"oracle float64 on {b} of {w.B} records (per-record norm, clip factor, clipped gradient "
+              f"added to the sum of every layer) timed, scaled to B; noise and division timed on {p} of "
+              f"{P} coordinates, scaled to P")
     return w.B / t_full, cores, sample, t_full
 
 
-def host_inputs(w, device="cuda"):
+def device_records(A_dev, E_dev):
+    """record(l, i) over device tensors: record i of layer l copied to the host in float64."""
+    import torch
+
+    def record(l, i):
+        return (A_dev[l][i].to("cpu", torch.float64).numpy(), E_dev[l][i].to("cpu", torch.float64).numpy())
+    return record
+
+
+def host_records(w, max_bytes: int = 2 << 30):
+    """record(l, i) over inputs drawn on the CPU with the workload's recipe,
+    keeping at most about max_bytes of them (the first records of a batch of
+    that size: per-record work does not depend on B); returns (record, n)."""
     import torch
     from synthetic import generate_layer
+    n = w.B if w.input_bytes <= max_bytes else max(2, int(w.B * max_bytes / w.input_bytes))
+    ws = w.scaled(B=n)
     A_host, E_host = [], []
     for i in range(len(w.layers)):
-        a, e = generate_layer(w, i, device)
-        A_host.append(a.to("cpu", torch.float64).numpy())
-        E_host.append(e.to("cpu", torch.float64).numpy())
-        del a, e
-    return A_host, E_host
+        a, e = generate_layer(ws, i, "cpu")
+        A_host.append(a)
+        E_host.append(e)
+
+    def record(l, i):
+        return A_host[l][i].to(torch.float64).numpy(), E_host[l][i].to(torch.float64).numpy()
+    return record, n
+
+
+def config_dict(w, world: int) -> dict:
+    """The workload's description, the same in both arms."""
+    return {"workload": w.name, "B": w.B, "layers": len(w.layers), "T": sorted({ly.T for ly in w.layers}),
+            "C": w.C, "sigma": w.sigma,
+            "l2": (f"flushed before every timed step: {L2_FLUSH_BYTES >> 20} MB written, "
+                   f"then {L2_FLUSH_BYTES >> 20} MB read"),
+            "parallelism": f"replicas x{world}"}
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def manifest(w, dp, device, kernels_per_step: dict) -> dict:
+    """Release record of the run: hardware and software, the step's public
+    parameters, the chooser's decision per layer and the kernels launched."""
+    import torch
+    props = torch.cuda.get_device_properties(device)
+    try:
+        drv = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader",
+                              "-i", str(device.index or 0)], capture_output=True, text=True, timeout=20).stdout.strip()
+    except (OSError, subprocess.SubprocessError):
+        drv = None
+    lib_sha = hashlib.sha256(open(dp.LIB_PATH, "rb").read()).hexdigest()[:16]
+    return {
+        "gpu": props.name, "compute_capability": f"{props.major}.{props.minor}", "sms": props.multi_processor_count,
+        "driver": drv, "cuda": torch.version.cuda, "torch": torch.__version__,
+        "library_version": dp.dp_version(), "library_sha256_16": lib_sha,
+        "B": w.B, "T": [ly.T for ly in w.layers], "C": w.C, "sigma": w.sigma, "seed": w.noise_seed,
+        "step": w.step, "L": float(w.B), "dtype": w.dtype,
+        "chooser": [[ly.name, ly.d_in, ly.d_out, ly.T,
+                     "ghost" if dp.dp_choose_path(ly.T, ly.d_in, ly.d_out) == dp.DP_PATH_GHOST else "materialize"]
+                    for ly in w.layers],
+        "kernels_per_step": kernels_per_step,
+        "host": {"cores": len(os.sched_getaffinity(0)), "cpu_model": cpu_model()},
+    }
 
 
 # ------------------------------------------------------------------- arms
@@ -271,15 +360,14 @@ def run_reference(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    import torch  # noqa: F401
-    A_host, E_host = host_inputs(w, "cpu")
+    record, n_avail = host_records(w)
     per = max(2.0, args.cpu_budget_s / max(1, args.steps + args.warmup) * 4)
     for _ in range(args.warmup):
-        oracle_sample_rate(w, A_host, E_host, min(per, 2.0))
+        oracle_sample_rate(w, record, n_avail, min(per, 2.0))
     times = []
     rate, cores, sample = None, None, None
     for _ in range(args.steps):
-        rate, cores, sample, t_full = oracle_sample_rate(w, A_host, E_host, per)
+        rate, cores, sample, t_full = oracle_sample_rate(w, record, n_avail, per)
         times.append(t_full)
     t_step = statistics.mean(times)
     value = w.B / t_step
@@ -287,8 +375,9 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "layers": len(w.layers)},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "config": config_dict(w, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample + f"; inputs drawn on the host ({n_avail} records)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -354,8 +443,8 @@ def run_ours(args, w):
     # same four C calls (begin, batched norms, clip factors, clipped noisy sum)
     prep = pg.prepare(A_dev, E_dev, T_list, outputs=(grads, clip, sq))
 
-    def step(evs=None):
-        prep.run(w.C, w.sigma, w.noise_seed, w.step, events=evs)
+    def step(evs=None, after_phase=None):
+        prep.run(w.C, w.sigma, w.noise_seed, w.step, events=evs, after_phase=after_phase)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -379,6 +468,7 @@ def run_ours(args, w):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     n_launch0 = dp.dp_kernel_launches()
+    per_kernel0 = dp.dp_kernel_launch_counts()
     for k in range(K):
         flush_l2()
         evs[k][0].record(stream)
@@ -386,6 +476,8 @@ def run_ours(args, w):
         evs[k][1].record(stream)
     torch.cuda.synchronize()
     n_launch = dp.dp_kernel_launches() - n_launch0
+    per_kernel = {name: (cnt - per_kernel0[name]) / K for name, cnt in dp.dp_kernel_launch_counts().items()
+                  if cnt != per_kernel0[name]}
     if world > 1:
         torch.distributed.barrier()
     for k in range(K):
@@ -393,6 +485,27 @@ def run_ours(args, w):
         step(pevs[k])
     torch.cuda.synchronize()
     clk = clocks.stop(since)
+    # SM clock at the end of each phase, from the device: a spin of a fixed
+    # number of SM cycles right after the phase, timed with events on the
+    # stream (a third pass of K steps; not part of the timed region)
+    probe_cycles = 200_000
+    probes = {"norm": [], "clip": [], "grad": []}
+
+    def probe(phase):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        torch.cuda._sleep(probe_cycles)
+        e1.record(stream)
+        probes[phase].append((e0, e1))
+
+    for k in range(K):
+        flush_l2()
+        step(after_phase=probe)
+    torch.cuda.synchronize()
+    phase_mhz = {ph: statistics.median([probe_cycles / (a.elapsed_time(b_) * 1e3) for a, b_ in v])
+                 for ph, v in probes.items() if v}
+    if clk is not None:
+        clk["sm_mhz_after_phase"] = phase_mhz
     st = dp.dp_step_status(ctx)
     if st != dp.DP_OK:
         raise dp.DPError(st, "dp_step_status", dp.dp_last_error(ctx))
@@ -438,8 +551,9 @@ def run_ours(args, w):
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        arena_pin = arena.cpu().pin_memory()
-        garena_pin = torch.empty(garena.numel(), dtype=torch.float32).pin_memory()
+        arena_pin = torch.empty(arena.numel(), dtype=torch.uint8, pin_memory=True)
+        arena_pin.copy_(arena)
+        garena_pin = torch.empty(garena.numel(), dtype=torch.float32, pin_memory=True)
         h2d = arena.numel()
         d2h = garena.numel() * 4
 
@@ -465,9 +579,7 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        A_host = [a.to("cpu", torch.float64).numpy() for a in A_dev]
-        E_host = [e.to("cpu", torch.float64).numpy() for e in E_dev]
-        rate, cores, sample, _ = oracle_sample_rate(w, A_host, E_host, args.cpu_budget_s)
+        rate, cores, sample, _ = oracle_sample_rate(w, device_records(A_dev, E_dev), w.B, args.cpu_budget_s)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
 
     if rank == 0:
@@ -475,11 +587,7 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "layers": len(w.layers),
-                       "T": sorted({ly.T for ly in w.layers}), "C": w.C, "sigma": w.sigma,
-                       "l2": (f"flushed before every timed step: {L2_FLUSH_BYTES >> 20} MB written, "
-                              f"then {L2_FLUSH_BYTES >> 20} MB read"),
-                       "parallelism": f"replicas x{world}"},
+            "config": config_dict(w, world),
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -487,6 +595,7 @@ def run_ours(args, w):
             "clocks": clk,
             "phases_ms": {"norm": mn, "clip": statistics.mean(clip_ms), "grad": mg,
                           "step_with_phase_events": statistics.mean([e[0].elapsed_time(e[3]) for e in pevs])},
+            "manifest": manifest(w, dp, device, per_kernel),
         }
         print(json.dumps(line), flush=True)
     pg.close()
@@ -499,6 +608,8 @@ def main():
     args = parse()
     from synthetic import by_index
     w = by_index(args.workload)
+    if args.batch is not None:
+        w = w.scaled(B=int(args.batch))
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

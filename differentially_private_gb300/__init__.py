@@ -31,22 +31,26 @@ from ._binding import (  # noqa: F401
     dp_choose_path,
     dp_clip_factors,
     dp_clipped_noisy_grad,
+    dp_clipped_sum,
     dp_create,
     dp_destroy,
     dp_int8_forward,
     dp_int8_quantize_weight,
     dp_int8_workspace_bytes,
+    dp_kernel_launch_counts,
     dp_kernel_launches,
     dp_last_error,
     dp_layer_info,
     dp_layer_sqnorms_static,
     dp_norm_accumulate,
+    dp_noise_shard,
     dp_norm_accumulate_batch,
     dp_num_coords,
     dp_pack_groups,
     dp_philox_normals,
     dp_register_layer,
     dp_set_normalizer,
+    dp_static_check_wait_timeout,
     dp_status_string,
     dp_step_status,
     dp_version,

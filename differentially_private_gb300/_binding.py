@@ -37,6 +37,7 @@ EXPORTS = (
     "dp_norm_accumulate", "dp_norm_accumulate_batch", "dp_clip_factors", "dp_clipped_noisy_grad",
     "dp_step_status", "dp_last_error", "dp_philox_normals", "dp_layer_sqnorms_static", "dp_pack_groups",
     "dp_int8_quantize_weight", "dp_int8_workspace_bytes", "dp_int8_forward", "dp_check_wait_timeout", "dp_box_muller",
+    "dp_kernel_launch_counts", "dp_clipped_sum", "dp_noise_shard", "dp_static_check_wait_timeout",
 )
 
 
@@ -69,6 +70,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     sig = {
         "dp_version": (i32, []),
         "dp_kernel_launches": (i64, []),
+        "dp_kernel_launch_counts": (i32, [c.POINTER(c.c_char_p), c.POINTER(i64), i32]),
+        "dp_clipped_sum": (i32, [vp, c.POINTER(vp)]),
+        "dp_noise_shard": (i32, [vp, vp, u64, i64, c.c_float, c.c_float, c.c_double, u64, u64, vp]),
+        "dp_static_check_wait_timeout": (i32, [c.c_uint32, vp]),
         "dp_status_string": (c.c_char_p, [i32]),
         "dp_create": (i32, [c.POINTER(vp), i32, vp]),
         "dp_destroy": (i32, [vp]),
@@ -138,6 +143,16 @@ def dp_version() -> int:
 
 def dp_kernel_launches() -> int:
     return load_library().dp_kernel_launches()
+
+
+def dp_kernel_launch_counts() -> dict:
+    """{kernel name: launches so far in this process} for every kernel of the library."""
+    lib = load_library()
+    k = lib.dp_kernel_launch_counts(None, None, 0)
+    names = (ctypes.c_char_p * k)()
+    counts = (ctypes.c_int64 * k)()
+    lib.dp_kernel_launch_counts(names, counts, k)
+    return {names[i].decode(): int(counts[i]) for i in range(k)}
 
 
 def dp_status_string(status: int) -> str:
@@ -210,6 +225,21 @@ def dp_clipped_noisy_grad(ctx, sigma: float, seed: int, step: int, G_list) -> No
                                                 int(step) & (2 ** 64 - 1), g), "dp_clipped_noisy_grad", ctx)
 
 
+def dp_clipped_sum(ctx, S_list) -> None:
+    """The clipped sum without noise or normalizer (one rank's partial sum); closes the step."""
+    n = len(S_list)
+    g = (ctypes.c_void_p * n)(*[_ptr(x) for x in S_list])
+    _check(load_library().dp_clipped_sum(ctx, g), "dp_clipped_sum", ctx)
+
+
+def dp_noise_shard(S, G, k0: int, n: int, sigma: float, C: float, L: float, seed: int, step: int,
+                   stream=None) -> None:
+    """G[j] = (S[j] + sigma C z_{k0+j}) / L over a contiguous range of global coordinates."""
+    _check(load_library().dp_noise_shard(_ptr(S), _ptr(G), int(k0), int(n), float(sigma), float(C), float(L),
+                                         int(seed) & (2 ** 64 - 1), int(step) & (2 ** 64 - 1), _stream(stream)),
+           "dp_noise_shard")
+
+
 def dp_step_status(ctx) -> int:
     """Synchronize and return the step's deferred status code (does not raise)."""
     return load_library().dp_step_status(ctx)
@@ -241,6 +271,12 @@ def dp_layer_sqnorms_static(A, E, B: int, T: int, d_in: int, d_out: int, has_bia
     _check(load_library().dp_layer_sqnorms_static(_ptr(A), _ptr(E), int(B), int(T), int(d_in), int(d_out),
                                                   int(bool(has_bias)), int(dtype), _ptr(sqnorm_out),
                                                   _stream(stream)), "dp_layer_sqnorms_static")
+
+
+def dp_static_check_wait_timeout(limit_ms: int, stream=None) -> None:
+    """Record a bounded wait that gave up for the next dp_layer_sqnorms_static call (test hook)."""
+    _check(load_library().dp_static_check_wait_timeout(int(limit_ms), _stream(stream)),
+           "dp_static_check_wait_timeout")
 
 
 def dp_pack_groups(src, dst, B: int, T: int, d: int, dtype: int, group_starts, U: int, kmax: int,

@@ -452,6 +452,41 @@ __global__ void __launch_bounds__(256) k_prescale_rows(const uint4* __restrict__
     }
 }
 
+// ------------------------------------------- noise on a coordinate range
+// G[j] = (S[j] + scale z_{k0 + j}) / L for 0 <= j < n: the noise and the
+// normalizer applied to a contiguous range of global coordinates (one rank's
+// shard of the summed clipped gradient when the records are split over
+// ranks).  One thread per noise block (4 coordinates) of the range; vector
+// loads and stores when k0 % 4 == 0 and both arrays are 16-byte aligned.
+template <bool VEC>
+__global__ void __launch_bounds__(256) k_noise_shard(const float* __restrict__ S, float* __restrict__ G, uint64_t k0,
+                                                     int64_t n, float scale, float L, uint64_t seed, uint64_t step) {
+    const uint64_t jb = k0 >> 2;
+    const int64_t nblocks = (int64_t)((k0 + (uint64_t)n - 1) >> 2) - (int64_t)jb + 1;
+    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblocks;
+         b += (int64_t)gridDim.x * blockDim.x) {
+        const uint64_t j = jb + (uint64_t)b;
+        const float4 z = noise4(seed, step, j);
+        const float zz[4] = {z.x, z.y, z.z, z.w};
+        const int64_t p0 = (int64_t)(4 * j - k0);   // index in S of the block's first coordinate
+        if (VEC && p0 + 3 < n) {
+            const float4 v = __ldcs(reinterpret_cast<const float4*>(S + p0));
+            float4 o;
+            o.x = (v.x + scale * zz[0]) / L;
+            o.y = (v.y + scale * zz[1]) / L;
+            o.z = (v.z + scale * zz[2]) / L;
+            o.w = (v.w + scale * zz[3]) / L;
+            __stcs(reinterpret_cast<float4*>(G + p0), o);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int64_t p = p0 + q;
+                if (p >= 0 && p < n) G[p] = (S[p] + scale * zz[q]) / L;
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------- noise test hook
 // The Box-Muller map of the noise on given word pairs (words[2i], words[2i+1])
 // -> (z[2i], z[2i+1]): the same device function as every noise draw.
@@ -503,7 +538,7 @@ cudaError_t launch_clip(const ClipParams& p, float* n2, float* c, float* n2_user
     } else {
         e = launch_dependent(k_clip<false>, dim3((unsigned)p.B), dim3(G), 0, s, p, n2, c, n2_user, c_user, status);
     }
-    count_launches(1);
+    count_launch(KL_CLIP);
     return e;
 }
 
@@ -524,7 +559,7 @@ cudaError_t launch_grad_wsum(const GradTask* tasks, int n, const float* c, const
         if (gx > 4096) gx = 4096;
         const cudaError_t e = launch_dependent(k_grad_wsum, dim3((unsigned)gx, (unsigned)P.n), dim3(256), 0, s, P, c,
                                                status, sc);
-        count_launches(1);
+        count_launch(KL_GRAD_WSUM);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -540,13 +575,13 @@ cudaError_t launch_grad_gemm_cc(const GradTask& t, const float* c, const unsigne
         const cudaError_t e =
             t.dtype == DT_F32 ? launch_dependent(k_grad_gemm_small<DT_F32>, g16, dim3(256), 0, s, t, c, status, sc)
                               : launch_dependent(k_grad_gemm_small<DT_BF16>, g16, dim3(256), 0, s, t, c, status, sc);
-        count_launches(1);
+        count_launch(KL_GRAD_GEMM_SMALL);
         return e;
     }
     const cudaError_t e = t.dtype == DT_F32
                               ? launch_dependent(k_grad_gemm_cc<DT_F32>, grid, dim3(256), 0, s, t, c, status, sc)
                               : launch_dependent(k_grad_gemm_cc<DT_BF16>, grid, dim3(256), 0, s, t, c, status, sc);
-    count_launches(1);
+    count_launch(KL_GRAD_GEMM_CC);
     return e;
 }
 
@@ -556,7 +591,7 @@ cudaError_t launch_bias_sum(const GradTask& t, const float* c, const unsigned* s
     const cudaError_t e = t.dtype == DT_F32
                               ? launch_dependent(k_bias_sum<DT_F32>, dim3(grid), dim3(256), 0, s, t, c, status, sc)
                               : launch_dependent(k_bias_sum<DT_BF16>, dim3(grid), dim3(256), 0, s, t, c, status, sc);
-    count_launches(1);
+    count_launch(KL_BIAS_SUM);
     return e;
 }
 
@@ -567,7 +602,7 @@ cudaError_t launch_prescale_rows(const void* E, void* E2, const float* c, int64_
     if (grid > 152 * 16) grid = 152 * 16;
     const cudaError_t e = launch_dependent(k_prescale_rows, dim3((unsigned)grid), dim3(256), 0, s,
                                            (const uint4*)E, (uint4*)E2, c, K, T, d / 8);
-    count_launches(1);
+    count_launch(KL_PRESCALE_ROWS);
     return e;
 }
 
@@ -577,7 +612,7 @@ cudaError_t launch_box_muller(const uint32_t* words, int64_t npairs, float* z, c
     if (grid > 152 * 64) grid = 152 * 64;
     k_box_muller<<<(unsigned)grid, 256, 0, s>>>(reinterpret_cast<const uint2*>(words), npairs,
                                                 reinterpret_cast<float2*>(z));
-    count_launches(1);
+    count_launch(KL_BOX_MULLER);
     return cudaGetLastError();
 }
 
@@ -588,6 +623,21 @@ cudaError_t launch_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int
     int64_t grid = (nblocks + 255) / 256;
     if (grid > 152 * 64) grid = 152 * 64;
     k_philox_normals<<<(unsigned)grid, 256, 0, s>>>(seed, step, k0, n, raw, z);
-    count_launches(1);
+    count_launch(KL_PHILOX_NORMALS);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_noise_shard(const float* S, float* G, uint64_t k0, int64_t n, float scale, float L,
+                               uint64_t seed, uint64_t step, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const int64_t nblocks = (int64_t)((k0 + (uint64_t)n - 1) >> 2) - (int64_t)(k0 >> 2) + 1;
+    int64_t grid = (nblocks + 255) / 256;
+    const int64_t cap = (int64_t)device_sm_count() * 8;   // 8 resident blocks of 256 threads per SM
+    if (grid > cap) grid = cap;
+    const bool vec = (k0 & 3u) == 0 && (reinterpret_cast<uintptr_t>(S) & 15u) == 0 &&
+                     (reinterpret_cast<uintptr_t>(G) & 15u) == 0;
+    if (vec) k_noise_shard<true><<<(unsigned)grid, 256, 0, s>>>(S, G, k0, n, scale, L, seed, step);
+    else k_noise_shard<false><<<(unsigned)grid, 256, 0, s>>>(S, G, k0, n, scale, L, seed, step);
+    count_launch(KL_NOISE_SHARD);
     return cudaGetLastError();
 }

@@ -44,6 +44,7 @@ __global__ void k_pack_groups_bytes(const uint8_t* __restrict__ src, uint8_t* __
 
 extern "C" dp_status dp_pack_groups(const void* src, void* dst, int64_t B, int64_t T, int64_t d, int dtype,
                                     const int64_t* group_starts, int64_t U, int64_t kmax, void* stream) {
+    NvtxRange nvtx_range("dp_pack_groups");
     if (!src || !dst || !group_starts) return DP_ERR_INVALID_ARG;
     if (dtype != DP_F32 && dtype != DP_BF16) return DP_ERR_INVALID_ARG;
     if (B < 0 || T < 1 || d < 1 || U < 0 || kmax < 0) return DP_ERR_SHAPE;
@@ -64,6 +65,6 @@ extern "C" dp_status dp_pack_groups(const void* src, void* dst, int64_t B, int64
         k_pack_groups_bytes<<<(unsigned)grid, 256, 0, s>>>(static_cast<const uint8_t*>(src),
                                                          static_cast<uint8_t*>(dst), B, rec_bytes, group_starts,
                                                          U, kmax);
-    count_launches(1);
+    count_launch(KL_PACK_GROUPS);
     return cudaGetLastError() == cudaSuccess ? DP_OK : DP_ERR_CUDA;
 }

@@ -188,18 +188,20 @@ extern "C" int64_t dp_int8_workspace_bytes(int64_t n, int64_t K, int64_t rows_pe
 
 extern "C" dp_status dp_int8_quantize_weight(const void* W, int64_t N, int64_t K, int8_t* Wq, float* sW, void* What,
                                              void* stream) {
+    NvtxRange nvtx_range("dp_int8_quantize_weight");
     if (!W || !Wq || !sW || !What) return DP_ERR_INVALID_ARG;
     if (N < 1 || K < 1) return DP_ERR_SHAPE;
     const int64_t blocks = (N + 7) / 8;
     k_int8_quantize_weight<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const __half*>(W), N, K, Wq, sW, static_cast<__half*>(What));
-    count_launches(1);
+    count_launch(KL_INT8_QUANTIZE_WEIGHT);
     return cudaGetLastError() == cudaSuccess ? DP_OK : DP_ERR_CUDA;
 }
 
 extern "C" dp_status dp_int8_forward(const void* A, int64_t n, int64_t K, int64_t rows_per_record, const int8_t* Wq,
                                      const float* sW, const void* What, int64_t N, float tau, int record_owned,
                                      void* Y, void* workspace, void* stream) {
+    NvtxRange nvtx_range("dp_int8_forward");
     if (!A || !Wq || !sW || !What || !Y || !workspace) return DP_ERR_INVALID_ARG;
     if (n < 1 || K < 1 || N < 1 || rows_per_record < 1 || n % rows_per_record) return DP_ERR_SHAPE;
     if (!(tau > 0.f)) return DP_ERR_INVALID_ARG;
@@ -231,6 +233,8 @@ extern "C" dp_status dp_int8_forward(const void* A, int64_t n, int64_t K, int64_
     p.s = scales;
     p.Y = static_cast<__half*>(Y);
     k_int8_gemm<<<dim3((unsigned)((N + kTN - 1) / kTN), (unsigned)((n + kTM - 1) / kTM)), 256, 0, s>>>(p);
-    count_launches(3);
+    count_launch(KL_INT8_SETS);
+    count_launch(KL_INT8_SCALES);
+    count_launch(KL_INT8_GEMM);
     return cudaGetLastError() == cudaSuccess ? DP_OK : DP_ERR_CUDA;
 }

@@ -110,8 +110,25 @@ EncodeTiledFn tensor_map_encoder();
 // device (once per device and kernel; safe from several host threads).
 cudaError_t ensure_smem_limit(const void* kernel, int bytes);
 
-// ---- every kernel launch of the library is counted here (dp_kernel_launches)
-void count_launches(int n);
+// ---- every kernel launch of the library is counted here, per kernel
+// (dp_kernel_launches, dp_kernel_launch_counts)
+enum KernelId {
+    KL_NORM_T1, KL_NORM_T1_GROUP, KL_NORM_GHOST_CC, KL_NORM_MAT_CC, KL_LAYER_SQNORM, KL_LAYER_SQNORM_STATUS,
+    KL_GHOST_GRAM_TC, KL_MAT_SKINNY_TC, KL_CLIP, KL_GRAD_WSUM, KL_GRAD_GEMM_SMALL, KL_GRAD_GEMM_CC, KL_BIAS_SUM,
+    KL_PRESCALE_ROWS, KL_CLIPPED_SUM_FOLD_PAIR_TC, KL_CLIPPED_SUM_TC, KL_SUM_LAYERS_PAIR_TC, KL_NOISE_SHARD,
+    KL_BOX_MULLER, KL_PHILOX_NORMALS, KL_PACK_GROUPS, KL_INT8_QUANTIZE_WEIGHT, KL_INT8_SETS, KL_INT8_SCALES,
+    KL_INT8_GEMM, KL_WAIT_EXPIRES, KL_COUNT
+};
+void count_launch(KernelId k);
+
+// ---- NVTX range over the body of a public entry point (header-only NVTX 3:
+// a no-op unless a profiler is attached)
+struct NvtxRange {
+    explicit NvtxRange(const char* name);
+    ~NvtxRange();
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // ---- slot counts (depend on the shapes only, never on B)
 int nslots_for(int kernel, int64_t T, int64_t d_in, int64_t d_out);
@@ -127,12 +144,18 @@ cudaError_t launch_norm_t1_group(const NormTask* tasks, int n, int64_t B, cudaSt
 cudaError_t launch_norm_ghost_cc(const NormTask& t, int64_t B, cudaStream_t s);
 cudaError_t launch_norm_mat_cc(const NormTask& t, int64_t B, cudaStream_t s);
 cudaError_t launch_layer_sqnorm(const float* partial, int nslots, int64_t B, float* out, cudaStream_t s);
+// the same, but every output is NaN when *status is not zero (read after the producers ran)
+cudaError_t launch_layer_sqnorm_checked(const float* partial, int nslots, int64_t B, float* out,
+                                        const unsigned* status, cudaStream_t s);
 cudaError_t launch_clip(const ClipParams& p, float* n2, float* c, float* n2_user, float* c_user,
                         unsigned* status, cudaStream_t s);
 cudaError_t launch_grad_wsum(const GradTask* tasks, int n, const float* c, const unsigned* status,
                              const StepScalars& sc, cudaStream_t s);
 cudaError_t launch_grad_gemm_cc(const GradTask& t, const float* c, const unsigned* status,
                                 const StepScalars& sc, cudaStream_t s);
+// G[j] = (S[j] + scale z_{k0+j}) / L over a contiguous range of global coordinates
+cudaError_t launch_noise_shard(const float* S, float* G, uint64_t k0, int64_t n, float scale, float L,
+                               uint64_t seed, uint64_t step, cudaStream_t s);
 cudaError_t launch_box_muller(const uint32_t* words, int64_t npairs, float* z, cudaStream_t s);
 cudaError_t launch_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int64_t n,
                                   uint32_t* raw, float* z, cudaStream_t s);

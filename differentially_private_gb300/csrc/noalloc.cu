@@ -28,6 +28,7 @@ static __device__ __align__(256) unsigned g_static_status[64];
 struct DeviceScratch {
     float* partials = nullptr;
     unsigned* status = nullptr;
+    CUcontext ctx = nullptr;   // the context the addresses belong to
     bool ready = false;
 };
 
@@ -35,14 +36,40 @@ constexpr int kMaxDevices = 128;
 DeviceScratch g_scratch[kMaxDevices];
 std::mutex g_scratch_mu;
 
+// cuCtxGetCurrent, fetched once through the runtime (the library does not
+// link libcuda directly).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+    static const CtxGetCurrentFn fn = [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (CtxGetCurrentFn) nullptr;
+        return reinterpret_cast<CtxGetCurrentFn>(ptr);
+    }();
+    return fn;
+}
+
 // Host code may not use the arrays' names as device addresses: resolve them
-// for the current device once, checking the return codes.
+// for the current device, checking the return codes.  The addresses are
+// kept per device and resolved again when the device's current context is
+// not the one they were resolved in (after a cudaDeviceReset the module is
+// loaded anew and the old addresses are stale).
 dp_status scratch_for_current_device(DeviceScratch* out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DP_ERR_CUDA;
+    const CtxGetCurrentFn get = ctx_get_current();
+    if (!get) return DP_ERR_CUDA;
+    // no context may be current yet on this thread: the runtime binds the
+    // device's primary context when the addresses are first resolved
+    CUcontext cur = nullptr;
+    if (get(&cur) != CUDA_SUCCESS) return DP_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
     DeviceScratch& s = g_scratch[dev];
-    if (!s.ready) {
+    if (!s.ready || !cur || s.ctx != cur) {
+        s.ready = false;
         void* p = nullptr;
         void* q = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_partials) != cudaSuccess) {
@@ -53,8 +80,10 @@ dp_status scratch_for_current_device(DeviceScratch* out) {
             cudaGetLastError();
             return DP_ERR_CUDA;
         }
+        if (get(&cur) != CUDA_SUCCESS || !cur) return DP_ERR_CUDA;
         s.partials = static_cast<float*>(p);
         s.status = static_cast<unsigned*>(q);
+        s.ctx = cur;
         s.ready = true;
     }
     *out = s;
@@ -68,6 +97,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 extern "C" dp_status dp_layer_sqnorms_static(const void* A, const void* E, int64_t B, int64_t T, int64_t d_in,
                                              int64_t d_out, int has_bias, dp_dtype dtype, float* sqnorm_out,
                                              void* stream) {
+    NvtxRange nvtx_range("dp_layer_sqnorms_static");
     if (!A || !E || !sqnorm_out) return DP_ERR_INVALID_ARG;
     if (!aligned(A, 16) || !aligned(E, 16) || !aligned(sqnorm_out, 4)) return DP_ERR_INVALID_ARG;
     if (dtype != DP_F32 && dtype != DP_BF16) return DP_ERR_INVALID_ARG;
@@ -86,8 +116,8 @@ extern "C" dp_status dp_layer_sqnorms_static(const void* A, const void* E, int64
     const dp_status st = scratch_for_current_device(&sc);
     if (st != DP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the partial slots are all overwritten; only the status word starts at zero
-    if (cudaMemsetAsync(sc.status, 0, sizeof(unsigned), s) != cudaSuccess) return DP_ERR_CUDA;
+    // The partial slots are all overwritten.  The status word is zero here:
+    // it starts at zero and every call clears it after reading it.
 
     NormTask t;
     t.A = A;
@@ -120,6 +150,21 @@ extern "C" dp_status dp_layer_sqnorms_static(const void* A, const void* E, int64
         default: return DP_ERR_UNSUPPORTED;
     }
     if (e != cudaSuccess) return DP_ERR_CUDA;
-    if (launch_layer_sqnorm(sc.partials, nslots, B, sqnorm_out, s) != cudaSuccess) return DP_ERR_CUDA;
+    // a wait of the tensor-core kernels that gave up left their partials
+    // unwritten: the totals are then NaN, so the caller sees a non-finite norm
+    if (launch_layer_sqnorm_checked(sc.partials, nslots, B, sqnorm_out, sc.status, s) != cudaSuccess)
+        return DP_ERR_CUDA;
+    if (cudaMemsetAsync(sc.status, 0, sizeof(unsigned), s) != cudaSuccess) return DP_ERR_CUDA;
     return DP_OK;
+}
+
+extern "C" dp_status dp_static_check_wait_timeout(uint32_t limit_ms, void* stream) {
+    NvtxRange nvtx_range("dp_static_check_wait_timeout");
+    if (limit_ms < 1 || limit_ms > 2000) return DP_ERR_INVALID_ARG;
+    DeviceScratch sc;
+    const dp_status st = scratch_for_current_device(&sc);
+    if (st != DP_OK) return st;
+    const cudaError_t e =
+        launch_wait_expiry(sc.status, (uint64_t)limit_ms * 1000000ull, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DP_OK : DP_ERR_CUDA;
 }

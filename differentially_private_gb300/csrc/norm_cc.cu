@@ -236,6 +236,19 @@ __global__ void k_layer_sqnorm(const float* __restrict__ partial, int nslots, in
     if (lane == 0) out[rec] = s;
 }
 
+// The same, for partials whose producers report a wait that gave up in
+// *status: every total is NaN when the word is not zero.
+__global__ void k_layer_sqnorm_status(const float* __restrict__ partial, int nslots, int64_t B,
+                                      float* __restrict__ out, const unsigned* __restrict__ status) {
+    const int64_t rec = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (rec >= B) return;
+    float s = 0.f;
+    for (int j = lane; j < nslots; j += 32) s += partial[rec * nslots + j];
+    s = warp_sum(s);
+    if (lane == 0) out[rec] = status_bad(status) ? __int_as_float(0x7fc00000) : s;
+}
+
 inline int ntri(int64_t T) {
     const int64_t nt = (T + kGT - 1) / kGT;
     return (int)(nt * (nt + 1) / 2);
@@ -264,7 +277,7 @@ cudaError_t launch_norm_t1(const NormTask& t, int64_t B, cudaStream_t s) {
         if (vec) k_norm_t1<DT_BF16, true><<<(unsigned)blocks, threads, 0, s>>>(t.A, t.E, B, t.d_in, t.d_out, t.has_bias, t.partial);
         else k_norm_t1<DT_BF16, false><<<(unsigned)blocks, threads, 0, s>>>(t.A, t.E, B, t.d_in, t.d_out, t.has_bias, t.partial);
     }
-    count_launches(1);
+    count_launch(KL_NORM_T1);
     return cudaGetLastError();
 }
 
@@ -286,7 +299,7 @@ cudaError_t launch_norm_t1_group(const NormTask* tasks, int n, int64_t B, cudaSt
         }
         const dim3 grid((unsigned)((B * 32 + 255) / 256), (unsigned)g.n);
         const cudaError_t e = launch_dependent(k_norm_t1_group, grid, dim3(256), 0, s, g);
-        count_launches(1);
+        count_launch(KL_NORM_T1_GROUP);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -298,7 +311,7 @@ cudaError_t launch_norm_ghost_cc(const NormTask& t, int64_t B, cudaStream_t s) {
         k_norm_ghost_cc<DT_F32><<<grid, 256, 0, s>>>(t.A, t.E, t.T, t.d_in, t.d_out, t.has_bias, t.partial, t.nslots);
     else
         k_norm_ghost_cc<DT_BF16><<<grid, 256, 0, s>>>(t.A, t.E, t.T, t.d_in, t.d_out, t.has_bias, t.partial, t.nslots);
-    count_launches(1);
+    count_launch(KL_NORM_GHOST_CC);
     return cudaGetLastError();
 }
 
@@ -308,7 +321,7 @@ cudaError_t launch_norm_mat_cc(const NormTask& t, int64_t B, cudaStream_t s) {
         k_norm_mat_cc<DT_F32><<<grid, 256, 0, s>>>(t.A, t.E, t.T, t.d_in, t.d_out, t.has_bias, t.partial, t.nslots, t.gstore);
     else
         k_norm_mat_cc<DT_BF16><<<grid, 256, 0, s>>>(t.A, t.E, t.T, t.d_in, t.d_out, t.has_bias, t.partial, t.nslots, t.gstore);
-    count_launches(1);
+    count_launch(KL_NORM_MAT_CC);
     return cudaGetLastError();
 }
 
@@ -316,6 +329,15 @@ cudaError_t launch_layer_sqnorm(const float* partial, int nslots, int64_t B, flo
     const int threads = 256;
     const int64_t blocks = (B * 32 + threads - 1) / threads;
     k_layer_sqnorm<<<(unsigned)blocks, threads, 0, s>>>(partial, nslots, B, out);
-    count_launches(1);
+    count_launch(KL_LAYER_SQNORM);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_layer_sqnorm_checked(const float* partial, int nslots, int64_t B, float* out,
+                                        const unsigned* status, cudaStream_t s) {
+    const int threads = 256;
+    const int64_t blocks = (B * 32 + threads - 1) / threads;
+    k_layer_sqnorm_status<<<(unsigned)blocks, threads, 0, s>>>(partial, nslots, B, out, status);
+    count_launch(KL_LAYER_SQNORM_STATUS);
     return cudaGetLastError();
 }

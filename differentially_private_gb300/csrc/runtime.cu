@@ -16,6 +16,8 @@
 #include <utility>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/dp_clip.h"
 #include "internal.h"
 
@@ -370,8 +372,25 @@ cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
 }
 
 static std::atomic<int64_t> g_launches{0};
+static std::atomic<int64_t> g_kernel_launches[KL_COUNT];
 
-void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+// Names of the kernels, in KernelId order.
+static const char* const kKernelNames[KL_COUNT] = {
+    "k_norm_t1", "k_norm_t1_group", "k_norm_ghost_cc", "k_norm_mat_cc", "k_layer_sqnorm",
+    "k_layer_sqnorm_status", "k_ghost_gram_tc", "k_mat_skinny_tc", "k_clip", "k_grad_wsum",
+    "k_grad_gemm_small", "k_grad_gemm_cc", "k_bias_sum", "k_prescale_rows", "k_clipped_sum_fold_pair_tc",
+    "k_clipped_sum_tc", "k_sum_layers_pair_tc", "k_noise_shard", "k_box_muller", "k_philox_normals",
+    "k_pack_groups", "k_int8_quantize_weight", "k_int8_sets", "k_int8_scales", "k_int8_gemm",
+    "k_wait_expires",
+};
+
+void count_launch(KernelId k) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    g_kernel_launches[k].fetch_add(1, std::memory_order_relaxed);
+}
+
+NvtxRange::NvtxRange(const char* name) { nvtxRangePushA(name); }
+NvtxRange::~NvtxRange() { nvtxRangePop(); }
 
 int plan_norm_kernel(int dtype, int64_t T, int64_t d_in, int64_t d_out, int has_bias, int* nslots) {
     Layer ly;
@@ -390,291 +409,14 @@ int nslots_for(int kernel, int64_t T, int64_t d_in, int64_t d_out) {
     return nslots_cc(kernel, T, d_in, d_out);
 }
 
-extern "C" {
+namespace {
 
-int dp_version(void) { return kVersion; }
-
-int64_t dp_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
-
-const char* dp_status_string(dp_status s) {
-    switch (s) {
-        case DP_OK: return "ok";
-        case DP_ERR_INVALID_ARG: return "invalid argument";
-        case DP_ERR_SHAPE: return "invalid shape";
-        case DP_ERR_STATE: return "call out of order";
-        case DP_ERR_NONFINITE: return "non-finite per-example norm";
-        case DP_ERR_CUDA: return "CUDA error";
-        case DP_ERR_OOM: return "out of device memory";
-        case DP_ERR_UNSUPPORTED: return "unsupported";
-    }
-    return "unknown status";
-}
-
-int dp_choose_path(int64_t T, int64_t d_in, int64_t d_out) {
-    if (T < 1 || d_in < 1 || d_out < 1) return -1;
-    return choose(T, d_in, d_out);
-}
-
-dp_status dp_create(dp_ctx** out, int device, void* cuda_stream) {
-    if (!out) return DP_ERR_INVALID_ARG;
-    *out = nullptr;
-    int ndev = 0;
-    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
-        cudaGetLastError();
-        return DP_ERR_CUDA;
-    }
-    cudaDeviceProp prop;
-    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return DP_ERR_CUDA;
-    if (prop.major != 10 || prop.minor != 3) return DP_ERR_UNSUPPORTED;
-    dp_ctx* ctx = new (std::nothrow) dp_ctx();
-    if (!ctx) return DP_ERR_OOM;
-    ctx->device = device;
-    ctx->stream = static_cast<cudaStream_t>(cuda_stream);
-    ctx->sm_count = prop.multiProcessorCount;
-    DeviceGuard g(device);
-    if (cudaMalloc(reinterpret_cast<void**>(&ctx->status_words), 2 * sizeof(unsigned)) != cudaSuccess) {
-        cudaGetLastError();
-        delete ctx;
-        return DP_ERR_OOM;
-    }
-    if (cudaMemsetAsync(ctx->status_words, 0, 2 * sizeof(unsigned), ctx->stream) != cudaSuccess) {
-        cudaFree(ctx->status_words);
-        delete ctx;
-        return DP_ERR_CUDA;
-    }
-    ctx->status = ctx->status_words + ctx->slot;
-    // the clip factor 1 of a layer whose operand was pre-scaled
-    const float one = 1.0f;
-    if (cudaMalloc(reinterpret_cast<void**>(&ctx->one), sizeof(float)) != cudaSuccess ||
-        cudaMemcpy(ctx->one, &one, sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) {
-        cudaGetLastError();
-        cudaFree(ctx->one);
-        cudaFree(ctx->status_words);
-        delete ctx;
-        return DP_ERR_OOM;
-    }
-    *out = ctx;
-    return DP_OK;
-}
-
-dp_status dp_destroy(dp_ctx* ctx) {
-    if (!ctx) return DP_OK;
-    DeviceGuard g(ctx->device);
-    cudaStreamSynchronize(ctx->stream);
-    for (Layer& ly : ctx->layers) {
-        cudaFree(ly.partial);
-        cudaFree(ly.gstore);
-        cudaFree(ly.escaled);
-    }
-    cudaFree(ctx->n2);
-    cudaFree(ctx->c);
-    cudaFree(ctx->status_words);
-    cudaFree(ctx->one);
-    cudaFree(ctx->d_slots);
-    cudaFree(ctx->fold_scratch);
-    cudaFree(ctx->fold_counters);
-    delete ctx;
-    return DP_OK;
-}
-
-dp_status dp_register_layer(dp_ctx* ctx, int64_t d_in, int64_t d_out, int has_bias, dp_dtype dtype,
-                            int* layer_id) {
-    if (!ctx || !layer_id) return fail(ctx, DP_ERR_INVALID_ARG, "NULL argument");
-    if (ctx->phase != IDLE) return fail(ctx, DP_ERR_STATE, "layers are registered between steps only");
-    if (d_in < 1 || d_out < 1) return fail(ctx, DP_ERR_SHAPE, "d_in and d_out must be >= 1");
-    if (dtype != DP_F32 && dtype != DP_BF16) return fail(ctx, DP_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
-    if ((int)ctx->layers.size() >= kMaxLayers) return fail(ctx, DP_ERR_UNSUPPORTED, "at most %d layers", kMaxLayers);
-    const unsigned __int128 nc = (unsigned __int128)(uint64_t)d_out * (uint64_t)d_in + (has_bias ? (uint64_t)d_out : 0);
-    if (nc + (uint64_t)ctx->P >= ((unsigned __int128)1 << 62)) return fail(ctx, DP_ERR_SHAPE, "too many coordinates");
-    Layer ly;
-    ly.d_in = d_in;
-    ly.d_out = d_out;
-    ly.has_bias = has_bias ? 1 : 0;
-    ly.dtype = dtype == DP_F32 ? DT_F32 : DT_BF16;
-    ly.coord_off = ctx->P;
-    ly.ncoords = (int64_t)nc;
-    ctx->P += ly.ncoords;
-    ctx->layers.push_back(ly);
-    *layer_id = (int)ctx->layers.size() - 1;
-    return DP_OK;
-}
-
-dp_status dp_layer_info(const dp_ctx* ctx, int layer_id, int64_t* coord_offset, int64_t* ncoords) {
-    if (!ctx) return DP_ERR_INVALID_ARG;
-    if (layer_id < 0 || layer_id >= (int)ctx->layers.size()) return DP_ERR_INVALID_ARG;
-    if (coord_offset) *coord_offset = ctx->layers[layer_id].coord_off;
-    if (ncoords) *ncoords = ctx->layers[layer_id].ncoords;
-    return DP_OK;
-}
-
-int64_t dp_num_coords(const dp_ctx* ctx) { return ctx ? ctx->P : 0; }
-
-dp_status dp_begin_step(dp_ctx* ctx, int64_t B) {
-    if (!ctx) return DP_ERR_INVALID_ARG;
-    if (B < 1) return fail(ctx, DP_ERR_SHAPE, "B must be >= 1");
-    if (ctx->layers.empty()) return fail(ctx, DP_ERR_STATE, "no layer registered");
-    DeviceGuard g(ctx->device);
-    dp_status st = grow(ctx, &ctx->n2, &ctx->bcap, (size_t)B);
-    if (st != DP_OK) return st;
-    st = grow(ctx, &ctx->c, &ctx->ccap, (size_t)B);
-    if (st != DP_OK) return st;
-    // the step takes the other status word; the previous step's clip kernel
-    // zeroed it, otherwise it is cleared here
-    const int next = ctx->slot ^ 1;
-    if (!ctx->clean[next]) {
-        const cudaError_t e = cudaMemsetAsync(ctx->status_words + next, 0, sizeof(unsigned), ctx->stream);
-        if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMemsetAsync");
-    }
-    ctx->clean[next] = false;
-    ctx->slot = next;
-    ctx->status = ctx->status_words + next;
-    for (Layer& ly : ctx->layers) {
-        ly.accumulated = false;
-        ly.A = ly.E = nullptr;
-        ly.T = 0;
-    }
-    ctx->B = B;
-    ctx->L = (double)B;
-    ctx->phase = OPEN;
-    ctx->err.clear();
-    return DP_OK;
-}
-
-dp_status dp_set_normalizer(dp_ctx* ctx, double L) {
-    if (!ctx) return DP_ERR_INVALID_ARG;
-    if (ctx->phase == IDLE) return fail(ctx, DP_ERR_STATE, "dp_set_normalizer needs an open step");
-    if (!std::isfinite(L) || L <= 0.0 || !std::isfinite((float)L))
-        return fail(ctx, DP_ERR_INVALID_ARG, "normalizer L must be finite and > 0");
-    ctx->L = L;
-    return DP_OK;
-}
-
-dp_status dp_norm_accumulate(dp_ctx* ctx, int layer_id, const void* A, const void* E, int64_t T,
-                             float* sqnorm_out) {
-    if (!ctx) return DP_ERR_INVALID_ARG;
-    dp_status st = check_accumulate(ctx, layer_id, A, E, T);
-    if (st != DP_OK) return st;
-    if (sqnorm_out && !aligned16(sqnorm_out) && (reinterpret_cast<uintptr_t>(sqnorm_out) & 3u))
-        return fail(ctx, DP_ERR_INVALID_ARG, "sqnorm_out must be 4-byte aligned");
-    DeviceGuard g(ctx->device);
-    Layer plan;
-    st = prepare(ctx, layer_id, A, E, T, plan);
-    if (st != DP_OK) return st;
-    st = launch_norm(ctx, plan);
-    if (st != DP_OK) return st;
-    return finish(ctx, layer_id, plan, sqnorm_out);
-}
-
-dp_status dp_norm_accumulate_batch(dp_ctx* ctx, int n, const int* layer_ids, const void* const* A,
-                                   const void* const* E, const int64_t* T, float* const* sqnorm_out) {
-    if (!ctx) return DP_ERR_INVALID_ARG;
-    if (n < 0 || (n > 0 && (!layer_ids || !A || !E || !T))) return fail(ctx, DP_ERR_INVALID_ARG, "bad batch arrays");
-    for (int i = 0; i < n; ++i) {
-        dp_status st = check_accumulate(ctx, layer_ids[i], A[i], E[i], T[i]);
-        if (st != DP_OK) return st;
-        for (int j = 0; j < i; ++j)
-            if (layer_ids[j] == layer_ids[i])
-                return fail(ctx, DP_ERR_STATE, "layer %d appears twice in one batch", layer_ids[i]);
-    }
-    DeviceGuard g(ctx->device);
-    std::vector<Layer> plans((size_t)n);
-    for (int i = 0; i < n; ++i) {
-        dp_status st = prepare(ctx, layer_ids[i], A[i], E[i], T[i], plans[i]);
-        if (st != DP_OK) return st;
-    }
-    // one grouped launch for every skinny materialized layer, one launch each for the rest
-    std::vector<NormTask> skinny, t1;
-    for (int i = 0; i < n; ++i) {
-        const NormTask t = make_norm_task(plans[i]);
-        if (plans[i].norm_kernel == NK_MAT_TC) {
-            skinny.push_back(t);
-        } else if (plans[i].norm_kernel == NK_T1 && t1_groupable(t)) {
-            t1.push_back(t);
-        } else {
-            dp_status st = launch_norm(ctx, plans[i]);
-            if (st != DP_OK) return st;
-        }
-    }
-    if (!t1.empty()) {
-        const cudaError_t e = launch_norm_t1_group(t1.data(), (int)t1.size(), ctx->B, ctx->stream);
-        if (e != cudaSuccess) return cuda_fail(ctx, e, "grouped norm kernel launch");
-    }
-    if (!skinny.empty()) {
-        const cudaError_t e = launch_mat_skinny_tc(skinny.data(), (int)skinny.size(), ctx->B, ctx->status, ctx->stream);
-        if (e != cudaSuccess) return cuda_fail(ctx, e, "grouped norm kernel launch");
-    }
-    for (int i = 0; i < n; ++i) {
-        dp_status st = finish(ctx, layer_ids[i], plans[i], sqnorm_out ? sqnorm_out[i] : nullptr);
-        if (st != DP_OK) return st;
-    }
-    return DP_OK;
-}
-
-dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnorm_out) {
-    if (!ctx) return DP_ERR_INVALID_ARG;
-    if (ctx->phase != OPEN) return fail(ctx, DP_ERR_STATE, "dp_clip_factors needs an open, unclipped step");
-    if (!std::isfinite(C) || !(C > 0.0f)) return fail(ctx, DP_ERR_INVALID_ARG, "clip bound C must be finite and > 0");
-    for (size_t l = 0; l < ctx->layers.size(); ++l)
-        if (!ctx->layers[l].accumulated)
-            return fail(ctx, DP_ERR_STATE, "layer %zu was not accumulated in this step", l);
-    DeviceGuard g(ctx->device);
-    std::vector<std::pair<const float*, int64_t>> key(ctx->layers.size());
-    int64_t total = 0;
-    for (size_t l = 0; l < ctx->layers.size(); ++l) {
-        key[l] = {ctx->layers[l].partial, (int64_t)ctx->layers[l].nslots};
-        total += ctx->layers[l].nslots;
-    }
-    if (key != ctx->slots_key) {
-        // the flat slot table changes only when the layer set or its scratch does
-        if (ctx->d_slots_cap < (size_t)total) {
-            cudaError_t e = cudaStreamSynchronize(ctx->stream);
-            if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamSynchronize");
-            cudaFree(ctx->d_slots);
-            ctx->d_slots = nullptr;
-            ctx->d_slots_cap = 0;
-            e = cudaMalloc(reinterpret_cast<void**>(&ctx->d_slots), (size_t)total * sizeof(SlotRef));
-            if (e != cudaSuccess) return fail(ctx, DP_ERR_OOM, "cudaMalloc of the slot table failed");
-            ctx->d_slots_cap = (size_t)total;
-        }
-        // an upload from pageable memory has been staged when the call returns,
-        // so h_slots can be rebuilt while an earlier upload is still in flight
-        ctx->h_slots.clear();
-        for (const auto& k : key)
-            for (int64_t j = 0; j < k.second; ++j) ctx->h_slots.push_back(SlotRef{k.first + j, k.second});
-        ctx->slots_key = key;
-        const cudaError_t e = cudaMemcpyAsync(ctx->d_slots, ctx->h_slots.data(), (size_t)total * sizeof(SlotRef),
-                                              cudaMemcpyHostToDevice, ctx->stream);
-        if (e != cudaSuccess) return cuda_fail(ctx, e, "slot table upload");
-    }
-    ClipParams p;
-    p.B = ctx->B;
-    p.C = C;
-    p.slots = ctx->d_slots;
-    p.total_slots = total;
-    // the clip kernel also zeroes the other status word for the next step
-    // (every kernel that could write it belongs to an earlier, finished step)
-    p.status_next = ctx->status_words + (ctx->slot ^ 1);
-    // the clip kernel also writes the first kMaxPrescale pre-scaled operand copies
-    p.nscale = 0;
-    for (Layer& ly : ctx->layers) {
-        ly.scaled_by_clip = ly.grad_kernel == GK_GEMM_TC && ly.prescale && p.nscale < kMaxPrescale;
-        if (!ly.scaled_by_clip) continue;
-        const int64_t d = ly.prescale_A ? ly.d_in : ly.d_out;
-        p.scale[p.nscale++] = PrescaleJob{static_cast<const uint4*>(ly.prescale_A ? ly.A : ly.E),
-                                          reinterpret_cast<uint4*>(ly.escaled), ly.T * d / 8};
-    }
-    const cudaError_t e = launch_clip(p, ctx->n2, ctx->c, total_sqnorm_out, c_out, ctx->status, ctx->stream);
-    if (e != cudaSuccess) return cuda_fail(ctx, e, "clip kernel launch");
-    ctx->clean[ctx->slot ^ 1] = true;
-    ctx->C = C;
-    ctx->phase = CLIPPED;
-    return DP_OK;
-}
-
-dp_status dp_clipped_noisy_grad(dp_ctx* ctx, float sigma, uint64_t seed, uint64_t step, float* const* G) {
-    if (!ctx) return DP_ERR_INVALID_ARG;
-    if (ctx->phase != CLIPPED) return fail(ctx, DP_ERR_STATE, "dp_clipped_noisy_grad needs dp_clip_factors first");
-    if (!std::isfinite(sigma) || sigma < 0.0f) return fail(ctx, DP_ERR_INVALID_ARG, "sigma must be finite and >= 0");
+// The gradient phase of a step: G = (sum_i c_i g_i + sigma C z) / L for every
+// layer, with L the step's normalizer (dp_clipped_noisy_grad) or 1 and
+// sigma = 0 (dp_clipped_sum: the clipped sum alone).
+dp_status clipped_grad(dp_ctx* ctx, float sigma, uint64_t seed, uint64_t step, float* const* G, float L,
+                       const char* who) {
+    if (ctx->phase != CLIPPED) return fail(ctx, DP_ERR_STATE, "%s needs dp_clip_factors first", who);
     if (!G) return fail(ctx, DP_ERR_INVALID_ARG, "G must not be NULL");
     for (size_t l = 0; l < ctx->layers.size(); ++l)
         if (!G[l] || !aligned16(G[l])) return fail(ctx, DP_ERR_INVALID_ARG, "G[%zu] is NULL or not 16-byte aligned", l);
@@ -683,7 +425,7 @@ dp_status dp_clipped_noisy_grad(dp_ctx* ctx, float sigma, uint64_t seed, uint64_
     sc.B = ctx->B;
     sc.C = ctx->C;
     sc.sigma = sigma;
-    sc.L = (float)ctx->L;
+    sc.L = L;
     sc.seed = seed;
     sc.step = step;
     // layers whose pre-scaled operand the clip kernel wrote are summed together
@@ -768,7 +510,337 @@ dp_status dp_clipped_noisy_grad(dp_ctx* ctx, float sigma, uint64_t seed, uint64_
     return DP_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+int dp_version(void) { return kVersion; }
+
+int64_t dp_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int dp_kernel_launch_counts(const char** names, int64_t* counts, int cap) {
+    for (int k = 0; k < KL_COUNT && k < cap; ++k) {
+        if (names) names[k] = kKernelNames[k];
+        if (counts) counts[k] = g_kernel_launches[k].load(std::memory_order_relaxed);
+    }
+    return KL_COUNT;
+}
+
+const char* dp_status_string(dp_status s) {
+    switch (s) {
+        case DP_OK: return "ok";
+        case DP_ERR_INVALID_ARG: return "invalid argument";
+        case DP_ERR_SHAPE: return "invalid shape";
+        case DP_ERR_STATE: return "call out of order";
+        case DP_ERR_NONFINITE: return "non-finite per-example norm";
+        case DP_ERR_CUDA: return "CUDA error";
+        case DP_ERR_OOM: return "out of device memory";
+        case DP_ERR_UNSUPPORTED: return "unsupported";
+    }
+    return "unknown status";
+}
+
+int dp_choose_path(int64_t T, int64_t d_in, int64_t d_out) {
+    if (T < 1 || d_in < 1 || d_out < 1) return -1;
+    return choose(T, d_in, d_out);
+}
+
+dp_status dp_create(dp_ctx** out, int device, void* cuda_stream) {
+    NvtxRange nvtx_range("dp_create");
+    if (!out) return DP_ERR_INVALID_ARG;
+    *out = nullptr;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+        cudaGetLastError();
+        return DP_ERR_CUDA;
+    }
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return DP_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return DP_ERR_UNSUPPORTED;
+    dp_ctx* ctx = new (std::nothrow) dp_ctx();
+    if (!ctx) return DP_ERR_OOM;
+    ctx->device = device;
+    ctx->stream = static_cast<cudaStream_t>(cuda_stream);
+    ctx->sm_count = prop.multiProcessorCount;
+    DeviceGuard g(device);
+    if (cudaMalloc(reinterpret_cast<void**>(&ctx->status_words), 2 * sizeof(unsigned)) != cudaSuccess) {
+        cudaGetLastError();
+        delete ctx;
+        return DP_ERR_OOM;
+    }
+    if (cudaMemsetAsync(ctx->status_words, 0, 2 * sizeof(unsigned), ctx->stream) != cudaSuccess) {
+        cudaFree(ctx->status_words);
+        delete ctx;
+        return DP_ERR_CUDA;
+    }
+    ctx->status = ctx->status_words + ctx->slot;
+    // the clip factor 1 of a layer whose operand was pre-scaled
+    const float one = 1.0f;
+    if (cudaMalloc(reinterpret_cast<void**>(&ctx->one), sizeof(float)) != cudaSuccess ||
+        cudaMemcpy(ctx->one, &one, sizeof(float), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(ctx->one);
+        cudaFree(ctx->status_words);
+        delete ctx;
+        return DP_ERR_OOM;
+    }
+    *out = ctx;
+    return DP_OK;
+}
+
+dp_status dp_destroy(dp_ctx* ctx) {
+    NvtxRange nvtx_range("dp_destroy");
+    if (!ctx) return DP_OK;
+    DeviceGuard g(ctx->device);
+    cudaStreamSynchronize(ctx->stream);
+    for (Layer& ly : ctx->layers) {
+        cudaFree(ly.partial);
+        cudaFree(ly.gstore);
+        cudaFree(ly.escaled);
+    }
+    cudaFree(ctx->n2);
+    cudaFree(ctx->c);
+    cudaFree(ctx->status_words);
+    cudaFree(ctx->one);
+    cudaFree(ctx->d_slots);
+    cudaFree(ctx->fold_scratch);
+    cudaFree(ctx->fold_counters);
+    delete ctx;
+    return DP_OK;
+}
+
+dp_status dp_register_layer(dp_ctx* ctx, int64_t d_in, int64_t d_out, int has_bias, dp_dtype dtype,
+                            int* layer_id) {
+    NvtxRange nvtx_range("dp_register_layer");
+    if (!ctx || !layer_id) return fail(ctx, DP_ERR_INVALID_ARG, "NULL argument");
+    if (ctx->phase != IDLE) return fail(ctx, DP_ERR_STATE, "layers are registered between steps only");
+    if (d_in < 1 || d_out < 1) return fail(ctx, DP_ERR_SHAPE, "d_in and d_out must be >= 1");
+    if (dtype != DP_F32 && dtype != DP_BF16) return fail(ctx, DP_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if ((int)ctx->layers.size() >= kMaxLayers) return fail(ctx, DP_ERR_UNSUPPORTED, "at most %d layers", kMaxLayers);
+    const unsigned __int128 nc = (unsigned __int128)(uint64_t)d_out * (uint64_t)d_in + (has_bias ? (uint64_t)d_out : 0);
+    if (nc + (uint64_t)ctx->P >= ((unsigned __int128)1 << 62)) return fail(ctx, DP_ERR_SHAPE, "too many coordinates");
+    Layer ly;
+    ly.d_in = d_in;
+    ly.d_out = d_out;
+    ly.has_bias = has_bias ? 1 : 0;
+    ly.dtype = dtype == DP_F32 ? DT_F32 : DT_BF16;
+    ly.coord_off = ctx->P;
+    ly.ncoords = (int64_t)nc;
+    ctx->P += ly.ncoords;
+    ctx->layers.push_back(ly);
+    *layer_id = (int)ctx->layers.size() - 1;
+    return DP_OK;
+}
+
+dp_status dp_layer_info(const dp_ctx* ctx, int layer_id, int64_t* coord_offset, int64_t* ncoords) {
+    if (!ctx) return DP_ERR_INVALID_ARG;
+    if (layer_id < 0 || layer_id >= (int)ctx->layers.size()) return DP_ERR_INVALID_ARG;
+    if (coord_offset) *coord_offset = ctx->layers[layer_id].coord_off;
+    if (ncoords) *ncoords = ctx->layers[layer_id].ncoords;
+    return DP_OK;
+}
+
+int64_t dp_num_coords(const dp_ctx* ctx) { return ctx ? ctx->P : 0; }
+
+dp_status dp_begin_step(dp_ctx* ctx, int64_t B) {
+    NvtxRange nvtx_range("dp_begin_step");
+    if (!ctx) return DP_ERR_INVALID_ARG;
+    if (B < 1) return fail(ctx, DP_ERR_SHAPE, "B must be >= 1");
+    if (ctx->layers.empty()) return fail(ctx, DP_ERR_STATE, "no layer registered");
+    DeviceGuard g(ctx->device);
+    dp_status st = grow(ctx, &ctx->n2, &ctx->bcap, (size_t)B);
+    if (st != DP_OK) return st;
+    st = grow(ctx, &ctx->c, &ctx->ccap, (size_t)B);
+    if (st != DP_OK) return st;
+    // the step takes the other status word; the previous step's clip kernel
+    // zeroed it, otherwise it is cleared here
+    const int next = ctx->slot ^ 1;
+    if (!ctx->clean[next]) {
+        const cudaError_t e = cudaMemsetAsync(ctx->status_words + next, 0, sizeof(unsigned), ctx->stream);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMemsetAsync");
+    }
+    ctx->clean[next] = false;
+    ctx->slot = next;
+    ctx->status = ctx->status_words + next;
+    for (Layer& ly : ctx->layers) {
+        ly.accumulated = false;
+        ly.A = ly.E = nullptr;
+        ly.T = 0;
+    }
+    ctx->B = B;
+    ctx->L = (double)B;
+    ctx->phase = OPEN;
+    ctx->err.clear();
+    return DP_OK;
+}
+
+dp_status dp_set_normalizer(dp_ctx* ctx, double L) {
+    NvtxRange nvtx_range("dp_set_normalizer");
+    if (!ctx) return DP_ERR_INVALID_ARG;
+    if (ctx->phase == IDLE) return fail(ctx, DP_ERR_STATE, "dp_set_normalizer needs an open step");
+    if (!std::isfinite(L) || L <= 0.0 || !std::isfinite((float)L))
+        return fail(ctx, DP_ERR_INVALID_ARG, "normalizer L must be finite and > 0");
+    ctx->L = L;
+    return DP_OK;
+}
+
+dp_status dp_norm_accumulate(dp_ctx* ctx, int layer_id, const void* A, const void* E, int64_t T,
+                             float* sqnorm_out) {
+    NvtxRange nvtx_range("dp_norm_accumulate");
+    if (!ctx) return DP_ERR_INVALID_ARG;
+    dp_status st = check_accumulate(ctx, layer_id, A, E, T);
+    if (st != DP_OK) return st;
+    if (sqnorm_out && !aligned16(sqnorm_out) && (reinterpret_cast<uintptr_t>(sqnorm_out) & 3u))
+        return fail(ctx, DP_ERR_INVALID_ARG, "sqnorm_out must be 4-byte aligned");
+    DeviceGuard g(ctx->device);
+    Layer plan;
+    st = prepare(ctx, layer_id, A, E, T, plan);
+    if (st != DP_OK) return st;
+    st = launch_norm(ctx, plan);
+    if (st != DP_OK) return st;
+    return finish(ctx, layer_id, plan, sqnorm_out);
+}
+
+dp_status dp_norm_accumulate_batch(dp_ctx* ctx, int n, const int* layer_ids, const void* const* A,
+                                   const void* const* E, const int64_t* T, float* const* sqnorm_out) {
+    NvtxRange nvtx_range("dp_norm_accumulate_batch");
+    if (!ctx) return DP_ERR_INVALID_ARG;
+    if (n < 0 || (n > 0 && (!layer_ids || !A || !E || !T))) return fail(ctx, DP_ERR_INVALID_ARG, "bad batch arrays");
+    for (int i = 0; i < n; ++i) {
+        dp_status st = check_accumulate(ctx, layer_ids[i], A[i], E[i], T[i]);
+        if (st != DP_OK) return st;
+        for (int j = 0; j < i; ++j)
+            if (layer_ids[j] == layer_ids[i])
+                return fail(ctx, DP_ERR_STATE, "layer %d appears twice in one batch", layer_ids[i]);
+    }
+    DeviceGuard g(ctx->device);
+    std::vector<Layer> plans((size_t)n);
+    for (int i = 0; i < n; ++i) {
+        dp_status st = prepare(ctx, layer_ids[i], A[i], E[i], T[i], plans[i]);
+        if (st != DP_OK) return st;
+    }
+    // one grouped launch for every skinny materialized layer, one launch each for the rest
+    std::vector<NormTask> skinny, t1;
+    for (int i = 0; i < n; ++i) {
+        const NormTask t = make_norm_task(plans[i]);
+        if (plans[i].norm_kernel == NK_MAT_TC) {
+            skinny.push_back(t);
+        } else if (plans[i].norm_kernel == NK_T1 && t1_groupable(t)) {
+            t1.push_back(t);
+        } else {
+            dp_status st = launch_norm(ctx, plans[i]);
+            if (st != DP_OK) return st;
+        }
+    }
+    if (!t1.empty()) {
+        const cudaError_t e = launch_norm_t1_group(t1.data(), (int)t1.size(), ctx->B, ctx->stream);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "grouped norm kernel launch");
+    }
+    if (!skinny.empty()) {
+        const cudaError_t e = launch_mat_skinny_tc(skinny.data(), (int)skinny.size(), ctx->B, ctx->status, ctx->stream);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "grouped norm kernel launch");
+    }
+    for (int i = 0; i < n; ++i) {
+        dp_status st = finish(ctx, layer_ids[i], plans[i], sqnorm_out ? sqnorm_out[i] : nullptr);
+        if (st != DP_OK) return st;
+    }
+    return DP_OK;
+}
+
+dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnorm_out) {
+    NvtxRange nvtx_range("dp_clip_factors");
+    if (!ctx) return DP_ERR_INVALID_ARG;
+    if (ctx->phase != OPEN) return fail(ctx, DP_ERR_STATE, "dp_clip_factors needs an open, unclipped step");
+    if (!std::isfinite(C) || !(C > 0.0f)) return fail(ctx, DP_ERR_INVALID_ARG, "clip bound C must be finite and > 0");
+    for (size_t l = 0; l < ctx->layers.size(); ++l)
+        if (!ctx->layers[l].accumulated)
+            return fail(ctx, DP_ERR_STATE, "layer %zu was not accumulated in this step", l);
+    DeviceGuard g(ctx->device);
+    std::vector<std::pair<const float*, int64_t>> key(ctx->layers.size());
+    int64_t total = 0;
+    for (size_t l = 0; l < ctx->layers.size(); ++l) {
+        key[l] = {ctx->layers[l].partial, (int64_t)ctx->layers[l].nslots};
+        total += ctx->layers[l].nslots;
+    }
+    if (key != ctx->slots_key) {
+        // the flat slot table changes only when the layer set or its scratch does
+        if (ctx->d_slots_cap < (size_t)total) {
+            cudaError_t e = cudaStreamSynchronize(ctx->stream);
+            if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamSynchronize");
+            cudaFree(ctx->d_slots);
+            ctx->d_slots = nullptr;
+            ctx->d_slots_cap = 0;
+            e = cudaMalloc(reinterpret_cast<void**>(&ctx->d_slots), (size_t)total * sizeof(SlotRef));
+            if (e != cudaSuccess) return fail(ctx, DP_ERR_OOM, "cudaMalloc of the slot table failed");
+            ctx->d_slots_cap = (size_t)total;
+        }
+        // an upload from pageable memory has been staged when the call returns,
+        // so h_slots can be rebuilt while an earlier upload is still in flight
+        ctx->h_slots.clear();
+        for (const auto& k : key)
+            for (int64_t j = 0; j < k.second; ++j) ctx->h_slots.push_back(SlotRef{k.first + j, k.second});
+        ctx->slots_key = key;
+        const cudaError_t e = cudaMemcpyAsync(ctx->d_slots, ctx->h_slots.data(), (size_t)total * sizeof(SlotRef),
+                                              cudaMemcpyHostToDevice, ctx->stream);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "slot table upload");
+    }
+    ClipParams p;
+    p.B = ctx->B;
+    p.C = C;
+    p.slots = ctx->d_slots;
+    p.total_slots = total;
+    // the clip kernel also zeroes the other status word for the next step
+    // (every kernel that could write it belongs to an earlier, finished step)
+    p.status_next = ctx->status_words + (ctx->slot ^ 1);
+    // the clip kernel also writes the first kMaxPrescale pre-scaled operand copies
+    p.nscale = 0;
+    for (Layer& ly : ctx->layers) {
+        ly.scaled_by_clip = ly.grad_kernel == GK_GEMM_TC && ly.prescale && p.nscale < kMaxPrescale;
+        if (!ly.scaled_by_clip) continue;
+        const int64_t d = ly.prescale_A ? ly.d_in : ly.d_out;
+        p.scale[p.nscale++] = PrescaleJob{static_cast<const uint4*>(ly.prescale_A ? ly.A : ly.E),
+                                          reinterpret_cast<uint4*>(ly.escaled), ly.T * d / 8};
+    }
+    const cudaError_t e = launch_clip(p, ctx->n2, ctx->c, total_sqnorm_out, c_out, ctx->status, ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "clip kernel launch");
+    ctx->clean[ctx->slot ^ 1] = true;
+    ctx->C = C;
+    ctx->phase = CLIPPED;
+    return DP_OK;
+}
+
+
+dp_status dp_clipped_noisy_grad(dp_ctx* ctx, float sigma, uint64_t seed, uint64_t step, float* const* G) {
+    NvtxRange nvtx_range("dp_clipped_noisy_grad");
+    if (!ctx) return DP_ERR_INVALID_ARG;
+    if (!std::isfinite(sigma) || sigma < 0.0f) return fail(ctx, DP_ERR_INVALID_ARG, "sigma must be finite and >= 0");
+    return clipped_grad(ctx, sigma, seed, step, G, (float)ctx->L, "dp_clipped_noisy_grad");
+}
+
+dp_status dp_clipped_sum(dp_ctx* ctx, float* const* S) {
+    NvtxRange nvtx_range("dp_clipped_sum");
+    if (!ctx) return DP_ERR_INVALID_ARG;
+    return clipped_grad(ctx, 0.0f, 0, 0, S, 1.0f, "dp_clipped_sum");
+}
+
+dp_status dp_noise_shard(const float* S, float* G, uint64_t k0, int64_t n, float sigma, float C, double L,
+                         uint64_t seed, uint64_t step, void* stream) {
+    NvtxRange nvtx_range("dp_noise_shard");
+    if (n < 0) return DP_ERR_SHAPE;
+    if (k0 + (uint64_t)n < k0) return DP_ERR_SHAPE;
+    if (!std::isfinite(sigma) || sigma < 0.0f) return DP_ERR_INVALID_ARG;
+    if (!std::isfinite(C) || !(C > 0.0f)) return DP_ERR_INVALID_ARG;
+    if (!std::isfinite(L) || L <= 0.0 || !std::isfinite((float)L) || !((float)L > 0.0f)) return DP_ERR_INVALID_ARG;
+    if (n == 0) return DP_OK;
+    if (!S || !G || (reinterpret_cast<uintptr_t>(S) & 3u) || (reinterpret_cast<uintptr_t>(G) & 3u))
+        return DP_ERR_INVALID_ARG;
+    const cudaError_t e =
+        launch_noise_shard(S, G, k0, n, sigma * C, (float)L, seed, step, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DP_OK : DP_ERR_CUDA;
+}
+
 dp_status dp_step_status(dp_ctx* ctx) {
+    NvtxRange nvtx_range("dp_step_status");
     if (!ctx) return DP_ERR_INVALID_ARG;
     DeviceGuard g(ctx->device);
     cudaError_t e = cudaStreamSynchronize(ctx->stream);
@@ -782,6 +854,7 @@ dp_status dp_step_status(dp_ctx* ctx) {
 }
 
 dp_status dp_check_wait_timeout(dp_ctx* ctx, uint32_t limit_ms) {
+    NvtxRange nvtx_range("dp_check_wait_timeout");
     if (!ctx) return DP_ERR_INVALID_ARG;
     if (ctx->phase == IDLE) return fail(ctx, DP_ERR_STATE, "dp_check_wait_timeout needs an open step");
     if (limit_ms < 1 || limit_ms > 2000) return fail(ctx, DP_ERR_INVALID_ARG, "limit_ms must be in 1..2000");
@@ -793,6 +866,7 @@ dp_status dp_check_wait_timeout(dp_ctx* ctx, uint32_t limit_ms) {
 const char* dp_last_error(const dp_ctx* ctx) { return ctx ? ctx->err.c_str() : ""; }
 
 dp_status dp_box_muller(const uint32_t* words, int64_t npairs, float* z_out, void* stream) {
+    NvtxRange nvtx_range("dp_box_muller");
     if (npairs < 0) return DP_ERR_SHAPE;
     if (npairs == 0) return DP_OK;
     if (!words || !z_out || (reinterpret_cast<uintptr_t>(words) & 7u) || (reinterpret_cast<uintptr_t>(z_out) & 7u))
@@ -803,6 +877,7 @@ dp_status dp_box_muller(const uint32_t* words, int64_t npairs, float* z_out, voi
 
 dp_status dp_philox_normals(uint64_t seed, uint64_t step, uint64_t k0, int64_t n, uint32_t* raw_out,
                             float* z_out, void* stream) {
+    NvtxRange nvtx_range("dp_philox_normals");
     if (n < 0) return DP_ERR_SHAPE;
     if (n == 0) return DP_OK;
     if ((raw_out && (reinterpret_cast<uintptr_t>(raw_out) & 3u)) || (z_out && (reinterpret_cast<uintptr_t>(z_out) & 3u)))

@@ -1011,7 +1011,7 @@ static cudaError_t launch_fold_pair(const GradTask& t, const float* c, unsigned*
         }
     }
     const cudaError_t e = launch_dependent(k_clipped_sum_fold_pair_tc, dim3(2 * npairs), dim3(kFoldThreads), kFoldPairSmem, s, p);
-    count_launches(1);
+    count_launch(KL_CLIPPED_SUM_FOLD_PAIR_TC);
     return e;
 }
 
@@ -1057,7 +1057,7 @@ cudaError_t launch_clipped_sum_tc(const GradTask& t, const float* c, unsigned* s
     const int sms = sm_count_cached();
     const int grid = ntiles < sms ? ntiles : sms;
     const cudaError_t e = launch_dependent(k_clipped_sum_tc, dim3(grid), dim3(kFoldThreads), kSumSmem, s, p);
-    count_launches(1);
+    count_launch(KL_CLIPPED_SUM_TC);
     return e;
 }
 
@@ -1107,6 +1107,6 @@ cudaError_t launch_sum_layers_tc(const GradTask* tasks, int n, unsigned* status,
     const int pairs = pair_clusters_cached(kern, (int)kPairSmem, clusters);
     const int grid = 2 * (tiles < pairs ? tiles : pairs);
     const cudaError_t e = launch_dependent(k_sum_layers_pair_tc, dim3(grid), dim3(kFoldThreads), kPairSmem, s, p);
-    count_launches(1);
+    count_launch(KL_SUM_LAYERS_PAIR_TC);
     return e;
 }

@@ -286,6 +286,6 @@ cudaError_t launch_ghost_gram_tc(const NormTask& t, int64_t B, unsigned* status,
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int grid = p.total_items < sms ? p.total_items : sms;
     const cudaError_t e = launch_dependent(k_ghost_gram_tc, dim3(grid), dim3(kGThreads), kGramSmem, s, p);
-    count_launches(1);
+    count_launch(KL_GHOST_GRAM_TC);
     return e;
 }

@@ -452,7 +452,7 @@ cudaError_t launch_mat_skinny_tc(const NormTask* tasks, int n, int64_t B, unsign
         p.blk_begin[p.nlayers] = blocks;
         const int grid = (int)(blocks < sms ? blocks : sms);
         const cudaError_t e = launch_dependent(k_mat_skinny_tc, dim3(grid), dim3(kThreads), kSmem, s, p);
-        count_launches(1);
+        count_launch(KL_MAT_SKINNY_TC);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -24,6 +24,6 @@ __global__ void k_wait_expires(unsigned* status, uint64_t limit_ns) {
 
 cudaError_t launch_wait_expiry(unsigned* status, uint64_t limit_ns, cudaStream_t s) {
     k_wait_expires<<<1, 1, 0, s>>>(status, limit_ns);
-    count_launches(1);
+    count_launch(KL_WAIT_EXPIRES);
     return cudaGetLastError();
 }

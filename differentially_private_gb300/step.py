@@ -149,11 +149,13 @@ class PreparedStep:
         self._clip = int(self.clip.data_ptr())
         self._sqn = int(self.sqnorm.data_ptr())
 
-    def run(self, C: float, sigma: float, seed: int, step: int, events=None) -> None:
+    def run(self, C: float, sigma: float, seed: int, step: int, events=None, after_phase=None) -> None:
         """Enqueue one step on the context's stream (asynchronous; no status check).
 
         events: optional four CUDA events recorded on the stream before the
         norms, after the norms, after the clip factors and after the gradient.
+        after_phase: optional callable, called with "norm", "clip" and "grad"
+        right after the calls of that phase were enqueued (instrumentation).
         """
         lib, ctx = self.lib, self.pg.ctx
         stream = self.pg.stream
@@ -166,13 +168,19 @@ class PreparedStep:
             st = lib.dp_norm_accumulate_batch(ctx, self.n, self._ids, self._a, self._e, self._t, self._sq)
         if events:
             events[1].record(stream)
+        if after_phase and st == b.DP_OK:
+            after_phase("norm")
         if st == b.DP_OK:
             st = lib.dp_clip_factors(ctx, C, self._clip, self._sqn)
         if events:
             events[2].record(stream)
+        if after_phase and st == b.DP_OK:
+            after_phase("clip")
         if st == b.DP_OK:
             st = lib.dp_clipped_noisy_grad(ctx, sigma, seed & (2 ** 64 - 1), step & (2 ** 64 - 1), self._g)
         if events:
             events[3].record(stream)
+        if after_phase and st == b.DP_OK:
+            after_phase("grad")
         if st != b.DP_OK:
             raise b.DPError(st, "PreparedStep.run", b.dp_last_error(ctx))

@@ -74,6 +74,15 @@ int dp_version(void);
  */
 int64_t dp_kernel_launches(void);
 
+/*
+ * dp_kernel_launch_counts -- the same counter split by kernel: for each
+ * kernel kind k < min(cap, K), names[k] receives its kernel's name (a static
+ * string owned by the library) and counts[k] the number of its launches so
+ * far; either array may be NULL.  Returns K, the number of kernel kinds.
+ * Host-side counters, for the release record of a run; never synchronizes.
+ */
+int dp_kernel_launch_counts(const char** names, int64_t* counts, int cap);
+
 /* Static description of a status code (never NULL). */
 const char* dp_status_string(dp_status s);
 
@@ -203,6 +212,38 @@ dp_status dp_clipped_noisy_grad(dp_ctx* ctx, float sigma, uint64_t seed, uint64_
                                 float* const* G);
 
 /*
+ * dp_clipped_sum -- the gradient phase without noise and without the
+ * normalizer: S = sum_i c_i g_i (+ the bias sum) for every registered layer,
+ * written to S[layer] in the layout of dp_clipped_noisy_grad (device,
+ * 16-byte aligned).  It is the partial sum one rank contributes when the
+ * records of a batch are split over several GPUs: the ranks add their
+ * partial sums, and the noise is then drawn once on the total by
+ * dp_noise_shard, keyed by the global coordinate, so each coordinate gets
+ * exactly one draw whatever the number of ranks ("Privacy-Preserving Machine
+ * Learning", phases 4-5: noise added once to the clipped sum, then the
+ * division; "Sensitivity Inflation ...", section 4.1, Proposition 2: every
+ * record's clipped contribution depends on that record only, so the sum over
+ * ranks is the batch's sum).  Same state rules and errors as
+ * dp_clipped_noisy_grad, which it replaces in a step: it closes the step.
+ */
+dp_status dp_clipped_sum(dp_ctx* ctx, float* const* S);
+
+/*
+ * dp_noise_shard -- noise and normalizer on a contiguous range of global
+ * coordinates: G[j] = (S[j] + sigma * C * z_{k0 + j}) / L for 0 <= j < n,
+ * with z the coordinate's standard normal of the (seed, step) stream exactly
+ * as dp_clipped_noisy_grad draws it, evaluated in float (sigma * C rounded to
+ * float first, L rounded to float).  S and G: device float [n], 4-byte
+ * aligned (16-byte alignment with k0 % 4 == 0 takes vector loads), G may
+ * equal S; caller-owned.  sigma finite and >= 0, C finite and > 0, L finite
+ * and > 0 (DP_ERR_INVALID_ARG otherwise); n >= 0 and k0 + n must not wrap
+ * (DP_ERR_SHAPE).  Launches on `stream` (NULL = legacy default);
+ * DP_ERR_CUDA for a launch failure.
+ */
+dp_status dp_noise_shard(const float* S, float* G, uint64_t k0, int64_t n, float sigma, float C, double L,
+                         uint64_t seed, uint64_t step, void* stream);
+
+/*
  * dp_step_status -- synchronize the context's stream and return the deferred
  * device-side result of the step: DP_OK, DP_ERR_NONFINITE, or DP_ERR_CUDA for
  * an asynchronous CUDA error or a device-side wait that gave up (a kernel
@@ -329,16 +370,34 @@ dp_status dp_check_wait_timeout(dp_ctx* ctx, uint32_t limit_ms);
  * (B times the slots per record, which depend on T, d_in and d_out) fails
  * with DP_ERR_SHAPE before anything is launched.  The first call on a
  * device resolves the array's device address (cudaGetSymbolAddress); make
- * that first call before any stream capture.  All calls share the one
- * array and it keeps the last call's contents: calls whose work overlaps on
- * the GPU (other streams, other host threads) race and give wrong results;
- * serialize them.  Returns DP_ERR_INVALID_ARG / DP_ERR_SHAPE for bad
- * arguments, DP_ERR_CUDA when a CUDA call or launch fails.  No cudaMalloc,
- * cudaFree or allocating library routine is called.
+ * that first call before any stream capture.  The address is kept per
+ * device and resolved again when the device's current context changes (a
+ * cudaDeviceReset loads the library's device code anew).  All calls share
+ * the one array and it keeps the last call's contents: calls whose work
+ * overlaps on the GPU (other streams, other host threads) race and give
+ * wrong results; serialize them.  The tensor-core norm kernels wait at most
+ * 2 s for their own copies and MMAs; when such a wait gives up, every
+ * sqnorm_out[i] of that call is NaN (the call itself has returned DP_OK
+ * before the kernels ran), and the next call starts clean.  Returns
+ * DP_ERR_INVALID_ARG / DP_ERR_SHAPE for bad arguments, DP_ERR_CUDA when a
+ * CUDA call or launch fails.  No cudaMalloc, cudaFree or allocating library
+ * routine is called.
  */
 dp_status dp_layer_sqnorms_static(const void* A, const void* E, int64_t B, int64_t T, int64_t d_in,
                                   int64_t d_out, int has_bias, dp_dtype dtype, float* sqnorm_out,
                                   void* stream);
+
+/*
+ * dp_static_check_wait_timeout -- test hook for the NaN report above:
+ * enqueues on `stream`, on the current device, a one-thread kernel whose
+ * wait on a barrier that nothing completes gives up after limit_ms
+ * milliseconds (1..2000, DP_ERR_INVALID_ARG otherwise) and records the
+ * timeout exactly as a norm kernel's wait would.  The next
+ * dp_layer_sqnorms_static call on the same stream then writes NaN norms; the
+ * one after it is clean.  Allocates nothing.  DP_ERR_CUDA for a launch
+ * failure.
+ */
+dp_status dp_static_check_wait_timeout(uint32_t limit_ms, void* stream);
 
 #ifdef __cplusplus
 }

@@ -66,12 +66,21 @@ def _static(A, E, T, d_in, d_out, has_bias, dtype):
 
 CASES = [
     # (B, T, d_in, d_out, bias, dtype): tensor-core Gram, skinny materialize,
-    # T = 1 closed form, CUDA-core Gram with a bias
+    # T = 1 closed form, CUDA-core Gram with a bias, CUDA-core materialize
+    # with a bias (its per-example gradients are not kept here)
     (4, 128, 256, 128, False, torch.bfloat16),
     (3, 128, 768, 8, False, torch.bfloat16),
     (64, 1, 1024, 512, False, torch.bfloat16),
     (5, 24, 48, 40, True, torch.float32),
+    (3, 64, 8, 8, True, torch.float32),
 ]
+
+
+def test_cases_cover_every_norm_path():
+    import differentially_private_gb300 as dp
+    paths = [dp.dp_choose_path(T, d_in, d_out) for (_, T, d_in, d_out, _, _) in CASES]
+    assert paths == [dp.DP_PATH_GHOST, dp.DP_PATH_MATERIALIZE, dp.DP_PATH_GHOST, dp.DP_PATH_GHOST,
+                     dp.DP_PATH_MATERIALIZE]
 
 
 def test_static_scratch_matches_context_entry_point_on_consecutive_calls():
@@ -102,4 +111,23 @@ def test_request_beyond_the_static_array_is_refused():
     assert ei.value.status == dp.DP_ERR_SHAPE
     with pytest.raises(dp.DPError) as ei:
         dp.dp_layer_sqnorms_static(None, A, 4, 1, 8, 8, False, dp.DP_BF16, out)
+    assert ei.value.status == dp.DP_ERR_INVALID_ARG
+
+
+def test_wait_that_gave_up_makes_the_norms_nan_and_the_next_call_is_clean():
+    """A tensor-core wait that gives up leaves the partial sums unwritten: the
+    call then reports NaN norms (the caller sees a non-finite norm) instead
+    of summing stale partials.  The test hook records such a timeout exactly
+    as a norm kernel's bounded wait would, without any fault."""
+    import differentially_private_gb300 as dp
+    B, T, d_in, d_out, bias, dt = CASES[0]
+    A, E = _inputs(7, B, T, d_in, d_out, dt)
+    ref = _with_context(A, E, T, d_in, d_out, bias, dt)
+    dp.dp_static_check_wait_timeout(20, torch.cuda.current_stream())
+    got = _static(A, E, T, d_in, d_out, bias, dt)
+    assert np.all(np.isnan(got)), got
+    got = _static(A, E, T, d_in, d_out, bias, dt)
+    assert np.all(np.abs(got - ref) <= NORM_RTOL[dt] * np.abs(ref)), (got, ref)
+    with pytest.raises(dp.DPError) as ei:
+        dp.dp_static_check_wait_timeout(0)
     assert ei.value.status == dp.DP_ERR_INVALID_ARG
