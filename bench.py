@@ -485,25 +485,31 @@ def run_ours(args, w):
         step(pevs[k])
     torch.cuda.synchronize()
     clk = clocks.stop(since)
-    # SM clock at the end of each phase, from the device: a spin of a fixed
+    # SM clock at the end of each phase, from the device: two spins of a fixed
     # number of SM cycles right after the phase, timed with events on the
-    # stream (a third pass of K steps; not part of the timed region)
-    probe_cycles = 200_000
+    # stream; the difference of their times cancels the launch and event
+    # overheads (a third pass of K steps; not part of the timed region)
+    short_cycles, long_cycles = 50_000, 250_000
     probes = {"norm": [], "clip": [], "grad": []}
 
     def probe(phase):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        torch.cuda._sleep(probe_cycles)
-        e1.record(stream)
-        probes[phase].append((e0, e1))
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(stream)
+        torch.cuda._sleep(short_cycles)
+        ev[1].record(stream)
+        torch.cuda._sleep(long_cycles)
+        ev[2].record(stream)
+        probes[phase].append(ev)
 
     for k in range(K):
         flush_l2()
         step(after_phase=probe)
     torch.cuda.synchronize()
-    phase_mhz = {ph: statistics.median([probe_cycles / (a.elapsed_time(b_) * 1e3) for a, b_ in v])
-                 for ph, v in probes.items() if v}
+
+    def mhz(ev):
+        dt_ms = ev[1].elapsed_time(ev[2]) - ev[0].elapsed_time(ev[1])
+        return (long_cycles - short_cycles) / (dt_ms * 1e3) if dt_ms > 0 else float("nan")
+    phase_mhz = {ph: statistics.median([mhz(ev) for ev in v]) for ph, v in probes.items() if v}
     if clk is not None:
         clk["sm_mhz_after_phase"] = phase_mhz
     st = dp.dp_step_status(ctx)

@@ -8,7 +8,13 @@ outputs it can compute one by one:
   sigma = 0) at sampled coordinates: sum_i E_i[:, m]^T A_i[:, n] / L;
 * the noise at sampled coordinates: G(sigma) - G(0) = sigma C z_k / L, both
   runs with the same C.
-Clip factors below one are covered element by element at reduced sizes
+* for the ghost-path workloads 3 and 5, the clipped sum at the workload's
+  own C (clip factors below one, sigma = 0) at sampled coordinates:
+  sum_i c_i E_i[:, m]^T A_i[:, n] / L with c_i from the oracle's norms of
+  all B records (each record's gradient materialized in float64), which
+  exercises the per-record fold of the clipped-sum kernel in the launch
+  shape the bench times.
+Clip factors below one are also covered element by element at reduced sizes
 (test_gpu_parity.py).  No oracle input comes from the GPU path: the GPU only
 supplies the input bytes (drawn by synthetic/) and the outputs under test.
 """
@@ -94,3 +100,36 @@ def test_fullsize_workload(widx):
         diff = to64(gs.grads[l])[p] - to64(gz.grads[l])[p]
         want = sigma * C * philox.normals_at(7, 3, offs[l] + p) / w.B
         assert np.allclose(diff, want, rtol=1e-4, atol=2e-6 * sigma * C / w.B), l
+
+
+@pytest.mark.parametrize("widx", [3, 5])
+def test_fullsize_clipped_sum_at_the_workload_clip_bound(widx):
+    w = by_index(widx)
+    A, E = [], []
+    for i in range(len(w.layers)):
+        a, e = generate_layer(w, i, "cuda")
+        A.append(a)
+        E.append(e)
+    # the oracle's clip factors: every record's gradient materialized in float64
+    n2 = np.zeros(w.B)
+    for r in range(w.B):
+        for l, ly in enumerate(w.layers):
+            n2[r] += dpsgd.record_sqnorm(to64(A[l][r]), to64(E[l][r]), ly.has_bias)
+    c = dpsgd.clip_factors(n2, w.C)
+    assert np.any(c < 1.0)
+    out, _ = _run(w, A, E, w.C, 0.0, 7, 3)
+    assert np.allclose(to64(out.clip), c, rtol=NORM_RTOL["bf16"], atol=0)
+    rng = np.random.default_rng(100 + widx)
+    # the ghost-path layer (the dense one): its sum is the per-record fold
+    for l, ly in enumerate(w.layers):
+        if dpsgd.choose_path(ly.T, ly.d_in, ly.d_out) != dpsgd.GHOST:
+            continue
+        rows = rng.integers(0, ly.d_out, SAMPLED_COORDS)
+        cols = rng.integers(0, ly.d_in, SAMPLED_COORDS)
+        Esub = to64(E[l][:, :, torch.as_tensor(rows, device="cuda")])
+        Asub = to64(A[l][:, :, torch.as_tensor(cols, device="cuda")])
+        q = np.arange(SAMPLED_COORDS)
+        want = dpsgd.clipped_sum_at(Asub, Esub, c, q, q) / w.B
+        got = to64(out.grads[l])[rows * ly.d_in + cols]
+        err = np.linalg.norm(got - want) / np.linalg.norm(want)
+        assert err <= 5e-3, (l, err)
