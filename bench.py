@@ -44,6 +44,8 @@ def parse():
     p.add_argument("--workload", type=int, default=5, help="workload index 1..5 (default: 5, the largest)")
     p.add_argument("--batch", type=int, default=None,
                    help="override the workload's B (smaller cases for profiler captures)")
+    p.add_argument("--int8-forward", action="store_true",
+                   help="time the record-owned LLM.int8 forward on OPT-125M-shaped layers instead")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget-s", type=float, default=12.0)
@@ -610,8 +612,64 @@ def run_ours(args, w):
     return 0
 
 
+def run_int8_forward(args):
+    """The record-owned LLM.int8 forward of a frozen layer on OPT-125M-shaped
+    inputs: 16 records x 256 rows of fp16 activations, d_model 768, with a
+    few outlier entries (|a| >= 6) in a few columns of some records.  Times
+    dp_int8_forward (all its launches) with CUDA events, 10 warm-up and K
+    timed calls, L2 flushed before each; beside it, the same product through
+    torch.matmul in fp16 (cuBLAS on the tensor cores, batched-LLM.int8-free
+    and not record-isolated: context only).  Prints one JSON line per layer."""
+    import torch
+    from differentially_private_gb300.int8 import Int8Linear
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = torch.Generator(device=dev).manual_seed(9)
+    records, rows, K = 16, 256, 768
+    n = records * rows
+    A = torch.randn(n, K, device=dev, generator=g)
+    for r in range(0, records, 3):                      # outliers in a few columns of every third record
+        A[r * rows + 5, 17] = 8.0
+        A[r * rows + 90, 300 + r] = -7.5
+    A = A.half()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for N in (768, 3072):
+        W = (torch.randn(N, K, device=dev, generator=g) * 0.03).half()
+        lin = Int8Linear(W, stream=stream)
+        for _ in range(10):
+            lin(A, rows)
+        torch.cuda.synchronize()
+        times, ref_times = [], []
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            lin(A, rows)
+            e1.record(stream)
+            flush.zero_()
+            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            f0.record(stream)
+            torch.matmul(A, W.t())
+            f1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+            ref_times.append(f0.elapsed_time(f1))
+        t = statistics.median(times)
+        ops = 2 * n * K * N
+        line = {"metric": "record-owned LLM.int8 forward", "layer": f"{K}->{N}", "records": records,
+                "rows_per_record": rows, "us_per_call": t * 1e3, "int8_tops": ops / (t / 1e3) / 1e12,
+                "bytes_moved_min": n * K * 2 + N * K * (1 + 2) + n * N * 2,
+                "torch_fp16_matmul_us": statistics.median(ref_times) * 1e3, "steps": args.steps,
+                "l2": "flushed before every timed call"}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
+    if args.int8_forward:
+        return run_int8_forward(args)
     from synthetic import by_index
     w = by_index(args.workload)
     if args.batch is not None:
