@@ -183,6 +183,24 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     return d;
 }
 
+// The descriptor of the operand `bytes` further on in shared memory (the
+// start-address field holds the address >> 4; shared addresses stay below
+// 2^18, so the field does not carry over).
+__device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
+// Position in a ring of N pipeline stages: the stage and the parity of its
+// current use, advanced without divisions.
+template <uint32_t N>
+struct StageRing {
+    uint32_t s = 0, ph = 0;
+    __device__ __forceinline__ void next() {
+        if (++s == N) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
 // Instruction descriptor of tcgen05.mma.kind::f16 with bf16 A and B and an
 // f32 accumulator; a_mn / b_mn select MN-major (1) or K-major (0) operands.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
@@ -257,6 +275,20 @@ __device__ __forceinline__ void tmem_ld16x4(uint32_t taddr, float (&v)[4][16]) {
         for (int i = 0; i < 16; ++i) v[b][i] = __uint_as_float(r[16 * b + i]);
 }
 
+// The inverse of tmem_ld16: thread t of the warp writes v[0..15] to lane
+// (base lane + t), columns col .. col+15; returns once the writes are done.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+        "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+        "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+        "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+        "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+        : "memory");
+}
 
 // ------------------------------------------------------------ CTA pairs
 // A cluster of two CTAs on neighbouring SMs sharing one tcgen05 MMA

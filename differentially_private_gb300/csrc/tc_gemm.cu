@@ -184,13 +184,13 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_tc(const __grid
     if (!skip && warp == 0) {
         if (lane == 0) {
             uint32_t it = 0;
+            tc::StageRing<kStages> ring;
             for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
                 int mb, nb;
                 tile_coords(tile, p.m_blocks, p.n_blocks, mb, nb);
-                for (int kt = 0; kt < nk; ++kt, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1u;
-                    if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort_flag, p.status)) goto sum_producer_done;
+                for (int kt = 0; kt < nk; ++kt, ++it, ring.next()) {
+                    const uint32_t s = ring.s;
+                    if (!tc::mbar_wait(&sh->empty[s], ring.ph ^ 1u, abort_flag, p.status)) goto sum_producer_done;
                     uint8_t* st = tiles + (size_t)s * kStageBytes;
                     tc::mbar_arrive_expect_tx(&sh->full[s], kStageBytes);
                     const int k0 = kt * kBK;
@@ -212,26 +212,26 @@ __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_tc(const __grid
         }
     } else if (!skip && warp == 1) {
         if (lane == 0) {
-            uint32_t it = 0, rc = 0;
+            uint32_t rc = 0;
+            tc::StageRing<kStages> ring;
+            const uint32_t tiles_u32 = tc::smem_u32(tiles);
             for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++rc) {
                 const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
                 if (!tc::mbar_wait(&sh->p_empty[b], bph ^ 1u, abort_flag, p.status)) break;
                 tc::tc_fence_after();
                 const uint32_t d_tmem = tmem + b * kAccCols;
                 bool ok = true;
-                for (int kt = 0; kt < nk; ++kt, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (it / kStages) & 1u;
-                    if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) { ok = false; break; }
+                for (int kt = 0; kt < nk; ++kt, ring.next()) {
+                    const uint32_t s = ring.s;
+                    if (!tc::mbar_wait(&sh->full[s], ring.ph, abort_flag, p.status)) { ok = false; break; }
                     tc::tc_fence_after();
-                    const uint32_t sa = tc::smem_u32(tiles + (size_t)s * kStageBytes);
-                    const uint32_t sb = sa + kAStage;
+                    const uint32_t sa = tiles_u32 + s * (uint32_t)kStageBytes;
+                    const uint64_t ad = tc::smem_desc(sa, 8192, 1024, tc::SW_128B);
+                    const uint64_t bd = tc::smem_desc(sa + kAStage, 8192, 1024, tc::SW_128B);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t ad = tc::smem_desc(sa + kk * 2048, 8192, 1024, tc::SW_128B);
-                        const uint64_t bd = tc::smem_desc(sb + kk * 2048, 8192, 1024, tc::SW_128B);
-                        tc::mma_bf16(d_tmem, ad, bd, kIdescSum, (kt | kk) != 0);
-                    }
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        tc::mma_bf16(d_tmem, tc::desc_advance(ad, kk * 2048), tc::desc_advance(bd, kk * 2048), kIdescSum,
+                                     (kt | kk) != 0);
                     tc::mma_commit(&sh->empty[s]);
                 }
                 if (!ok) break;
@@ -379,6 +379,40 @@ struct PairSmem {
 };
 static_assert(sizeof(PairSmem) <= 256, "pair barriers exceed their shared-memory slot");
 
+// sigma C z at this thread's 64 coordinates of tile g (row `row` of the
+// CTA's half, the warp's column part), written into the warp's TMEM columns
+// starting at tb: the accumulator of the tile then starts from its noise.
+// Rows past d_out get zeros; columns past d_in get values that are never
+// stored.  All lanes of the warp call it (the TMEM stores are warp-wide).
+__device__ __forceinline__ void write_tile_noise(const LayersParams& p, int g, uint32_t rank, int row, int part,
+                                                 uint32_t tb) {
+    const int l = layer_of(p, g);
+    const SumLayer& ly = p.L[l];
+    int mb, nb;
+    tile_coords(g - p.tile_begin[l], ly.m_blocks, ly.n_blocks, mb, nb);
+    const int64_t m = (int64_t)mb * kPairTile + (int64_t)rank * kHalf + row;
+    const int64_t n0 = (int64_t)nb * kPairTile + part * kColsPerWarp;
+#pragma unroll 1
+    for (int ch = 0; ch < kColsPerWarp / 16; ++ch) {
+        float z[16];
+        if (m < ly.d_out) {
+            float za[8], zb[8];
+            const uint64_t k = (uint64_t)(ly.coord_off + m * ly.d_in + n0 + ch * 16);
+            noise8(p.seed, p.step, k, za);
+            noise8(p.seed, p.step, k + 8, zb);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                z[j] = p.scale * za[j];
+                z[8 + j] = p.scale * zb[j];
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) z[j] = 0.f;
+        }
+        tc::tmem_st16(tb + ch * 16, z);
+    }
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
     k_sum_layers_pair_tc(const __grid_constant__ LayersParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -423,15 +457,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
         if (lane == 0) {
             const uint32_t full0 = tc::mapa_shared(tc::smem_u32(&sh->full[0]), 0);
             uint32_t it = 0;
+            tc::StageRing<kPairStages> ring;
             for (int g = pair; g < ntiles; g += npairs) {
                 const int l = layer_of(p, g);
                 const SumLayer& ly = p.L[l];
                 int mb, nb;
                 tile_coords(g - p.tile_begin[l], ly.m_blocks, ly.n_blocks, mb, nb);
-                for (int kt = 0; kt < p.nk; ++kt, ++it) {
-                    const int s = it % kPairStages;
-                    const uint32_t ph = (it / kPairStages) & 1u;
-                    if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort_flag, p.status)) goto pair_producer_done;
+                for (int kt = 0; kt < p.nk; ++kt, ++it, ring.next()) {
+                    const uint32_t s = ring.s;
+                    if (!tc::mbar_wait(&sh->empty[s], ring.ph ^ 1u, abort_flag, p.status)) goto pair_producer_done;
                     uint8_t* st = tiles + (size_t)s * kPairStageBytes;
                     if (rank == 0) tc::mbar_arrive_expect_tx(&sh->full[s], 2 * kPairStageBytes);
                     const uint32_t fb = full0 + (uint32_t)(s * sizeof(uint64_t));
@@ -458,26 +492,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
         }
     } else if (!skip && warp == 1) {
         if (lane == 0 && rank == 0) {
-            uint32_t it = 0, rc = 0;
+            uint32_t rc = 0;
+            tc::StageRing<kPairStages> ring;
+            const uint32_t tiles_u32 = tc::smem_u32(tiles);
             bool ok = true;
             for (int g = pair; g < ntiles && ok; g += npairs, ++rc) {
                 const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
-                if (!tc::mbar_wait(&sh->p_empty[b], bph ^ 1u, abort_flag, p.status)) break;
+                // buffer 1 has one more phase: the epilogue releases it once at
+                // the start, after writing the pair's second tile's noise into it
+                if (!tc::mbar_wait(&sh->p_empty[b], b ? bph : (bph ^ 1u), abort_flag, p.status)) break;
                 tc::tc_fence_after();
                 const uint32_t d_tmem = tmem + b * kAccCols;
-                for (int kt = 0; kt < p.nk; ++kt, ++it) {
-                    const int s = it % kPairStages;
-                    const uint32_t ph = (it / kPairStages) & 1u;
-                    if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) { ok = false; break; }
+                // every tile but the pair's first accumulates onto its noise
+                const uint32_t acc0 = (rc >= 1 && p.scale != 0.f) ? 1u : 0u;
+                for (int kt = 0; kt < p.nk; ++kt, ring.next()) {
+                    const uint32_t s = ring.s;
+                    if (!tc::mbar_wait(&sh->full[s], ring.ph, abort_flag, p.status)) { ok = false; break; }
                     tc::tc_fence_after();
-                    const uint32_t sa = tc::smem_u32(tiles + (size_t)s * kPairStageBytes);
-                    const uint32_t sb = sa + kPairEStage;
+                    const uint32_t sa = tiles_u32 + s * (uint32_t)kPairStageBytes;
+                    const uint64_t ad = tc::smem_desc(sa, 8192, 1024, tc::SW_128B);
+                    const uint64_t bd = tc::smem_desc(sa + kPairEStage, 8192, 1024, tc::SW_128B);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t ad = tc::smem_desc(sa + kk * 2048, 8192, 1024, tc::SW_128B);
-                        const uint64_t bd = tc::smem_desc(sb + kk * 2048, 8192, 1024, tc::SW_128B);
-                        tc::mma_bf16_pair(d_tmem, ad, bd, kIdescPair, (kt | kk) != 0);
-                    }
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        tc::mma_bf16_pair(d_tmem, tc::desc_advance(ad, kk * 2048), tc::desc_advance(bd, kk * 2048),
+                                          kIdescPair, acc0 | (uint32_t)((kt | kk) != 0));
                     tc::mma_commit_pair(&sh->empty[s], 0x3);
                 }
                 if (!ok) break;
@@ -489,6 +527,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
         const int part = (warp - 2) >> 2;          // columns part*64 .. +63
         const int row = quarter * 32 + lane;
         const uint32_t pe0 = tc::mapa_shared(tc::smem_u32(&sh->p_empty[0]), 0);
+        const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16) + part * kColsPerWarp;
+        const bool noisy = p.scale != 0.f;
+        // the pair's second tile starts from its noise, written into buffer 1
+        // while the tensor cores accumulate the first tile
+        if (noisy && pair + npairs < ntiles) write_tile_noise(p, pair + npairs, rank, row, part, tq + kAccCols);
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_cluster(pe0 + (uint32_t)sizeof(uint64_t));
         uint32_t rc = 0;
         for (int g = pair; g < ntiles; g += npairs, ++rc) {
             const int l = layer_of(p, g);
@@ -497,35 +543,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
             tile_coords(g - p.tile_begin[l], ly.m_blocks, ly.n_blocks, mb, nb);
             const int64_t m = (int64_t)mb * kPairTile + (int64_t)rank * kHalf + row;
             const int64_t n0 = (int64_t)nb * kPairTile + part * kColsPerWarp;
-            float z[kColsPerWarp];
-            if (m < ly.d_out) {
-#pragma unroll
-                for (int ch = 0; ch < kColsPerWarp / 8; ++ch) {
-                    float zc[8];
-                    noise8(p.seed, p.step, (uint64_t)(ly.coord_off + m * ly.d_in + n0 + ch * 8), zc);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) z[ch * 8 + j] = zc[j];
-                }
-            }
             const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
             if (!tc::mbar_wait_warp(&sh->p_full[b], bph, abort_flag, p.status)) break;
             tc::tc_fence_after();
-            const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + part * kColsPerWarp;
+            const uint32_t tb = tq + b * kAccCols;
+            // the pair's first tile takes its noise here, 16 coordinates at a
+            // time, while the tensor cores accumulate the next tile; the others
+            // already hold theirs
+            const bool add_noise = noisy && rc == 0;
             // the warp's 32 rows x 16 columns pass through its staging block so
             // that each store instruction writes 8 rows x 64 contiguous bytes
             const int64_t m_top = m - lane;
             float4* stg = reinterpret_cast<float4*>(staging) + (warp - 2) * 128;
-#pragma unroll
+#pragma unroll 1
             for (int ch = 0; ch < kColsPerWarp / 16; ++ch) {
                 float v[16];
                 tc::tmem_ld16(tb + ch * 16, v);
+                if (add_noise) {
+                    float za[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, zb[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    if (m < ly.d_out) {
+                        const uint64_t k = (uint64_t)(ly.coord_off + m * ly.d_in + n0 + ch * 16);
+                        noise8(p.seed, p.step, k, za);
+                        noise8(p.seed, p.step, k + 8, zb);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        v[j] = v[j] + p.scale * za[j];
+                        v[8 + j] = v[8 + j] + p.scale * zb[j];
+                    }
+                }
 #pragma unroll
                 for (int j4 = 0; j4 < 4; ++j4) {
                     float4 o;
-                    o.x = (v[4 * j4] + p.scale * z[ch * 16 + 4 * j4]) * p.inv_L;
-                    o.y = (v[4 * j4 + 1] + p.scale * z[ch * 16 + 4 * j4 + 1]) * p.inv_L;
-                    o.z = (v[4 * j4 + 2] + p.scale * z[ch * 16 + 4 * j4 + 2]) * p.inv_L;
-                    o.w = (v[4 * j4 + 3] + p.scale * z[ch * 16 + 4 * j4 + 3]) * p.inv_L;
+                    o.x = v[4 * j4] * p.inv_L;
+                    o.y = v[4 * j4 + 1] * p.inv_L;
+                    o.z = v[4 * j4 + 2] * p.inv_L;
+                    o.w = v[4 * j4 + 3] * p.inv_L;
                     stg[lane * 4 + (j4 ^ ((lane >> 1) & 3))] = o;
                 }
                 __syncwarp();
@@ -548,6 +601,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
                 }
                 __syncwarp();
             }
+            // buffer b is read; the tile two places later in the pair's list
+            // reuses it and starts from its noise
+            if (noisy && g + 2 * npairs < ntiles) write_tile_noise(p, g + 2 * npairs, rank, row, part, tb);
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster(pe0 + (uint32_t)(b * sizeof(uint64_t)));
@@ -668,16 +724,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
         if (lane == 0) {
             const uint32_t full0 = tc::mapa_shared(tc::smem_u32(&sh->full[0]), 0);
             uint32_t it = 0;
+            tc::StageRing<kFoldPairStages> ring;
             int cursor = pair;
             Work wk;
             while (next_pair_work(p, ntiles, B, pair, npairs, cursor, wk)) {
                 int mb, nb;
                 tile_coords(wk.tile, p.m_blocks, p.n_blocks, mb, nb);
                 const int kt_end = (int)(wk.r1 * kpr);
-                for (int kt = (int)(wk.r0 * kpr); kt < kt_end; ++kt, ++it) {
-                    const int s = it % kFoldPairStages;
-                    const uint32_t ph = (it / kFoldPairStages) & 1u;
-                    if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort_flag, p.status)) goto fold_pair_producer_done;
+                for (int kt = (int)(wk.r0 * kpr); kt < kt_end; ++kt, ++it, ring.next()) {
+                    const uint32_t s = ring.s;
+                    if (!tc::mbar_wait(&sh->empty[s], ring.ph ^ 1u, abort_flag, p.status)) goto fold_pair_producer_done;
                     uint8_t* st = tiles + (size_t)s * kPairStageBytes;
                     if (rank == 0) tc::mbar_arrive_expect_tx(&sh->full[s], 2 * kPairStageBytes);
                     const uint32_t fb = full0 + (uint32_t)(s * sizeof(uint64_t));
@@ -702,7 +758,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
         }
     } else if (!skip && warp == 1) {
         if (lane == 0 && rank == 0) {
-            uint32_t it = 0, rc = 0;
+            uint32_t rc = 0;
+            tc::StageRing<kFoldPairStages> ring;
+            const uint32_t tiles_u32 = tc::smem_u32(tiles);
             int cursor = pair;
             Work wk;
             while (next_pair_work(p, ntiles, B, pair, npairs, cursor, wk)) {
@@ -712,19 +770,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
                     if (!tc::mbar_wait(&sh->p_empty[b], bph ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     tc::tc_fence_after();
                     const uint32_t d_tmem = tmem + b * kAccCols;
-                    for (int kt = 0; kt < kpr; ++kt, ++it) {
-                        const int s = it % kFoldPairStages;
-                        const uint32_t ph = (it / kFoldPairStages) & 1u;
-                        if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) { ok = false; break; }
+                    for (int kt = 0; kt < kpr; ++kt, ring.next()) {
+                        const uint32_t s = ring.s;
+                        if (!tc::mbar_wait(&sh->full[s], ring.ph, abort_flag, p.status)) { ok = false; break; }
                         tc::tc_fence_after();
-                        const uint32_t sa = tc::smem_u32(tiles + (size_t)s * kPairStageBytes);
-                        const uint32_t sb = sa + kPairEStage;
+                        const uint32_t sa = tiles_u32 + s * (uint32_t)kPairStageBytes;
+                        const uint64_t ad = tc::smem_desc(sa, 8192, 1024, tc::SW_128B);
+                        const uint64_t bd = tc::smem_desc(sa + kPairEStage, 8192, 1024, tc::SW_128B);
 #pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk) {
-                            const uint64_t ad = tc::smem_desc(sa + kk * 2048, 8192, 1024, tc::SW_128B);
-                            const uint64_t bd = tc::smem_desc(sb + kk * 2048, 8192, 1024, tc::SW_128B);
-                            tc::mma_bf16_pair(d_tmem, ad, bd, kIdescPair, (kt | kk) != 0);
-                        }
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            tc::mma_bf16_pair(d_tmem, tc::desc_advance(ad, kk * 2048), tc::desc_advance(bd, kk * 2048),
+                                              kIdescPair, (kt | kk) != 0);
                         tc::mma_commit_pair(&sh->empty[s], 0x3);
                     }
                     if (!ok) break;

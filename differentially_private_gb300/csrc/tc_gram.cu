@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
     if (warp == 0) {
         if (lane == 0) {
             uint32_t it = 0;
+            tc::StageRing<kGStages> ring;
             for (int item = blockIdx.x; item < p.total_items; item += gridDim.x) {
                 const int rec = item / p.tiles_per_rec;
                 int pb, qb;
@@ -112,10 +113,9 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
                 // the left 128 columns of the tile lie below the diagonal when p = 2q + 1:
                 // they are neither loaded nor multiplied
                 const bool left = pb <= 2 * qb;
-                for (int kt = 0; kt < nkA + nkE; ++kt, ++it) {
-                    const int s = it % kGStages;
-                    const uint32_t ph = (it / kGStages) & 1u;
-                    if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort_flag, p.status)) goto gram_producer_done;
+                for (int kt = 0; kt < nkA + nkE; ++kt, ++it, ring.next()) {
+                    const uint32_t s = ring.s;
+                    if (!tc::mbar_wait(&sh->empty[s], ring.ph ^ 1u, abort_flag, p.status)) goto gram_producer_done;
                     uint8_t* st = tiles + (size_t)s * kGStageBytes;
                     const CUtensorMap* tm = kt < nkA ? &p.tmA : &p.tmE;
                     const int k0 = (kt < nkA ? kt : kt - nkA) * kGK;
@@ -131,7 +131,9 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            uint32_t it = 0, lt = 0;
+            uint32_t lt = 0;
+            tc::StageRing<kGStages> ring;
+            const uint32_t tiles_u32 = tc::smem_u32(tiles);
             for (int item = blockIdx.x; item < p.total_items; item += gridDim.x, ++lt) {
                 int pb, qb;
                 gram_tile(item % p.tiles_per_rec, p.np, p.nq, pb, qb);
@@ -143,23 +145,21 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
                 if (!tc::mbar_wait(&sh->acc_empty, (lt & 1u) ^ 1u, abort_flag, p.status)) break;
                 tc::tc_fence_after();
                 bool ok = true;
-                for (int kt = 0; kt < nkA + nkE; ++kt, ++it) {
-                    const int s = it % kGStages;
-                    const uint32_t ph = (it / kGStages) & 1u;
-                    if (!tc::mbar_wait(&sh->full[s], ph, abort_flag, p.status)) { ok = false; break; }
+                for (int kt = 0; kt < nkA + nkE; ++kt, ring.next()) {
+                    const uint32_t s = ring.s;
+                    if (!tc::mbar_wait(&sh->full[s], ring.ph, abort_flag, p.status)) { ok = false; break; }
                     tc::tc_fence_after();
-                    const uint32_t sa = tc::smem_u32(tiles + (size_t)s * kGStageBytes);
-                    const uint32_t sb = sa + kGAStage + boff;
+                    const uint32_t sa = tiles_u32 + s * (uint32_t)kGStageBytes;
                     const bool phaseA = kt < nkA;
                     const uint32_t d_tmem = tmem + (phaseA ? 0u : 256u) + coff;
                     const int kl = phaseA ? kt : kt - nkA;
+                    // K-major, 128B swizzle: 16 features = 32 bytes inside the swizzle row
+                    const uint64_t ad = tc::smem_desc(sa, 16, 1024, tc::SW_128B);
+                    const uint64_t bd = tc::smem_desc(sa + kGAStage + boff, 16, 1024, tc::SW_128B);
 #pragma unroll
-                    for (int kk = 0; kk < kGK / 16; ++kk) {
-                        // K-major, 128B swizzle: 16 features = 32 bytes inside the swizzle row
-                        const uint64_t ad = tc::smem_desc(sa + kk * 32, 16, 1024, tc::SW_128B);
-                        const uint64_t bd = tc::smem_desc(sb + kk * 32, 16, 1024, tc::SW_128B);
-                        tc::mma_bf16(d_tmem, ad, bd, idesc, (kl | kk) != 0);
-                    }
+                    for (int kk = 0; kk < kGK / 16; ++kk)
+                        tc::mma_bf16(d_tmem, tc::desc_advance(ad, kk * 32), tc::desc_advance(bd, kk * 32), idesc,
+                                     (kl | kk) != 0);
                     tc::mma_commit(&sh->empty[s]);
                 }
                 if (!ok) break;
