@@ -332,9 +332,34 @@ def cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
+MANIFEST_KEYS = ("gpu", "compute_capability", "sms", "driver", "cuda", "torch", "library_version",
+                 "library_sha256_16", "B", "T", "C", "sigma", "seed", "step", "L", "dtype", "chooser",
+                 "kernels_per_step", "host")
+
+
+def release_record(w, gpu: dict, lib: dict, kernels_per_step: dict, host: dict) -> dict:
+    """Release record of a run: hardware and software (gpu: name,
+    compute_capability, sms, driver, cuda, torch; lib: version, sha256_16),
+    the step's public parameters (B, T, C, sigma, seed, step, L, dtype), the
+    chooser's decision per layer (exact integer rule T^2 < d_in d_out), the
+    kernels launched per step and the host the oracle ran on."""
+    import differentially_private_gb300 as dp
+    rec = dict(gpu)
+    rec.update({
+        "library_version": lib.get("version"), "library_sha256_16": lib.get("sha256_16"),
+        "B": w.B, "T": [ly.T for ly in w.layers], "C": w.C, "sigma": w.sigma, "seed": w.noise_seed,
+        "step": w.step, "L": float(w.B), "dtype": w.dtype,
+        "chooser": [[ly.name, ly.d_in, ly.d_out, ly.T,
+                     "ghost" if dp.dp_choose_path(ly.T, ly.d_in, ly.d_out) == dp.DP_PATH_GHOST else "materialize"]
+                    for ly in w.layers],
+        "kernels_per_step": kernels_per_step,
+        "host": host,
+    })
+    return {k: rec.get(k) for k in MANIFEST_KEYS}
+
+
 def manifest(w, dp, device, kernels_per_step: dict) -> dict:
-    """Release record of the run: hardware and software, the step's public
-    parameters, the chooser's decision per layer and the kernels launched."""
+    """The release record of this run, collected from the device, the driver and the library."""
     import torch
     props = torch.cuda.get_device_properties(device)
     try:
@@ -342,19 +367,11 @@ def manifest(w, dp, device, kernels_per_step: dict) -> dict:
                               "-i", str(device.index or 0)], capture_output=True, text=True, timeout=20).stdout.strip()
     except (OSError, subprocess.SubprocessError):
         drv = None
-    lib_sha = hashlib.sha256(open(dp.LIB_PATH, "rb").read()).hexdigest()[:16]
-    return {
-        "gpu": props.name, "compute_capability": f"{props.major}.{props.minor}", "sms": props.multi_processor_count,
-        "driver": drv, "cuda": torch.version.cuda, "torch": torch.__version__,
-        "library_version": dp.dp_version(), "library_sha256_16": lib_sha,
-        "B": w.B, "T": [ly.T for ly in w.layers], "C": w.C, "sigma": w.sigma, "seed": w.noise_seed,
-        "step": w.step, "L": float(w.B), "dtype": w.dtype,
-        "chooser": [[ly.name, ly.d_in, ly.d_out, ly.T,
-                     "ghost" if dp.dp_choose_path(ly.T, ly.d_in, ly.d_out) == dp.DP_PATH_GHOST else "materialize"]
-                    for ly in w.layers],
-        "kernels_per_step": kernels_per_step,
-        "host": {"cores": len(os.sched_getaffinity(0)), "cpu_model": cpu_model()},
-    }
+    gpu = {"gpu": props.name, "compute_capability": f"{props.major}.{props.minor}",
+           "sms": props.multi_processor_count, "driver": drv, "cuda": torch.version.cuda, "torch": torch.__version__}
+    lib = {"version": dp.dp_version(), "sha256_16": hashlib.sha256(open(dp.LIB_PATH, "rb").read()).hexdigest()[:16]}
+    host = {"cores": len(os.sched_getaffinity(0)), "cpu_model": cpu_model()}
+    return release_record(w, gpu, lib, kernels_per_step, host)
 
 
 # ------------------------------------------------------------------- arms

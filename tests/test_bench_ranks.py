@@ -101,3 +101,20 @@ def test_dominant_kernel_names_the_runtime_choice():
             got = bench.dominant_kernel(w, phase, bound)
             assert got == name, (i, phase, bound, got)
             assert got in defined, (got, sorted(defined))
+
+
+def test_release_record_keys_and_chooser():
+    """The release record each bench line carries: every key, the public step
+    parameters of the workload and the chooser's decision per layer."""
+    from synthetic import by_index
+    w = by_index(5)
+    gpu = {"gpu": "NVIDIA GB300", "compute_capability": "10.3", "sms": 152, "driver": "580", "cuda": "13.0",
+           "torch": "2.x"}
+    rec = bench.release_record(w, gpu, {"version": 100, "sha256_16": "0" * 16},
+                               {"k_ghost_gram_tc": 1.0}, {"cores": 16, "cpu_model": "cpu"})
+    assert tuple(rec) == bench.MANIFEST_KEYS
+    assert all(rec[k] is not None for k in bench.MANIFEST_KEYS)
+    assert (rec["B"], rec["C"], rec["sigma"], rec["seed"], rec["step"], rec["L"]) == (32, 1.0, 1.0, 0, 0, 32.0)
+    paths = [c[4] for c in rec["chooser"]]
+    assert paths == ["materialize"] * 12 + ["ghost"]
+    assert rec["chooser"][-1][:4] == ["down_proj", 14336, 4096, 2048]
