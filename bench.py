@@ -46,6 +46,8 @@ def parse():
                    help="override the workload's B (smaller cases for profiler captures)")
     p.add_argument("--int8-forward", action="store_true",
                    help="time the record-owned LLM.int8 forward on OPT-125M-shaped layers instead")
+    p.add_argument("--floors", action="store_true",
+                   help="also time a device copy of the step's input bytes (the read floor at this size)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget-s", type=float, default=12.0)
@@ -573,6 +575,30 @@ def run_ours(args, w):
     roof["peak_source"] = ("derived: 152 SMs x 128 fp32 lanes x 2 flops x max SM clock"
                            if roof["bound"] == "alu" else peaks["source"])
 
+    # what a plain copy of the step's input bytes reaches at this size (a
+    # device-to-device copy of the input arena, L2 flushed first): the
+    # fraction of the peak a launch of this size can reach, outside the library
+    floors = None
+    if args.floors:
+        dst = torch.empty_like(arena)
+        cp = []
+        for _ in range(max(3, args.warmup)):
+            dst.copy_(arena)
+        for _ in range(K):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dst.copy_(arena)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            cp.append(e0.elapsed_time(e1))
+        del dst
+        t_cp = statistics.median(cp)
+        eff = 2 * arena.numel() / (t_cp / 1e3) / 1e9 / peaks["hbm_gbs"]
+        floors = {"input_bytes": arena.numel(), "copy_us": t_cp * 1e3, "copy_frac_of_peak": eff,
+                  "read_floor_us": arena.numel() / (peaks["hbm_gbs"] * 1e9 * eff) * 1e6,
+                  "ideal_read_us": arena.numel() / (peaks["hbm_gbs"] * 1e9) * 1e6}
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -621,6 +647,7 @@ def run_ours(args, w):
             "phases_ms": {"norm": mn, "clip": statistics.mean(clip_ms), "grad": mg,
                           "step_with_phase_events": statistics.mean([e[0].elapsed_time(e[3]) for e in pevs])},
             "manifest": manifest(w, dp, device, per_kernel),
+            **({"floors": floors} if floors is not None else {}),
         }
         print(json.dumps(line), flush=True)
     pg.close()

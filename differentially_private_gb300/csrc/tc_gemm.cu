@@ -349,23 +349,34 @@ __device__ __forceinline__ int layer_of(const LayersParams& p, int g) {
 // buffers, so a tile's epilogue overlaps the next tile's MMAs).  Per SM the
 // tensor cores do the same work per K step as a 128 x 256 tile of one CTA
 // but stage two thirds of its bytes, which leaves room for six stages and a
-// 2 KB staging block per epilogue warp.  The epilogue draws the tile's noise
-// while the tensor cores accumulate, then writes G = (S + sigma C z) / L
-// through its staging block: a store instruction covers 8 rows x 64
-// contiguous bytes instead of 32 rows x 16 bytes, four times fewer (and
-// whole-sector) L2 writes.
+// 2 KB staging block per epilogue warp.  Every tile of a pair but its first
+// starts from its noise: the epilogue warps write sigma C z into the tile's
+// TMEM buffer while the tensor cores accumulate the tile before it, and the
+// MMAs accumulate onto it; the first tile's noise is drawn in its epilogue,
+// 16 columns at a time, while the tensor cores accumulate the second.  The
+// epilogue writes G = S / L through its staging block: a store instruction
+// covers 8 rows x 64 contiguous bytes instead of 32 rows x 16 bytes, four
+// times fewer (and whole-sector) L2 writes.
 //
 // Barriers: rank 0's full[s] counts both CTAs' copies (its producer expects
 // the bytes of both halves); the MMA commits arrive on empty[s], p_full[b]
 // and drain of both CTAs; the epilogue warps of both CTAs arrive on rank 0's
 // p_empty[b].
+//
+// Eight epilogue warps, two per TMEM lane quarter, each owning 128 of the 256
+// columns: with fewer warps drawing noise next to them, the TMA and MMA warps
+// on the same schedulers keep pace (on the 1024 -> 4096 -> 1024 MLP with 4096
+// records, sixteen warps took 61.4 us for both sums, eight take 59.4 us).
+constexpr int kLEpiWarps = 8;
+constexpr int kLColsPerWarp = kBN / (kLEpiWarps / 4);
+constexpr int kLThreads = 32 * (2 + kLEpiWarps);
 constexpr int kPairStages = 6;
 constexpr int kHalf = 128;                    // M rows and N columns staged per CTA
 constexpr int kPairTile = 2 * kHalf;          // output tile of the pair: 256 x 256
 constexpr int kPairEStage = kHalf * kBK * 2;  // 2 boxes of 64 columns x 64 rows
 constexpr int kPairStageBytes = 2 * kPairEStage;
 constexpr uint32_t kIdescPair = tc::idesc_bf16_f32(kPairTile, kPairTile, 1, 1);
-constexpr int kStagingBytes = kEpiWarps * 32 * 16 * 4;  // 32 rows x 16 fp32 per epilogue warp
+constexpr int kStagingBytes = kLEpiWarps * 32 * 16 * 4;  // 32 rows x 16 fp32 per epilogue warp
 constexpr size_t kPairSmem = 1024 + (size_t)kPairStages * kPairStageBytes + kStagingBytes + 256;
 
 struct PairSmem {
@@ -379,7 +390,8 @@ struct PairSmem {
 };
 static_assert(sizeof(PairSmem) <= 256, "pair barriers exceed their shared-memory slot");
 
-// sigma C z at this thread's 64 coordinates of tile g (row `row` of the
+
+// sigma C z at this thread's 128 coordinates of tile g (row `row` of the
 // CTA's half, the warp's column part), written into the warp's TMEM columns
 // starting at tb: the accumulator of the tile then starts from its noise.
 // Rows past d_out get zeros; columns past d_in get values that are never
@@ -391,9 +403,9 @@ __device__ __forceinline__ void write_tile_noise(const LayersParams& p, int g, u
     int mb, nb;
     tile_coords(g - p.tile_begin[l], ly.m_blocks, ly.n_blocks, mb, nb);
     const int64_t m = (int64_t)mb * kPairTile + (int64_t)rank * kHalf + row;
-    const int64_t n0 = (int64_t)nb * kPairTile + part * kColsPerWarp;
+    const int64_t n0 = (int64_t)nb * kPairTile + part * kLColsPerWarp;
 #pragma unroll 1
-    for (int ch = 0; ch < kColsPerWarp / 16; ++ch) {
+    for (int ch = 0; ch < kLColsPerWarp / 16; ++ch) {
         float z[16];
         if (m < ly.d_out) {
             float za[8], zb[8];
@@ -413,7 +425,7 @@ __device__ __forceinline__ void write_tile_noise(const LayersParams& p, int g, u
     }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLThreads, 1)
     k_sum_layers_pair_tc(const __grid_constant__ LayersParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -432,7 +444,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&sh->p_full[b], 1);
-            tc::mbar_init(&sh->p_empty[b], 2 * kEpiWarps);
+            tc::mbar_init(&sh->p_empty[b], 2 * kLEpiWarps);
         }
         tc::mbar_init(&sh->drain, 1);
         sh->abort_flag = 0;
@@ -527,7 +539,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
         const int part = (warp - 2) >> 2;          // columns part*64 .. +63
         const int row = quarter * 32 + lane;
         const uint32_t pe0 = tc::mapa_shared(tc::smem_u32(&sh->p_empty[0]), 0);
-        const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16) + part * kColsPerWarp;
+        const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16) + part * kLColsPerWarp;
         const bool noisy = p.scale != 0.f;
         // the pair's second tile starts from its noise, written into buffer 1
         // while the tensor cores accumulate the first tile
@@ -542,7 +554,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
             int mb, nb;
             tile_coords(g - p.tile_begin[l], ly.m_blocks, ly.n_blocks, mb, nb);
             const int64_t m = (int64_t)mb * kPairTile + (int64_t)rank * kHalf + row;
-            const int64_t n0 = (int64_t)nb * kPairTile + part * kColsPerWarp;
+            const int64_t n0 = (int64_t)nb * kPairTile + part * kLColsPerWarp;
             const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
             if (!tc::mbar_wait_warp(&sh->p_full[b], bph, abort_flag, p.status)) break;
             tc::tc_fence_after();
@@ -556,7 +568,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
             const int64_t m_top = m - lane;
             float4* stg = reinterpret_cast<float4*>(staging) + (warp - 2) * 128;
 #pragma unroll 1
-            for (int ch = 0; ch < kColsPerWarp / 16; ++ch) {
+            for (int ch = 0; ch < kLColsPerWarp / 16; ++ch) {
                 float v[16];
                 tc::tmem_ld16(tb + ch * 16, v);
                 if (add_noise) {
@@ -982,7 +994,7 @@ int device_sm_count() { return sm_count_cached(); }
 // Clusters of two CTAs of a pair kernel resident at once on the current
 // device (queried once per device and kernel, kept in `cache`; half the SM
 // count if the query fails).
-static int pair_clusters_cached(const void* kern, int smem, std::atomic<int> (&cache)[64]) {
+static int pair_clusters_cached(const void* kern, int threads, int smem, std::atomic<int> (&cache)[64]) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64) {
@@ -991,7 +1003,7 @@ static int pair_clusters_cached(const void* kern, int smem, std::atomic<int> (&c
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (unsigned)sm_count_cached());
-    cfg.blockDim = dim3(kFoldThreads);
+    cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = (size_t)smem;
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
@@ -1039,7 +1051,7 @@ static cudaError_t launch_fold_pair(const GradTask& t, const float* c, unsigned*
     p.step = sc.step;
     const int ntiles = p.m_blocks * p.n_blocks;
     static std::atomic<int> clusters[64];
-    const int pairs = pair_clusters_cached(kern, (int)kFoldPairSmem, clusters);
+    const int pairs = pair_clusters_cached(kern, kFoldThreads, (int)kFoldPairSmem, clusters);
     int npairs = ntiles < pairs ? ntiles : pairs;
     p.full_tiles = ntiles;
     p.nsplit = 1;
@@ -1160,9 +1172,9 @@ cudaError_t launch_sum_layers_tc(const GradTask* tasks, int n, unsigned* status,
     p.seed = sc.seed;
     p.step = sc.step;
     static std::atomic<int> clusters[64];
-    const int pairs = pair_clusters_cached(kern, (int)kPairSmem, clusters);
+    const int pairs = pair_clusters_cached(kern, kLThreads, (int)kPairSmem, clusters);
     const int grid = 2 * (tiles < pairs ? tiles : pairs);
-    const cudaError_t e = launch_dependent(k_sum_layers_pair_tc, dim3(grid), dim3(kFoldThreads), kPairSmem, s, p);
+    const cudaError_t e = launch_dependent(k_sum_layers_pair_tc, dim3(grid), dim3(kLThreads), kPairSmem, s, p);
     count_launch(KL_SUM_LAYERS_PAIR_TC);
     return e;
 }
