@@ -129,7 +129,8 @@ __device__ __forceinline__ void noise8(uint64_t seed, uint64_t step, uint64_t kb
 
 // S[4q .. 4q+3] += sigma C z at this thread's coordinates k0 + 4q .. k0 + 4q + 3
 constexpr int kNoiseChunks = kColsPerWarp / 4;
-__device__ __forceinline__ void add_noise_chunk(const SumParams& p, uint64_t k0, int q, float (&S)[kColsPerWarp]) {
+template <int NC>
+__device__ __forceinline__ void add_noise_chunk_n(const SumParams& p, uint64_t k0, int q, float (&S)[NC]) {
     const uint64_t k = k0 + 4u * (uint64_t)q;
     float z[4];
     if ((k & 3u) == 0) {
@@ -139,11 +140,14 @@ __device__ __forceinline__ void add_noise_chunk(const SumParams& p, uint64_t k0,
         for (int j = 0; j < 4; ++j) z[j] = noise_at(p.seed, p.step, k + j);
     }
 #pragma unroll
-    for (int qq = 0; qq < kNoiseChunks; ++qq)
+    for (int qq = 0; qq < NC / 4; ++qq)
         if (qq == q) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) S[4 * qq + j] = fmaf(p.scale, z[j], S[4 * qq + j]);
         }
+}
+__device__ __forceinline__ void add_noise_chunk(const SumParams& p, uint64_t k0, int q, float (&S)[kColsPerWarp]) {
+    add_noise_chunk_n<kColsPerWarp>(p, k0, q, S);
 }
 
 __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_tc(const __grid_constant__ SumParams p) {
@@ -650,6 +654,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLThreads, 1)
 // CTA of a pair keeps its half's partial sum in its own scratch slot, and the
 // arrival counters are per (tile, half), so the CTA arriving last among the
 // ranges of a half adds that half's slots in range order.
+//
+// Eight epilogue warps, two per TMEM lane quarter, each folding 128 of the
+// 256 columns into 128 fp32 registers (with sixteen warps of 64 columns the
+// dense 4096 x 4096 layer's sum took 2.8% longer); the tile's noise joins S
+// four columns at a time after each of the first 32 records.
+constexpr int kFEpiWarps = 8;
+constexpr int kFColsPerWarp = kBN / (kFEpiWarps / 4);
+constexpr int kFThreads = 32 * (2 + kFEpiWarps);
+constexpr int kFNoiseChunks = kFColsPerWarp / 4;
 constexpr int kFoldPairStages = 6;
 
 struct FoldPairSmem {
@@ -691,7 +704,7 @@ __device__ __forceinline__ bool next_pair_work(const SumParams& p, int ntiles, i
     return true;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFThreads, 1)
     k_clipped_sum_fold_pair_tc(const __grid_constant__ SumParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -711,10 +724,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&sh->p_full[b], 1);
-            tc::mbar_init(&sh->p_empty[b], 2 * kEpiWarps);
+            tc::mbar_init(&sh->p_empty[b], 2 * kFEpiWarps);
         }
         tc::mbar_init(&sh->drain, 1);
-        tc::mbar_init(&sh->fix_in, 32 * kEpiWarps);
+        tc::mbar_init(&sh->fix_in, 32 * kFEpiWarps);
         tc::mbar_init(&sh->fix_out, 1);
         sh->abort_flag = 0;
         sh->fix_last = 0;
@@ -813,13 +826,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
             int mb, nb;
             tile_coords(wk.tile, p.m_blocks, p.n_blocks, mb, nb);
             const int64_t m = (int64_t)mb * kPairTile + (int64_t)rank * kHalf + row;
-            const int64_t n0 = (int64_t)nb * kPairTile + part * kColsPerWarp;
+            const int64_t n0 = (int64_t)nb * kPairTile + part * kFColsPerWarp;
             const uint64_t k0 = (uint64_t)(p.coord_off + m * p.d_in + n0);   // this thread's first coordinate
             // the range holding the tile's first record also carries its noise
             const bool noisy = wk.r0 == 0 && m < p.d_out;
-            float S[kColsPerWarp];
+            float S[kFColsPerWarp];
 #pragma unroll
-            for (int j = 0; j < kColsPerWarp; ++j) S[j] = 0.f;
+            for (int j = 0; j < kFColsPerWarp; ++j) S[j] = 0.f;
             bool ok = true;
             for (int64_t i = wk.r0; i < wk.r1; ++i, ++rc) {
                 const uint32_t b = rc & 1u, bph = (rc >> 1) & 1u;
@@ -827,9 +840,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
                 tc::tc_fence_after();
                 const float ci = __ldca(p.c + i);
                 const uint32_t tb =
-                    tmem + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + part * kColsPerWarp;
+                    tmem + ((uint32_t)(quarter * 32) << 16) + b * kAccCols + part * kFColsPerWarp;
 #pragma unroll
-                for (int ch = 0; ch < kColsPerWarp / 16; ++ch) {
+                for (int ch = 0; ch < kFColsPerWarp / 16; ++ch) {
                     float v[16];
                     tc::tmem_ld16(tb + ch * 16, v);
 #pragma unroll
@@ -838,19 +851,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive_cluster(pe0 + (uint32_t)(b * sizeof(uint64_t)));
-                if (noisy && i < kNoiseChunks) add_noise_chunk(p, k0, (int)i, S);
+                if (noisy && i < kFNoiseChunks) add_noise_chunk_n<kFColsPerWarp>(p, k0, (int)i, S);
             }
             if (!ok) break;
             if (noisy)
-                for (int q = (int)(wk.r1 < kNoiseChunks ? wk.r1 : kNoiseChunks); q < kNoiseChunks; ++q)
-                    add_noise_chunk(p, k0, q, S);
+                for (int q = (int)(wk.r1 < kFNoiseChunks ? wk.r1 : kFNoiseChunks); q < kFNoiseChunks; ++q)
+                    add_noise_chunk_n<kFColsPerWarp>(p, k0, q, S);
             if (wk.seg >= 0) {
                 // split tile: this half's partial sum to the CTA's slot, then the half's counter
                 const int R = ntiles - p.full_tiles;
                 const int r = wk.tile - p.full_tiles;
                 float* slot = p.scratch + (size_t)blockIdx.x * (kBM * kBN);
 #pragma unroll
-                for (int j = 0; j < kColsPerWarp; ++j) slot[(size_t)(part * kColsPerWarp + j) * kBM + row] = S[j];
+                for (int j = 0; j < kFColsPerWarp; ++j) slot[(size_t)(part * kFColsPerWarp + j) * kBM + row] = S[j];
                 __threadfence();
                 tc::mbar_arrive(&sh->fix_in);
                 if (warp == 2 && lane == 0) {
@@ -879,17 +892,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFoldThreads, 1)
                 if (!*(volatile int*)&sh->fix_last) continue;
                 // last arrival for this half: the ranges' partial sums in range order
 #pragma unroll
-                for (int j = 0; j < kColsPerWarp; ++j) S[j] = 0.f;
+                for (int j = 0; j < kFColsPerWarp; ++j) S[j] = 0.f;
                 for (int sg = 0; sg < p.nsplit; ++sg) {
                     const float* src = p.scratch + (size_t)(2 * (r + sg * R) + (int)rank) * (kBM * kBN);
 #pragma unroll
-                    for (int j = 0; j < kColsPerWarp; ++j)
-                        S[j] += __ldcg(src + (size_t)(part * kColsPerWarp + j) * kBM + row);
+                    for (int j = 0; j < kFColsPerWarp; ++j)
+                        S[j] += __ldcg(src + (size_t)(part * kFColsPerWarp + j) * kBM + row);
                 }
             }
             if (m < p.d_out) {
 #pragma unroll
-                for (int ch = 0; ch < kColsPerWarp / 8; ++ch) {
+                for (int ch = 0; ch < kFColsPerWarp / 8; ++ch) {
                     const int64_t n = n0 + ch * 8;
                     if (n >= p.d_in) continue;
                     float* out = p.G + m * p.d_in + n;
@@ -1051,7 +1064,7 @@ static cudaError_t launch_fold_pair(const GradTask& t, const float* c, unsigned*
     p.step = sc.step;
     const int ntiles = p.m_blocks * p.n_blocks;
     static std::atomic<int> clusters[64];
-    const int pairs = pair_clusters_cached(kern, kFoldThreads, (int)kFoldPairSmem, clusters);
+    const int pairs = pair_clusters_cached(kern, kFThreads, (int)kFoldPairSmem, clusters);
     int npairs = ntiles < pairs ? ntiles : pairs;
     p.full_tiles = ntiles;
     p.nsplit = 1;
@@ -1078,7 +1091,7 @@ static cudaError_t launch_fold_pair(const GradTask& t, const float* c, unsigned*
             npairs = pairs;
         }
     }
-    const cudaError_t e = launch_dependent(k_clipped_sum_fold_pair_tc, dim3(2 * npairs), dim3(kFoldThreads), kFoldPairSmem, s, p);
+    const cudaError_t e = launch_dependent(k_clipped_sum_fold_pair_tc, dim3(2 * npairs), dim3(kFThreads), kFoldPairSmem, s, p);
     count_launch(KL_CLIPPED_SUM_FOLD_PAIR_TC);
     return e;
 }
