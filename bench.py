@@ -661,7 +661,8 @@ def run_int8_forward(args):
     inputs: 16 records x 256 rows of fp16 activations, d_model 768, with a
     few outlier entries (|a| >= 6) in a few columns of some records.  Times
     dp_int8_forward (all its launches) with CUDA events, 10 warm-up and K
-    timed calls, L2 flushed before each; beside it, the same product through
+    timed calls, L2 flushed before each and the GPU kept busy while the host
+    enqueues them (the host's enqueue time is reported apart); beside it, the same product through
     torch.matmul in fp16 (cuBLAS on the tensor cores, batched-LLM.int8-free
     and not record-isolated: context only).  Prints one JSON line per layer."""
     import torch
@@ -677,6 +678,14 @@ def run_int8_forward(args):
         A[r * rows + 90, 300 + r] = -7.5
     A = A.half()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        # write a buffer larger than L2, then read another one (the write-back
+        # of the dirty lines happens here, not inside the timed calls)
+        flush.zero_()
+        flush_rd.sum()
+
     stream = torch.cuda.current_stream(dev)
     for N in (768, 3072):
         W = (torch.randn(N, K, device=dev, generator=g) * 0.03).half()
@@ -684,14 +693,20 @@ def run_int8_forward(args):
         for _ in range(10):
             lin(A, rows)
         torch.cuda.synchronize()
-        times, ref_times = [], []
+        times, ref_times, host = [], [], []
         for _ in range(args.steps):
-            flush.zero_()
+            # a spin first, so that the GPU time between the events is the
+            # calls' own and not the host's time to enqueue them
+            flush_l2()
+            torch.cuda._sleep(2_000_000)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
+            h0 = time.perf_counter()
             lin(A, rows)
+            host.append(time.perf_counter() - h0)
             e1.record(stream)
-            flush.zero_()
+            flush_l2()
+            torch.cuda._sleep(2_000_000)
             f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             f0.record(stream)
             torch.matmul(A, W.t())
@@ -704,9 +719,37 @@ def run_int8_forward(args):
         line = {"metric": "record-owned LLM.int8 forward", "layer": f"{K}->{N}", "records": records,
                 "rows_per_record": rows, "us_per_call": t * 1e3, "int8_tops": ops / (t / 1e3) / 1e12,
                 "bytes_moved_min": n * K * 2 + N * K * (1 + 2) + n * N * 2,
+                "host_enqueue_us": statistics.median(host) * 1e6,
                 "torch_fp16_matmul_us": statistics.median(ref_times) * 1e3, "steps": args.steps,
                 "l2": "flushed before every timed call"}
         print(json.dumps(line), flush=True)
+    # the GPU's own int8 and bf16 tensor-core rates on a large product (cuBLAS
+    # through torch: context for the int8 forward, which runs on dp4a)
+    rates = {}
+    m = 8192
+    for name, mk in (("int8", lambda: (torch.randint(-127, 128, (m, m), dtype=torch.int8, device=dev),
+                                       torch.randint(-127, 128, (m, m), dtype=torch.int8, device=dev).t())),
+                     ("bf16", lambda: (torch.randn(m, m, device=dev, dtype=torch.bfloat16),
+                                       torch.randn(m, m, device=dev, dtype=torch.bfloat16).t()))):
+        try:
+            a, bm = mk()
+            f = torch._int_mm if name == "int8" else torch.matmul
+            for _ in range(3):
+                f(a, bm)
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(10):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                f(a, bm)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            rates[name + "_tops"] = 2 * m ** 3 / (min(ts) / 1e3) / 1e12
+            del a, bm
+        except (RuntimeError, AttributeError) as exc:
+            rates[name + "_tops"] = f"unavailable: {type(exc).__name__}"
+    print(json.dumps({"metric": "tensor-core rate, 8192^3 product (torch/cuBLAS), best of 10", **rates}), flush=True)
     return 0
 
 

@@ -96,7 +96,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "dp_layer_sqnorms_static": (i32, [vp, vp, i64, i64, i64, i64, i32, i32, vp, vp]),
         "dp_pack_groups": (i32, [vp, vp, i64, i64, i64, i32, vp, i64, i64, vp]),
         "dp_int8_quantize_weight": (i32, [vp, i64, i64, vp, vp, vp, vp]),
-        "dp_int8_workspace_bytes": (i64, [i64, i64, i64]),
+        "dp_int8_workspace_bytes": (i64, [i64, i64, i64, i64]),
         "dp_int8_forward": (i32, [vp, i64, i64, i64, vp, vp, vp, i64, c.c_float, i32, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
@@ -291,8 +291,8 @@ def dp_int8_quantize_weight(W, N: int, K: int, Wq, sW, What, stream=None) -> Non
                                                   _stream(stream)), "dp_int8_quantize_weight")
 
 
-def dp_int8_workspace_bytes(n: int, K: int, rows_per_record: int) -> int:
-    return int(load_library().dp_int8_workspace_bytes(int(n), int(K), int(rows_per_record)))
+def dp_int8_workspace_bytes(n: int, K: int, N: int, rows_per_record: int) -> int:
+    return int(load_library().dp_int8_workspace_bytes(int(n), int(K), int(N), int(rows_per_record)))
 
 
 def dp_int8_forward(A, n: int, K: int, rows_per_record: int, Wq, sW, What, N: int, tau: float, record_owned: bool,

@@ -10,16 +10,27 @@
 //
 // so that a row's output depends only on its own record's data (record
 // isolation, Proposition 2) in record-owned mode, and on the whole batch in
-// the batched mode LLM.int8 ships with.  The integer product is exact
-// (int32, dp4a on the CUDA cores: GB300's int8 tensor rate is low and the
-// layer is a producer off the gradient hot path); the correction runs over
-// the set's columns in ascending order, one fused multiply-add each.
+// the batched mode LLM.int8 ships with.  The correction runs over the set's
+// columns in ascending order, one fused multiply-add each.
+//
+// The integer product Q Wq^T is exact.  On GB300 the int8 tensor rate is a
+// small fraction of the bf16 one (cuBLAS: 155 against 1904 dense TOPS on an
+// 8192^3 product), so the product runs on the bf16 tensor cores instead:
+// int8 codes are exact in bf16, their products (at most 127^2 = 16129) are
+// exact in the fp32 accumulator, and so is every partial sum of at most 1024
+// products (below 2^24).  K is cut into chunks of 1024 accumulated in their
+// own TMEM columns; the epilogue adds the chunks in int32.  Layers with K
+// above 4096 take a dp4a kernel on the CUDA cores.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "../../include/dp_clip.h"
+#include "common.cuh"
 #include "internal.h"
+#include "launch.cuh"
+#include "tc_common.cuh"
 
 namespace {
 
@@ -44,37 +55,60 @@ __global__ void k_int8_quantize_weight(const __half* __restrict__ W, int64_t N, 
     if (lane == 0) sW[n] = m;
 }
 
-// per (record, 32-column word): bit set when some row of the record has |a| >= tau
-__global__ void k_int8_sets(const __half* __restrict__ A, int64_t K, int64_t rows, int64_t words, float tau,
-                            uint32_t* __restrict__ sets, uint32_t* __restrict__ uni) {
-    const int64_t r = blockIdx.y;
-    const int lane = threadIdx.x & 31;
-    const int64_t word = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (word >= words) return;
-    const int64_t j = word * 32 + lane;
-    bool hit = false;
-    if (j < K)
-        for (int64_t i = r * rows; i < (r + 1) * rows; ++i) hit |= fabsf(__half2float(A[i * K + j])) >= tau;
-    const uint32_t bits = __ballot_sync(0xffffffffu, hit);
-    if (lane == 0) {
-        sets[r * words + word] = bits;
-        if (bits) atomicOr(uni + word, bits);
-    }
-}
-
-// row-local scales: max |a| over the row's entries below tau
-__global__ void k_int8_scales(const __half* __restrict__ A, int64_t n, int64_t K, float tau, float* __restrict__ s) {
+// One warp per row i: the row's outlier bits (|a| >= tau) per 32-column word,
+// ORed into its record's set and into the union (only nonzero words: the
+// sets and the union start at zero), and its scale s_i = max |a| over the
+// entries below tau.  Lane l reads 8-column groups l, l + 32, ...; the four
+// lanes of a word combine their bits by shuffles.
+__global__ void k_int8_rowscan(const __half* __restrict__ A, int64_t n, int64_t K, int64_t rows, int64_t words,
+                               float tau, uint32_t* __restrict__ sets, uint32_t* __restrict__ uni,
+                               float* __restrict__ scales) {
     const int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (i >= n) return;
+    const __half* a = A + i * K;
+    uint32_t* set = sets + (i / rows) * words;
+    const int64_t groups = (K + 7) / 8;
+    const bool vec = (K & 7) == 0;
     float m = 0.f;
-    for (int64_t j = lane; j < K; j += 32) {
-        const float a = fabsf(__half2float(A[i * K + j]));
-        if (a < tau) m = fmaxf(m, a);
+    for (int64_t g0 = 0; g0 < groups; g0 += 32) {
+        const int64_t g = g0 + lane;
+        uint32_t bits = 0u;
+        if (g < groups) {
+            float v[8];
+            if (vec) {
+                const uint4 raw = __ldg(reinterpret_cast<const uint4*>(a + g * 8));
+                const __half2* h = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f = __half22float2(h[q]);
+                    v[2 * q] = f.x;
+                    v[2 * q + 1] = f.y;
+                }
+            } else {
+#pragma unroll
+                for (int b = 0; b < 8; ++b) v[b] = g * 8 + b < K ? __half2float(a[g * 8 + b]) : 0.f;
+            }
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                const float x = fabsf(v[b]);
+                if (x >= tau) bits |= 1u << b;
+                else m = fmaxf(m, x);
+            }
+        }
+        // the group's 8 bits at their place in the 32-column word, ORed over the word's 4 lanes
+        bits <<= 8 * (lane & 3);
+        bits |= __shfl_xor_sync(0xffffffffu, bits, 1);
+        bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
+        const int64_t w = g / 4;
+        if ((lane & 3) == 0 && bits && w < words) {
+            atomicOr(set + w, bits);
+            atomicOr(uni + w, bits);
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) s[i] = m;
+    if (lane == 0) scales[i] = m;
 }
 
 struct Int8Args {
@@ -176,14 +210,315 @@ __global__ void __launch_bounds__(256) k_int8_gemm(const Int8Args p) {
     }
 }
 
+// ------------------------------------------------ tensor-core integer product
+// Workspace of one forward call (every region 256-byte aligned): the outlier
+// sets, the row scales, the sets as ascending column lists, a status word,
+// and the bf16 codes of A and of the weights, rows padded to Kp = K rounded
+// up to 8 (16-byte rows for TMA).
+struct Int8Workspace {
+    int64_t sets, scales, lists, status, qa, qw, total, Kp;
+    static int64_t pad(int64_t b) { return (b + 255) / 256 * 256; }
+    static Int8Workspace layout(int64_t n, int64_t K, int64_t N, int64_t records) {
+        Int8Workspace w;
+        const int64_t words = (K + 31) / 32;
+        w.Kp = (K + 7) / 8 * 8;
+        w.sets = 0;
+        w.scales = w.sets + pad((records + 1) * words * 4);
+        w.lists = w.scales + pad(n * 4);
+        w.status = w.lists + pad((records + 1) * (K + 1) * 4);
+        w.qa = w.status + 256;
+        w.qw = w.qa + pad(n * w.Kp * 2);
+        w.total = w.qw + pad(N * w.Kp * 2);
+        return w;
+    }
+};
+
+constexpr int kQChunk = 1024;                  // products per exact fp32 partial sum
+constexpr int kQM = 128, kQK = 64, kQStages = 4;
+constexpr int kQEpiWarps = 16;
+constexpr int kQThreads = 32 * (2 + kQEpiWarps);
+constexpr int kQAStage = kQM * kQK * 2;        // 16 KB: 128 rows x 64 codes, 128-byte swizzle
+constexpr int kQBStageMax = 256 * kQK * 2;     // 32 KB: up to 256 weight rows
+constexpr int kQStageBytes = kQAStage + kQBStageMax;
+constexpr size_t kQSmem = 1024 + (size_t)kQStages * kQStageBytes + 256;
+
+// One warp per set (the records' sets, then the union): its columns in
+// ascending order, lists[t][0] = count, lists[t][1 ..] = columns.
+__global__ void k_int8_lists(const uint32_t* __restrict__ sets, int64_t words, int64_t K, int64_t nsets,
+                             int* __restrict__ lists) {
+    const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= nsets) return;
+    const uint32_t* bits = sets + t * words;
+    int* out = lists + t * (K + 1);
+    int cnt = 0;
+    for (int64_t w = 0; w < words; ++w) {
+        const uint32_t word = bits[w];                 // the same word for every lane
+        const bool mine = (word >> lane) & 1u;
+        const uint32_t below = word & ((1u << lane) - 1u);
+        if (mine) out[1 + cnt + __popc(below)] = (int)(w * 32 + lane);
+        cnt += __popc(word);
+    }
+    if (lane == 0) out[0] = cnt;
+}
+
+// bf16 codes, one thread per 8 columns of a row: rows 0 .. n-1 of A as Q_ij
+// (0 in the row's outlier columns or when s_i = 0), then the rows of the
+// weights' int8 codes; columns K .. Kp-1 zero.  Each thread writes 16 bytes.
+__global__ void k_int8_codes(const __half* __restrict__ A, int64_t n, int64_t K, int64_t Kp, int64_t rows,
+                             int64_t words, int record_owned, const uint32_t* __restrict__ sets,
+                             const uint32_t* __restrict__ uni, const float* __restrict__ scales,
+                             const int8_t* __restrict__ Wq, int64_t N, __nv_bfloat16* __restrict__ qa,
+                             __nv_bfloat16* __restrict__ qw) {
+    const int64_t gpr = Kp / 8;                        // groups per row
+    const int64_t total = (n + N) * gpr;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = t / gpr, j0 = (t - r * gpr) * 8;
+        __align__(16) __nv_bfloat16 out[8];
+        if (r < n) {
+            const uint32_t* set = record_owned ? sets + (r / rows) * words : uni;
+            const float s = __ldg(scales + r);
+            const uint32_t word = j0 < K ? __ldg(set + (j0 >> 5)) : 0u;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                const int64_t j = j0 + b;
+                int q = 0;
+                if (j < K && s > 0.f && !((word >> (j & 31)) & 1u))
+                    q = (int)rintf((127.0f * __half2float(A[r * K + j])) / s);
+                out[b] = __float2bfloat16_rn((float)q);
+            }
+            *reinterpret_cast<uint4*>(qa + r * Kp + j0) = *reinterpret_cast<const uint4*>(out);
+        } else {
+            const int64_t nn = r - n;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) out[b] = __float2bfloat16_rn(j0 + b < K ? (float)Wq[nn * K + j0 + b] : 0.f);
+            *reinterpret_cast<uint4*>(qw + nn * Kp + j0) = *reinterpret_cast<const uint4*>(out);
+        }
+    }
+}
+
+struct QGemmParams {
+    CUtensorMap tmA;     // codes of A: {K, n}, row pitch Kp, box {64, 128}, 128-byte swizzle
+    CUtensorMap tmW;     // codes of W: {K, N}, row pitch Kp, box {64, NT}
+    int64_t n, N, K;
+    int NT;              // output columns per tile (256 or 128)
+    int nch;             // K chunks of kQChunk, each in its own TMEM columns
+    int nk;              // 64-wide K tiles
+    int m_tiles, n_tiles;
+    int64_t rows, records;
+    int record_owned;
+    const __half* A;
+    const __half* What;
+    const float* s;
+    const float* sW;
+    const int* lists;
+    __half* Y;
+    int y_vec;           // Y rows start on 16-byte boundaries (N % 8 == 0)
+    unsigned* status;
+};
+
+struct QSmem {
+    uint64_t full[kQStages];
+    uint64_t empty[kQStages];
+    uint64_t acc_full;
+    uint64_t acc_empty;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// Y = half(dequant(Q Wq^T) + correction) for 128 x NT output tiles, strided
+// over the CTAs.  Warp 0: TMA producer; warp 1: TMEM owner and MMA issuer
+// (tcgen05.mma kind::f16, bf16 x bf16 -> fp32, M = 128, N = NT, both operands
+// K-major); warps 2-17: epilogue, a thread per output row and column quarter.
+__global__ void __launch_bounds__(kQThreads, 1) k_int8_gemm_tc(const __grid_constant__ QGemmParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    QSmem* sh = reinterpret_cast<QSmem*>(tiles + (size_t)kQStages * kQStageBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntiles = p.m_tiles * p.n_tiles;
+    const int bstage = p.NT * kQK * 2;
+    volatile int* abort_flag = &sh->abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kQStages; ++s) {
+            tc::mbar_init(&sh->full[s], 1);
+            tc::mbar_init(&sh->empty[s], 1);
+        }
+        tc::mbar_init(&sh->acc_full, 1);
+        tc::mbar_init(&sh->acc_empty, 32 * kQEpiWarps);
+        tc::mbar_init(&sh->drain, 1);
+        sh->abort_flag = 0;
+        tc::fence_barrier_init();
+        tc::tma_prefetch_desc(&p.tmA);
+        tc::tma_prefetch_desc(&p.tmW);
+    }
+    if (warp == 1) tc::tmem_alloc(&sh->tmem_base, 512);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+    // the codes come from the kernel before this one on the stream
+    dpk::grid_dep_wait();
+    dpk::grid_dep_trigger();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            tc::StageRing<kQStages> ring;
+            for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+                const int mb = tile / p.n_tiles, nb = tile % p.n_tiles;
+                for (int kt = 0; kt < p.nk; ++kt, ++it, ring.next()) {
+                    const uint32_t s = ring.s;
+                    if (!tc::mbar_wait(&sh->empty[s], ring.ph ^ 1u, abort_flag, p.status)) goto q_producer_done;
+                    uint8_t* st = tiles + (size_t)s * kQStageBytes;
+                    tc::mbar_arrive_expect_tx(&sh->full[s], (uint32_t)(kQAStage + bstage));
+                    tc::tma_load_2d(st, &p.tmA, &sh->full[s], kt * kQK, mb * kQM);
+                    tc::tma_load_2d(st + kQAStage, &p.tmW, &sh->full[s], kt * kQK, nb * p.NT);
+                }
+            }
+        q_producer_done:
+            for (uint32_t j = it > kQStages ? it - kQStages : 0; j < it; ++j)
+                tc::mbar_wait_drain(&sh->full[j % kQStages], (j / kQStages) & 1u);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = tc::idesc_bf16_f32(kQM, p.NT, 0, 0);
+            const uint32_t tiles_u32 = tc::smem_u32(tiles);
+            const int kt_per_chunk = kQChunk / kQK;
+            uint32_t lt = 0;
+            tc::StageRing<kQStages> ring;
+            for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++lt) {
+                if (!tc::mbar_wait(&sh->acc_empty, (lt & 1u) ^ 1u, abort_flag, p.status)) break;
+                tc::tc_fence_after();
+                bool ok = true;
+                for (int kt = 0; kt < p.nk; ++kt, ring.next()) {
+                    const uint32_t s = ring.s;
+                    if (!tc::mbar_wait(&sh->full[s], ring.ph, abort_flag, p.status)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    const int ch = kt / kt_per_chunk, kl = kt - ch * kt_per_chunk;
+                    const uint32_t d_tmem = tmem + (uint32_t)(ch * p.NT);
+                    const uint32_t sa = tiles_u32 + s * (uint32_t)kQStageBytes;
+                    const uint64_t ad = tc::smem_desc(sa, 16, 1024, tc::SW_128B);
+                    const uint64_t bd = tc::smem_desc(sa + kQAStage, 16, 1024, tc::SW_128B);
+#pragma unroll
+                    for (int kk = 0; kk < kQK / 16; ++kk)
+                        tc::mma_bf16(d_tmem, tc::desc_advance(ad, kk * 32), tc::desc_advance(bd, kk * 32), idesc,
+                                     (kl | kk) != 0);
+                    tc::mma_commit(&sh->empty[s]);
+                }
+                if (!ok) break;
+                tc::mma_commit(&sh->acc_full);
+            }
+        }
+    } else {
+        // four warps per TMEM lane quarter, each taking a quarter of the tile's
+        // columns, 16 at a time (the divisions of the dequantization are many
+        // dependent instructions: sixteen warps keep the schedulers busy)
+        const int quarter = warp & 3;
+        const int part = (warp - 2) >> 2;
+        const int row = quarter * 32 + lane;
+        const int cols = p.NT / 4;
+        const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);
+        uint32_t lt = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++lt) {
+            const int mb = tile / p.n_tiles, nb = tile % p.n_tiles;
+            if (!tc::mbar_wait_warp(&sh->acc_full, lt & 1u, abort_flag, p.status)) break;
+            tc::tc_fence_after();
+            const int64_t i = (int64_t)mb * kQM + row;
+            const bool valid = i < p.n;
+            const float si = valid ? p.s[i] : 0.f;
+            const int64_t set = p.record_owned ? (valid ? i / p.rows : 0) : p.records;
+            const int* list = p.lists + set * (p.K + 1);
+            const int cnt = valid ? list[0] : 0;
+#pragma unroll 1
+            for (int c0 = part * cols; c0 < (part + 1) * cols; c0 += 16) {
+                // every partial sum is an integer below 2^24, exact in fp32
+                int acc[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[j] = 0;
+                for (int ch = 0; ch < p.nch; ++ch) {
+                    float v[16];
+                    tc::tmem_ld16(tq + (uint32_t)(ch * p.NT + c0), v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc[j] += __float2int_rz(v[j]);
+                }
+                const int64_t n0 = (int64_t)nb * p.NT + c0;
+                if (valid && n0 < p.N) {
+                    float corr[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) corr[j] = 0.f;
+                    for (int c = 0; c < cnt; ++c) {
+                        const int jj = list[1 + c];
+                        const float a = __half2float(p.A[i * p.K + jj]);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (n0 + j < p.N) corr[j] = fmaf(a, __half2float(p.What[(n0 + j) * p.K + jj]), corr[j]);
+                    }
+                    __align__(16) __half y[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float sw = n0 + j < p.N ? __ldg(p.sW + n0 + j) : 0.f;
+                        const float deq = (((float)acc[j] * si) * sw) / 16129.0f;
+                        y[j] = __float2half_rn(deq + corr[j]);
+                    }
+                    __half* dst = p.Y + i * p.N + n0;
+                    if (p.y_vec && n0 + 16 <= p.N) {
+                        reinterpret_cast<uint4*>(dst)[0] = reinterpret_cast<const uint4*>(y)[0];
+                        reinterpret_cast<uint4*>(dst)[1] = reinterpret_cast<const uint4*>(y)[1];
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (n0 + j < p.N) dst[j] = y[j];
+                    }
+                }
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&sh->acc_empty);
+        }
+        // a wait that gave up leaves this CTA's tiles undone: they read NaN
+        if (*abort_flag) {
+            for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+                const int mb = tile / p.n_tiles, nb = tile % p.n_tiles;
+                const int64_t i = (int64_t)mb * kQM + row;
+                if (i >= p.n) continue;
+                for (int c = part * cols; c < (part + 1) * cols; ++c) {
+                    const int64_t nn = (int64_t)nb * p.NT + c;
+                    if (nn < p.N) p.Y[i * p.N + nn] = __float2half_rn(__int_as_float(0x7fc00000));
+                }
+            }
+        }
+    }
+
+    if (warp == 1 && lane == 0) {
+        tc::mma_commit(&sh->drain);
+        tc::mbar_wait_drain(&sh->drain, 0);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+bool encode_codes(CUtensorMap* m, const void* base, int64_t K, int64_t Kp, int64_t rows, uint32_t box_rows) {
+    const EncodeTiledFn fn = tensor_map_encoder();
+    if (!fn) return false;
+    cuuint64_t gd[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t gs[1] = {(cuuint64_t)(Kp * 2)};
+    cuuint32_t bd[2] = {(cuuint32_t)kQK, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gd, gs, bd, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
-extern "C" int64_t dp_int8_workspace_bytes(int64_t n, int64_t K, int64_t rows_per_record) {
-    if (n < 0 || K < 1 || rows_per_record < 1 || n % rows_per_record) return -1;
-    const int64_t words = (K + 31) / 32;
-    const int64_t records = n / rows_per_record;
-    const int64_t sets = ((records + 1) * words * 4 + 15) / 16 * 16;
-    return sets + (n * 4 + 15) / 16 * 16;
+extern "C" int64_t dp_int8_workspace_bytes(int64_t n, int64_t K, int64_t N, int64_t rows_per_record) {
+    if (n < 1 || K < 1 || N < 1 || rows_per_record < 1 || n % rows_per_record) return -1;
+    return Int8Workspace::layout(n, K, N, n / rows_per_record).total;
 }
 
 extern "C" dp_status dp_int8_quantize_weight(const void* W, int64_t N, int64_t K, int8_t* Wq, float* sW, void* What,
@@ -205,36 +540,87 @@ extern "C" dp_status dp_int8_forward(const void* A, int64_t n, int64_t K, int64_
     if (!A || !Wq || !sW || !What || !Y || !workspace) return DP_ERR_INVALID_ARG;
     if (n < 1 || K < 1 || N < 1 || rows_per_record < 1 || n % rows_per_record) return DP_ERR_SHAPE;
     if (!(tau > 0.f)) return DP_ERR_INVALID_ARG;
-    if (reinterpret_cast<uintptr_t>(workspace) & 15u) return DP_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return DP_ERR_INVALID_ARG;
+    if (n >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31) || K >= 133000) return DP_ERR_SHAPE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t words = (K + 31) / 32;
     const int64_t records = n / rows_per_record;
-    uint32_t* sets = static_cast<uint32_t*>(workspace);
+    const Int8Workspace lay = Int8Workspace::layout(n, K, N, records);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint32_t* sets = reinterpret_cast<uint32_t*>(ws + lay.sets);
     uint32_t* uni = sets + records * words;
-    float* scales = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                             ((records + 1) * words * 4 + 15) / 16 * 16);
-    if (cudaMemsetAsync(uni, 0, (size_t)words * 4, s) != cudaSuccess) return DP_ERR_CUDA;
-    k_int8_sets<<<dim3((unsigned)((words + 7) / 8), (unsigned)records), 256, 0, s>>>(
-        static_cast<const __half*>(A), K, rows_per_record, words, tau, sets, uni);
-    k_int8_scales<<<(unsigned)((n + 7) / 8), 256, 0, s>>>(static_cast<const __half*>(A), n, K, tau, scales);
-    Int8Args p;
-    p.A = static_cast<const __half*>(A);
+    float* scales = reinterpret_cast<float*>(ws + lay.scales);
+    if (cudaMemsetAsync(sets, 0, (size_t)(records + 1) * words * 4, s) != cudaSuccess) return DP_ERR_CUDA;
+    k_int8_rowscan<<<(unsigned)((n + 7) / 8), 256, 0, s>>>(static_cast<const __half*>(A), n, K, rows_per_record, words,
+                                                           tau, sets, uni, scales);
+    count_launch(KL_INT8_ROWSCAN);
+    if (K > 4 * kQChunk) {
+        // beyond four exact chunks per tile: the integer product on the CUDA cores
+        Int8Args p;
+        p.A = static_cast<const __half*>(A);
+        p.n = n;
+        p.K = K;
+        p.rows = rows_per_record;
+        p.words = words;
+        p.Wq = Wq;
+        p.sW = sW;
+        p.What = static_cast<const __half*>(What);
+        p.N = N;
+        p.record_owned = record_owned ? 1 : 0;
+        p.sets = sets;
+        p.uni = uni;
+        p.s = scales;
+        p.Y = static_cast<__half*>(Y);
+        k_int8_gemm<<<dim3((unsigned)((N + kTN - 1) / kTN), (unsigned)((n + kTM - 1) / kTM)), 256, 0, s>>>(p);
+        count_launch(KL_INT8_GEMM);
+        return cudaGetLastError() == cudaSuccess ? DP_OK : DP_ERR_CUDA;
+    }
+    int* lists = reinterpret_cast<int*>(ws + lay.lists);
+    unsigned* status = reinterpret_cast<unsigned*>(ws + lay.status);
+    __nv_bfloat16* qa = reinterpret_cast<__nv_bfloat16*>(ws + lay.qa);
+    __nv_bfloat16* qw = reinterpret_cast<__nv_bfloat16*>(ws + lay.qw);
+    if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return DP_ERR_CUDA;
+    k_int8_lists<<<(unsigned)((records + 1 + 7) / 8), 256, 0, s>>>(sets, words, K, records + 1, lists);
+    count_launch(KL_INT8_LISTS);
+    {
+        const int64_t groups = (n + N) * (lay.Kp / 8);
+        int64_t grid = (groups + 255) / 256;
+        const int64_t cap = (int64_t)device_sm_count() * 16;
+        if (grid > cap) grid = cap;
+        k_int8_codes<<<(unsigned)grid, 256, 0, s>>>(static_cast<const __half*>(A), n, K, lay.Kp, rows_per_record, words,
+                                                   record_owned ? 1 : 0, sets, uni, scales, Wq, N, qa, qw);
+    }
+    count_launch(KL_INT8_CODES);
+    QGemmParams p;
+    p.nch = (int)((K + kQChunk - 1) / kQChunk);
+    p.NT = p.nch <= 2 ? 256 : 128;
+    if (!encode_codes(&p.tmA, qa, K, lay.Kp, n, kQM) || !encode_codes(&p.tmW, qw, K, lay.Kp, N, (uint32_t)p.NT))
+        return DP_ERR_CUDA;
     p.n = n;
-    p.K = K;
-    p.rows = rows_per_record;
-    p.words = words;
-    p.Wq = Wq;
-    p.sW = sW;
-    p.What = static_cast<const __half*>(What);
     p.N = N;
+    p.K = K;
+    p.nk = (int)((K + kQK - 1) / kQK);
+    p.m_tiles = (int)((n + kQM - 1) / kQM);
+    p.n_tiles = (int)((N + p.NT - 1) / p.NT);
+    p.rows = rows_per_record;
+    p.records = records;
     p.record_owned = record_owned ? 1 : 0;
-    p.sets = sets;
-    p.uni = uni;
+    p.A = static_cast<const __half*>(A);
+    p.What = static_cast<const __half*>(What);
     p.s = scales;
+    p.sW = sW;
+    p.lists = lists;
     p.Y = static_cast<__half*>(Y);
-    k_int8_gemm<<<dim3((unsigned)((N + kTN - 1) / kTN), (unsigned)((n + kTM - 1) / kTM)), 256, 0, s>>>(p);
-    count_launch(KL_INT8_SETS);
-    count_launch(KL_INT8_SCALES);
-    count_launch(KL_INT8_GEMM);
-    return cudaGetLastError() == cudaSuccess ? DP_OK : DP_ERR_CUDA;
+    p.y_vec = (N % 8 == 0 && (reinterpret_cast<uintptr_t>(Y) & 15u) == 0) ? 1 : 0;
+    p.status = status;
+    {
+        const cudaError_t a = ensure_smem_limit(reinterpret_cast<const void*>(k_int8_gemm_tc), (int)kQSmem);
+        if (a != cudaSuccess) return DP_ERR_CUDA;
+    }
+    const int64_t ntiles = (int64_t)p.m_tiles * p.n_tiles;
+    const int sms = device_sm_count();
+    const int grid = (int)(ntiles < sms ? ntiles : sms);
+    const cudaError_t e = launch_dependent(k_int8_gemm_tc, dim3(grid), dim3(kQThreads), kQSmem, s, p);
+    count_launch(KL_INT8_GEMM_TC);
+    return e == cudaSuccess ? DP_OK : DP_ERR_CUDA;
 }

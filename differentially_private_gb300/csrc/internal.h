@@ -116,8 +116,8 @@ enum KernelId {
     KL_NORM_T1, KL_NORM_T1_GROUP, KL_NORM_GHOST_CC, KL_NORM_MAT_CC, KL_LAYER_SQNORM, KL_LAYER_SQNORM_STATUS,
     KL_GHOST_GRAM_TC, KL_MAT_SKINNY_TC, KL_CLIP, KL_GRAD_WSUM, KL_GRAD_GEMM_SMALL, KL_GRAD_GEMM_CC, KL_BIAS_SUM,
     KL_PRESCALE_ROWS, KL_CLIPPED_SUM_FOLD_PAIR_TC, KL_CLIPPED_SUM_TC, KL_SUM_LAYERS_PAIR_TC, KL_NOISE_SHARD,
-    KL_BOX_MULLER, KL_PHILOX_NORMALS, KL_PACK_GROUPS, KL_INT8_QUANTIZE_WEIGHT, KL_INT8_SETS, KL_INT8_SCALES,
-    KL_INT8_GEMM, KL_WAIT_EXPIRES, KL_COUNT
+    KL_BOX_MULLER, KL_PHILOX_NORMALS, KL_PACK_GROUPS, KL_INT8_QUANTIZE_WEIGHT, KL_INT8_ROWSCAN,
+    KL_INT8_GEMM, KL_INT8_LISTS, KL_INT8_CODES, KL_INT8_GEMM_TC, KL_WAIT_EXPIRES, KL_COUNT
 };
 void count_launch(KernelId k);
 

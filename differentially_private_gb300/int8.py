@@ -32,7 +32,7 @@ class Int8Linear:
             raise ValueError("A must be float16 [n, K]")
         A = A.contiguous()
         n = A.shape[0]
-        ws = b.dp_int8_workspace_bytes(n, self.K, rows_per_record)
+        ws = b.dp_int8_workspace_bytes(n, self.K, self.N, rows_per_record)
         if ws < 0:
             raise ValueError("rows must split into whole records")
         work = torch.empty(max(ws, 16), dtype=torch.uint8, device=A.device)

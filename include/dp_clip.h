@@ -293,8 +293,9 @@ dp_status dp_pack_groups(const void* src, void* dst, int64_t B, int64_t T, int64
  * K < 1.
  *
  * dp_int8_workspace_bytes -- bytes of the device workspace dp_int8_forward
- * needs for n rows of K columns in records of rows_per_record rows; -1 for
- * invalid sizes (n not a multiple of rows_per_record, K or rows < 1).
+ * needs for n rows of K columns in records of rows_per_record rows and N
+ * outputs; -1 for invalid sizes (n not a multiple of rows_per_record, n, K,
+ * N or rows < 1).
  *
  * dp_int8_forward -- A: device half [n, K] row-major, rows r*rows_per_record
  * .. (r+1)*rows_per_record-1 owned by record r.  With O_r the columns where
@@ -304,15 +305,19 @@ dp_status dp_pack_groups(const void* src, void* dst, int64_t B, int64_t T, int64
  *   Q_ij = rint((127 A_ij) / s_i) for j not in O (0 when s_i = 0), else 0;
  *   Y_in = half( ((float(sum_j Q_ij Wq_nj) * s_i) * sW_n) / 16129
  *                + sum over j in O ascending of fma(A_ij, What_nj, .) )
- * written to Y (device half [n, N]).  The integer sum is exact (K below
- * 133,000).  workspace: device, 16-byte aligned, dp_int8_workspace_bytes
- * bytes, overwritten.  Launches on `stream`.  DP_ERR_INVALID_ARG for NULL
- * pointers, tau <= 0 or a misaligned workspace; DP_ERR_SHAPE for invalid
- * sizes; DP_ERR_CUDA for a launch failure.
+ * written to Y (device half [n, N]).  The integer sum is exact: for K up to
+ * 4096 on the bf16 tensor cores (the int8 codes are exact in bf16, and each
+ * chunk of 1024 products stays below 2^24 in the fp32 accumulator; the
+ * chunks are added in int32), beyond on the CUDA cores; K below 133,000.
+ * workspace: device, 256-byte aligned, dp_int8_workspace_bytes bytes,
+ * overwritten.  Launches on `stream`.  A wait of the tensor-core kernel that
+ * gives up (2 s bound) leaves NaN in the affected outputs.  DP_ERR_INVALID_ARG
+ * for NULL pointers, tau <= 0 or a misaligned workspace; DP_ERR_SHAPE for
+ * invalid sizes; DP_ERR_CUDA for a launch failure.
  */
 dp_status dp_int8_quantize_weight(const void* W, int64_t N, int64_t K, int8_t* Wq, float* sW, void* What,
                                   void* stream);
-int64_t dp_int8_workspace_bytes(int64_t n, int64_t K, int64_t rows_per_record);
+int64_t dp_int8_workspace_bytes(int64_t n, int64_t K, int64_t N, int64_t rows_per_record);
 dp_status dp_int8_forward(const void* A, int64_t n, int64_t K, int64_t rows_per_record, const int8_t* Wq,
                           const float* sW, const void* What, int64_t N, float tau, int record_owned, void* Y,
                           void* workspace, void* stream);

@@ -92,3 +92,38 @@ def test_record_owned_rows_do_not_depend_on_other_records():
     b1 = lin(A2, rows, record_owned=False)
     torch.cuda.synchronize()
     assert not torch.equal(b0[:rows], b1[:rows])      # batched routing couples the records
+
+
+@pytest.mark.parametrize("K,signs", [(1024, "same"), (1024, "random"), (2048, "same"), (3072, "random"),
+                                     (4096, "same"), (4104, "random")])
+def test_integer_product_exact_at_the_largest_partial_sums(K, signs):
+    """Codes of +-127 on both sides: up to K, the partial sums reach 16129 K.
+    Up to K = 4096 the product runs on the bf16 tensor cores in chunks of 1024
+    (each below 2^24, exact in fp32, added in int32); beyond, on the CUDA
+    cores.  Either way it must match the oracle's exact integer product bit
+    for bit, including the float rounding of sums beyond 2^24."""
+    import differentially_private_gb300 as dp
+    g = torch.Generator(device="cuda").manual_seed(K)
+    rows, records, N = 40, 3, 200
+    n = rows * records
+    if signs == "same":
+        A = torch.ones(n, K, device="cuda")
+        W = torch.full((N, K), 0.25, device="cuda")
+    else:
+        A = torch.where(torch.rand(n, K, device="cuda", generator=g) < 0.5, -1.0, 1.0)
+        W = torch.where(torch.rand(N, K, device="cuda", generator=g) < 0.5, -0.25, 0.25)
+    A[5, 7] = 9.0                          # one outlier column in record 0
+    A = A.half()
+    W = W.half()
+    lin = Int8Linear(W)
+    before = dp.dp_kernel_launch_counts()
+    Y = lin(A, rows, tau=6.0, record_owned=True)
+    torch.cuda.synchronize()
+    after = dp.dp_kernel_launch_counts()
+    tc_path = after["k_int8_gemm_tc"] - before["k_int8_gemm_tc"]
+    assert tc_path == (1 if K <= 4096 else 0)
+    assert after["k_int8_gemm"] - before["k_int8_gemm"] == (0 if K <= 4096 else 1)
+    want = oint8.forward(A.cpu().numpy(), rows, lin.Wq.cpu().numpy(), lin.sW.cpu().numpy(),
+                         lin.What.cpu().numpy(), 6.0, record_owned=True)
+    got = _bits(Y)
+    assert np.array_equal(got, want.view(np.uint16)), int((got != want.view(np.uint16)).sum())
