@@ -17,8 +17,8 @@
 // by k-tile and, inside a k-tile, block by block, so the blocks of one
 // 64-row slab are read back to back (whole rows of X in DRAM order).  Y has
 // its own small ring and is loaded once per k-tile for all blocks.  Each
-// block accumulates into its own 16 TMEM columns; items alternate between
-// two accumulator sets.  One launch serves up to kMaxSkinnyGroup layers.
+// block accumulates into its own 16 TMEM columns; items rotate through four
+// accumulator sets.  One launch serves up to kMaxSkinnyGroup layers.
 //
 // The epilogue writes one partial squared norm per (record, block, epilogue
 // warp) -- no barrier, no atomics: a record's norm depends only on its own
@@ -42,8 +42,8 @@ constexpr int kXStage = kBM * kBK * 2;
 constexpr int kYStage = kBN * kBK * 2;
 constexpr int kMaxMb = 8;                   // column blocks per work item (TMEM columns of one set)
 constexpr int kEpiGroup = 4;                // blocks whose TMEM columns the epilogue loads at once (tmem_ld16x4)
-constexpr int kAccSets = 2;
-constexpr uint32_t kTmemCols = 256;         // kAccSets * kMaxMb * kBN
+constexpr int kAccSets = 4;                 // the MMAs run up to three items ahead of the epilogue
+constexpr uint32_t kTmemCols = 512;         // kAccSets * kMaxMb * kBN
 constexpr int kThreads = 192;
 constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kBM, kBN, 1, 1);
 constexpr size_t kSmem = 1024 + (size_t)kXStages * kXStage + (size_t)kYStages * kYStage + 8192 + 512;
