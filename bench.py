@@ -661,7 +661,7 @@ def run_int8_forward(args):
     inputs: 16 records x 256 rows of fp16 activations, d_model 768, with a
     few outlier entries (|a| >= 6) in a few columns of some records.  Times
     dp_int8_forward (all its launches) with CUDA events, 10 warm-up and K
-    timed calls, L2 flushed before each and the GPU kept busy while the host
+    timed calls (both products warmed up), L2 flushed before each and the GPU kept busy while the host
     enqueues them (the host's enqueue time is reported apart); beside it, the same product through
     torch.matmul in fp16 (cuBLAS on the tensor cores, batched-LLM.int8-free
     and not record-isolated: context only).  Prints one JSON line per layer."""
@@ -692,6 +692,7 @@ def run_int8_forward(args):
         lin = Int8Linear(W, stream=stream)
         for _ in range(10):
             lin(A, rows)
+            torch.matmul(A, W.t())
         torch.cuda.synchronize()
         times, ref_times, host = [], [], []
         for _ in range(args.steps):
@@ -724,7 +725,8 @@ def run_int8_forward(args):
                 "l2": "flushed before every timed call"}
         print(json.dumps(line), flush=True)
     # the GPU's own int8 and bf16 tensor-core rates on a large product (cuBLAS
-    # through torch: context for the int8 forward, which runs on dp4a)
+    # through torch): context for the int8 forward, whose exact integer
+    # product runs on the bf16 tensor cores for K up to 4096
     rates = {}
     m = 8192
     for name, mk in (("int8", lambda: (torch.randint(-127, 128, (m, m), dtype=torch.int8, device=dev),

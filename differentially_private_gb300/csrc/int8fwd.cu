@@ -62,9 +62,10 @@ __global__ void k_int8_quantize_weight(const __half* __restrict__ W, int64_t N, 
 // lanes of a word combine their bits by shuffles.
 __global__ void k_int8_rowscan(const __half* __restrict__ A, int64_t n, int64_t K, int64_t rows, int64_t words,
                                float tau, uint32_t* __restrict__ sets, uint32_t* __restrict__ uni,
-                               float* __restrict__ scales) {
+                               float* __restrict__ scales, unsigned* __restrict__ status) {
     const int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    if (status && i == 0 && lane == 0) *status = 0u;   // the tensor-core product's wait status
     if (i >= n) return;
     const __half* a = A + i * K;
     uint32_t* set = sets + (i / rows) * words;
@@ -236,6 +237,8 @@ struct Int8Workspace {
 constexpr int kQChunk = 1024;                  // products per exact fp32 partial sum
 constexpr int kQM = 128, kQK = 64, kQStages = 4;
 constexpr int kQEpiWarps = 16;
+constexpr int kQPre = 2;                       // set columns whose half weights are loaded ahead (one per half-warp)
+static_assert(kQPre == 2, "the epilogue hands the preloaded half weights around as two half-warps");
 constexpr int kQThreads = 32 * (2 + kQEpiWarps);
 constexpr int kQAStage = kQM * kQK * 2;        // 16 KB: 128 rows x 64 codes, 128-byte swizzle
 constexpr int kQBStageMax = 256 * kQK * 2;     // 32 KB: up to 256 weight rows
@@ -244,11 +247,9 @@ constexpr size_t kQSmem = 1024 + (size_t)kQStages * kQStageBytes + 256;
 
 // One warp per set (the records' sets, then the union): its columns in
 // ascending order, lists[t][0] = count, lists[t][1 ..] = columns.
-__global__ void k_int8_lists(const uint32_t* __restrict__ sets, int64_t words, int64_t K, int64_t nsets,
-                             int* __restrict__ lists) {
-    const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+__device__ void set_list(const uint32_t* __restrict__ sets, int64_t words, int64_t K, int64_t t,
+                         int* __restrict__ lists) {
     const int lane = threadIdx.x & 31;
-    if (t >= nsets) return;
     const uint32_t* bits = sets + t * words;
     int* out = lists + t * (K + 1);
     int cnt = 0;
@@ -262,17 +263,26 @@ __global__ void k_int8_lists(const uint32_t* __restrict__ sets, int64_t words, i
     if (lane == 0) out[0] = cnt;
 }
 
-// bf16 codes, one thread per 8 columns of a row: rows 0 .. n-1 of A as Q_ij
-// (0 in the row's outlier columns or when s_i = 0), then the rows of the
-// weights' int8 codes; columns K .. Kp-1 zero.  Each thread writes 16 bytes.
+// The first list_blocks blocks write the sets' column lists (a warp per
+// set); the others the bf16 codes, one thread per 8 columns of a row: rows
+// 0 .. n-1 of A as Q_ij (0 in the row's outlier columns or when s_i = 0),
+// then the rows of the weights' int8 codes; columns K .. Kp-1 zero.  Each
+// thread writes 16 bytes.
 __global__ void k_int8_codes(const __half* __restrict__ A, int64_t n, int64_t K, int64_t Kp, int64_t rows,
                              int64_t words, int record_owned, const uint32_t* __restrict__ sets,
                              const uint32_t* __restrict__ uni, const float* __restrict__ scales,
                              const int8_t* __restrict__ Wq, int64_t N, __nv_bfloat16* __restrict__ qa,
-                             __nv_bfloat16* __restrict__ qw) {
+                             __nv_bfloat16* __restrict__ qw, int64_t nsets, int* __restrict__ lists,
+                             int list_blocks) {
+    if ((int)blockIdx.x < list_blocks) {
+        const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+        if (t < nsets) set_list(sets, words, K, t, lists);
+        return;
+    }
     const int64_t gpr = Kp / 8;                        // groups per row
     const int64_t total = (n + N) * gpr;
-    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t nthreads = (int64_t)(gridDim.x - list_blocks) * blockDim.x;
+    for (int64_t t = (int64_t)(blockIdx.x - list_blocks) * blockDim.x + threadIdx.x; t < total; t += nthreads) {
         const int64_t r = t / gpr, j0 = (t - r * gpr) * 8;
         __align__(16) __nv_bfloat16 out[8];
         if (r < n) {
@@ -320,8 +330,8 @@ struct QGemmParams {
 struct QSmem {
     uint64_t full[kQStages];
     uint64_t empty[kQStages];
-    uint64_t acc_full;
-    uint64_t acc_empty;
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -345,8 +355,10 @@ __global__ void __launch_bounds__(kQThreads, 1) k_int8_gemm_tc(const __grid_cons
             tc::mbar_init(&sh->full[s], 1);
             tc::mbar_init(&sh->empty[s], 1);
         }
-        tc::mbar_init(&sh->acc_full, 1);
-        tc::mbar_init(&sh->acc_empty, 32 * kQEpiWarps);
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&sh->acc_full[b], 1);
+            tc::mbar_init(&sh->acc_empty[b], 32 * kQEpiWarps);
+        }
         tc::mbar_init(&sh->drain, 1);
         sh->abort_flag = 0;
         tc::fence_barrier_init();
@@ -358,6 +370,9 @@ __global__ void __launch_bounds__(kQThreads, 1) k_int8_gemm_tc(const __grid_cons
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
+    // two accumulators (the next tile's MMAs run during this tile's epilogue)
+    // when a tile's chunks fit in half of the 512 TMEM columns
+    const uint32_t nbuf = p.nch * p.NT <= 256 ? 2u : 1u;
     // the codes come from the kernel before this one on the stream
     dpk::grid_dep_wait();
     dpk::grid_dep_trigger();
@@ -389,7 +404,8 @@ __global__ void __launch_bounds__(kQThreads, 1) k_int8_gemm_tc(const __grid_cons
             uint32_t lt = 0;
             tc::StageRing<kQStages> ring;
             for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++lt) {
-                if (!tc::mbar_wait(&sh->acc_empty, (lt & 1u) ^ 1u, abort_flag, p.status)) break;
+                const uint32_t b = lt % nbuf, use = lt / nbuf;
+                if (!tc::mbar_wait(&sh->acc_empty[b], (use & 1u) ^ 1u, abort_flag, p.status)) break;
                 tc::tc_fence_after();
                 bool ok = true;
                 for (int kt = 0; kt < p.nk; ++kt, ring.next()) {
@@ -397,7 +413,7 @@ __global__ void __launch_bounds__(kQThreads, 1) k_int8_gemm_tc(const __grid_cons
                     if (!tc::mbar_wait(&sh->full[s], ring.ph, abort_flag, p.status)) { ok = false; break; }
                     tc::tc_fence_after();
                     const int ch = kt / kt_per_chunk, kl = kt - ch * kt_per_chunk;
-                    const uint32_t d_tmem = tmem + (uint32_t)(ch * p.NT);
+                    const uint32_t d_tmem = tmem + b * 256u + (uint32_t)(ch * p.NT);
                     const uint32_t sa = tiles_u32 + s * (uint32_t)kQStageBytes;
                     const uint64_t ad = tc::smem_desc(sa, 16, 1024, tc::SW_128B);
                     const uint64_t bd = tc::smem_desc(sa + kQAStage, 16, 1024, tc::SW_128B);
@@ -408,13 +424,18 @@ __global__ void __launch_bounds__(kQThreads, 1) k_int8_gemm_tc(const __grid_cons
                     tc::mma_commit(&sh->empty[s]);
                 }
                 if (!ok) break;
-                tc::mma_commit(&sh->acc_full);
+                tc::mma_commit(&sh->acc_full[b]);
             }
         }
     } else {
         // four warps per TMEM lane quarter, each taking a quarter of the tile's
         // columns, 16 at a time (the divisions of the dequantization are many
-        // dependent instructions: sixteen warps keep the schedulers busy)
+        // dependent instructions: sixteen warps keep the schedulers busy).
+        // Everything the epilogue reads from global memory -- the row's scale,
+        // its set's first kQPre columns and their A entries, the weights'
+        // scales and (when the warp's rows share one set) the half weights of
+        // those set columns in the warp's columns -- is loaded while the tensor
+        // cores work, one value per lane, and handed around by shuffles.
         const int quarter = warp & 3;
         const int part = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
@@ -423,58 +444,104 @@ __global__ void __launch_bounds__(kQThreads, 1) k_int8_gemm_tc(const __grid_cons
         uint32_t lt = 0;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++lt) {
             const int mb = tile / p.n_tiles, nb = tile % p.n_tiles;
-            if (!tc::mbar_wait_warp(&sh->acc_full, lt & 1u, abort_flag, p.status)) break;
-            tc::tc_fence_after();
             const int64_t i = (int64_t)mb * kQM + row;
             const bool valid = i < p.n;
             const float si = valid ? p.s[i] : 0.f;
             const int64_t set = p.record_owned ? (valid ? i / p.rows : 0) : p.records;
             const int* list = p.lists + set * (p.K + 1);
             const int cnt = valid ? list[0] : 0;
+            int jj[kQPre];
+            float av[kQPre];
+#pragma unroll
+            for (int u = 0; u < kQPre; ++u) {
+                jj[u] = u < cnt ? list[1 + u] : 0;   // column 0 stands in for an absent entry
+                av[u] = u < cnt ? __half2float(p.A[i * p.K + jj[u]]) : 0.f;
+            }
+            const int64_t cbase = (int64_t)nb * p.NT + part * cols;   // the warp's first column
+            const float swv0 = cbase + lane < p.N ? __ldg(p.sW + cbase + lane) : 0.f;
+            const float swv1 = cols > 32 && cbase + 32 + lane < p.N ? __ldg(p.sW + cbase + 32 + lane) : 0.f;
+            // the rows of a warp usually belong to one record (or all take the union):
+            // then lane l holds, for each 16-column group g, the half weight of column
+            // 16 g + (l mod 16) and set column l / 16
+            // (every lane takes part in each shuffle: none sits behind a short-circuit)
+            const int cnt_l0 = __shfl_sync(0xffffffffu, cnt, 0);
+            const int jj0_l0 = __shfl_sync(0xffffffffu, jj[0], 0);
+            const int jj1_l0 = __shfl_sync(0xffffffffu, jj[1], 0);
+            const bool shared_set = __all_sync(0xffffffffu, cnt == cnt_l0 && jj[0] == jj0_l0 && jj[1] == jj1_l0);
+            float wpre[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const int64_t nn = cbase + 16 * g + (lane & 15);
+                const int u = lane >> 4;
+                wpre[g] = shared_set && u < cnt && 16 * g < cols && nn < p.N
+                              ? __half2float(p.What[nn * p.K + (u ? jj[1] : jj[0])])
+                              : 0.f;
+            }
+            const uint32_t b = lt % nbuf, use = lt / nbuf;
+            if (!tc::mbar_wait_warp(&sh->acc_full[b], use & 1u, abort_flag, p.status)) break;
+            tc::tc_fence_after();
 #pragma unroll 1
-            for (int c0 = part * cols; c0 < (part + 1) * cols; c0 += 16) {
+            for (int c0 = 0; c0 < cols; c0 += 16) {
                 // every partial sum is an integer below 2^24, exact in fp32
                 int acc[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) acc[j] = 0;
                 for (int ch = 0; ch < p.nch; ++ch) {
                     float v[16];
-                    tc::tmem_ld16(tq + (uint32_t)(ch * p.NT + c0), v);
+                    tc::tmem_ld16(tq + b * 256u + (uint32_t)(ch * p.NT + part * cols + c0), v);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) acc[j] += __float2int_rz(v[j]);
                 }
-                const int64_t n0 = (int64_t)nb * p.NT + c0;
-                if (valid && n0 < p.N) {
+                const int64_t n0 = cbase + c0;
+                if (n0 < p.N) {   // uniform across the warp; rows past n have an empty set
+                    // the correction over the row's set in ascending column order: the
+                    // first kQPre columns' weights loaded together, the rest one by one
                     float corr[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) corr[j] = 0.f;
-                    for (int c = 0; c < cnt; ++c) {
-                        const int jj = list[1 + c];
-                        const float a = __half2float(p.A[i * p.K + jj]);
+                    if (shared_set) {
+                        const int g = c0 >> 4;
+                        const float wg = g == 0 ? wpre[0] : (g == 1 ? wpre[1] : (g == 2 ? wpre[2] : wpre[3]));
+#pragma unroll
+                        for (int u = 0; u < kQPre; ++u) {
+                            if (u < cnt) {
+#pragma unroll
+                                for (int j = 0; j < 16; ++j)
+                                    corr[j] = fmaf(av[u], __shfl_sync(0xffffffffu, wg, 16 * u + j), corr[j]);
+                            }
+                        }
+                    }
+                    for (int c = shared_set ? kQPre : 0; c < cnt; ++c) {
+                        const int jc = list[1 + c];
+                        const float a = __half2float(p.A[i * p.K + jc]);
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            if (n0 + j < p.N) corr[j] = fmaf(a, __half2float(p.What[(n0 + j) * p.K + jj]), corr[j]);
+                            if (n0 + j < p.N) corr[j] = fmaf(a, __half2float(p.What[(n0 + j) * p.K + jc]), corr[j]);
                     }
                     __align__(16) __half y[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float sw = n0 + j < p.N ? __ldg(p.sW + n0 + j) : 0.f;
+                        // the weight's scale of column n0 + j, from the lane that loaded it
+                        const int cc = c0 + j;
+                        const float sw = __shfl_sync(0xffffffffu, (cc & 32) ? swv1 : swv0, cc & 31);
                         const float deq = (((float)acc[j] * si) * sw) / 16129.0f;
                         y[j] = __float2half_rn(deq + corr[j]);
                     }
-                    __half* dst = p.Y + i * p.N + n0;
-                    if (p.y_vec && n0 + 16 <= p.N) {
-                        reinterpret_cast<uint4*>(dst)[0] = reinterpret_cast<const uint4*>(y)[0];
-                        reinterpret_cast<uint4*>(dst)[1] = reinterpret_cast<const uint4*>(y)[1];
-                    } else {
+                    if (valid) {
+                        __half* dst = p.Y + i * p.N + n0;
+                        if (p.y_vec && n0 + 16 <= p.N) {
+                            reinterpret_cast<uint4*>(dst)[0] = reinterpret_cast<const uint4*>(y)[0];
+                            reinterpret_cast<uint4*>(dst)[1] = reinterpret_cast<const uint4*>(y)[1];
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            if (n0 + j < p.N) dst[j] = y[j];
+                            for (int j = 0; j < 16; ++j)
+                                if (n0 + j < p.N) dst[j] = y[j];
+                        }
                     }
                 }
             }
             tc::tc_fence_before();
-            tc::mbar_arrive(&sh->acc_empty);
+            tc::mbar_arrive(&sh->acc_empty[b]);
         }
         // a wait that gave up leaves this CTA's tiles undone: they read NaN
         if (*abort_flag) {
@@ -551,10 +618,12 @@ extern "C" dp_status dp_int8_forward(const void* A, int64_t n, int64_t K, int64_
     uint32_t* uni = sets + records * words;
     float* scales = reinterpret_cast<float*>(ws + lay.scales);
     if (cudaMemsetAsync(sets, 0, (size_t)(records + 1) * words * 4, s) != cudaSuccess) return DP_ERR_CUDA;
+    const bool tensor_cores = K <= 4 * kQChunk;
+    unsigned* status = reinterpret_cast<unsigned*>(ws + lay.status);
     k_int8_rowscan<<<(unsigned)((n + 7) / 8), 256, 0, s>>>(static_cast<const __half*>(A), n, K, rows_per_record, words,
-                                                           tau, sets, uni, scales);
+                                                           tau, sets, uni, scales, tensor_cores ? status : nullptr);
     count_launch(KL_INT8_ROWSCAN);
-    if (K > 4 * kQChunk) {
+    if (!tensor_cores) {
         // beyond four exact chunks per tile: the integer product on the CUDA cores
         Int8Args p;
         p.A = static_cast<const __half*>(A);
@@ -576,19 +645,17 @@ extern "C" dp_status dp_int8_forward(const void* A, int64_t n, int64_t K, int64_
         return cudaGetLastError() == cudaSuccess ? DP_OK : DP_ERR_CUDA;
     }
     int* lists = reinterpret_cast<int*>(ws + lay.lists);
-    unsigned* status = reinterpret_cast<unsigned*>(ws + lay.status);
     __nv_bfloat16* qa = reinterpret_cast<__nv_bfloat16*>(ws + lay.qa);
     __nv_bfloat16* qw = reinterpret_cast<__nv_bfloat16*>(ws + lay.qw);
-    if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return DP_ERR_CUDA;
-    k_int8_lists<<<(unsigned)((records + 1 + 7) / 8), 256, 0, s>>>(sets, words, K, records + 1, lists);
-    count_launch(KL_INT8_LISTS);
     {
         const int64_t groups = (n + N) * (lay.Kp / 8);
         int64_t grid = (groups + 255) / 256;
         const int64_t cap = (int64_t)device_sm_count() * 16;
         if (grid > cap) grid = cap;
-        k_int8_codes<<<(unsigned)grid, 256, 0, s>>>(static_cast<const __half*>(A), n, K, lay.Kp, rows_per_record, words,
-                                                   record_owned ? 1 : 0, sets, uni, scales, Wq, N, qa, qw);
+        const int64_t list_blocks = (records + 1 + 7) / 8;   // a warp per set, 8 warps per block
+        k_int8_codes<<<(unsigned)(list_blocks + grid), 256, 0, s>>>(
+            static_cast<const __half*>(A), n, K, lay.Kp, rows_per_record, words, record_owned ? 1 : 0, sets, uni,
+            scales, Wq, N, qa, qw, records + 1, lists, (int)list_blocks);
     }
     count_launch(KL_INT8_CODES);
     QGemmParams p;

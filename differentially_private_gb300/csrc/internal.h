@@ -117,7 +117,7 @@ enum KernelId {
     KL_GHOST_GRAM_TC, KL_MAT_SKINNY_TC, KL_CLIP, KL_GRAD_WSUM, KL_GRAD_GEMM_SMALL, KL_GRAD_GEMM_CC, KL_BIAS_SUM,
     KL_PRESCALE_ROWS, KL_CLIPPED_SUM_FOLD_PAIR_TC, KL_CLIPPED_SUM_TC, KL_SUM_LAYERS_PAIR_TC, KL_NOISE_SHARD,
     KL_BOX_MULLER, KL_PHILOX_NORMALS, KL_PACK_GROUPS, KL_INT8_QUANTIZE_WEIGHT, KL_INT8_ROWSCAN,
-    KL_INT8_GEMM, KL_INT8_LISTS, KL_INT8_CODES, KL_INT8_GEMM_TC, KL_WAIT_EXPIRES, KL_COUNT
+    KL_INT8_GEMM, KL_INT8_CODES, KL_INT8_GEMM_TC, KL_WAIT_EXPIRES, KL_COUNT
 };
 void count_launch(KernelId k);
 

@@ -381,7 +381,7 @@ static const char* const kKernelNames[KL_COUNT] = {
     "k_grad_gemm_small", "k_grad_gemm_cc", "k_bias_sum", "k_prescale_rows", "k_clipped_sum_fold_pair_tc",
     "k_clipped_sum_tc", "k_sum_layers_pair_tc", "k_noise_shard", "k_box_muller", "k_philox_normals",
     "k_pack_groups", "k_int8_quantize_weight", "k_int8_rowscan", "k_int8_gemm",
-    "k_int8_lists", "k_int8_codes", "k_int8_gemm_tc", "k_wait_expires",
+    "k_int8_codes", "k_int8_gemm_tc", "k_wait_expires",
 };
 
 void count_launch(KernelId k) {

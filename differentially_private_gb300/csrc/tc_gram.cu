@@ -111,18 +111,24 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
                 int pb, qb;
                 gram_tile(item % p.tiles_per_rec, p.np, p.nq, pb, qb);
                 // the left 128 columns of the tile lie below the diagonal when p = 2q + 1:
-                // they are neither loaded nor multiplied
+                // they are neither loaded nor multiplied.  On the diagonal the row block p
+                // is one of the two halves of the column block q, so it is loaded once:
+                // p = 2q uses the left half as A, p = 2q + 1 its own rows as the right half
                 const bool left = pb <= 2 * qb;
+                const bool diag = pb == 2 * qb;
+                const uint32_t bytes = diag ? 2u * kGAStage : (left ? kGStageBytes : kGAStage);
                 for (int kt = 0; kt < nkA + nkE; ++kt, ++it, ring.next()) {
                     const uint32_t s = ring.s;
                     if (!tc::mbar_wait(&sh->empty[s], ring.ph ^ 1u, abort_flag, p.status)) goto gram_producer_done;
                     uint8_t* st = tiles + (size_t)s * kGStageBytes;
                     const CUtensorMap* tm = kt < nkA ? &p.tmA : &p.tmE;
                     const int k0 = (kt < nkA ? kt : kt - nkA) * kGK;
-                    tc::mbar_arrive_expect_tx(&sh->full[s], left ? kGStageBytes : kGStageBytes - kGAStage);
-                    tc::tma_load_3d(st, tm, &sh->full[s], k0, pb * kGM, rec);
-                    if (left) tc::tma_load_3d(st + kGAStage, tm, &sh->full[s], k0, qb * kGN, rec);
-                    tc::tma_load_3d(st + kGAStage + kGAStage, tm, &sh->full[s], k0, qb * kGN + 128, rec);
+                    tc::mbar_arrive_expect_tx(&sh->full[s], bytes);
+                    if (!diag) tc::tma_load_3d(st, tm, &sh->full[s], k0, pb * kGM, rec);
+                    if (left) {
+                        tc::tma_load_3d(st + kGAStage, tm, &sh->full[s], k0, qb * kGN, rec);
+                        tc::tma_load_3d(st + kGAStage + kGAStage, tm, &sh->full[s], k0, qb * kGN + 128, rec);
+                    }
                 }
             }
         gram_producer_done:
@@ -138,9 +144,12 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
                 int pb, qb;
                 gram_tile(item % p.tiles_per_rec, p.np, p.nq, pb, qb);
                 const bool left = pb <= 2 * qb;
-                // full tile: N = 256 from the first B row; right half only: N = 128 from row 128
+                const bool diag = pb == 2 * qb;
+                // full tile: N = 256 from the first B row; right half only: N = 128, its B rows
+                // being the A rows; on the diagonal A is the B block's left half
                 const uint32_t idesc = left ? kIdescGram : kIdescGramHalf;
-                const uint32_t boff = left ? 0u : (uint32_t)kGAStage;
+                const uint32_t aoff = diag ? (uint32_t)kGAStage : 0u;
+                const uint32_t boff = left ? (uint32_t)kGAStage : 0u;
                 const uint32_t coff = left ? 0u : 128u;
                 if (!tc::mbar_wait(&sh->acc_empty, (lt & 1u) ^ 1u, abort_flag, p.status)) break;
                 tc::tc_fence_after();
@@ -154,8 +163,8 @@ __global__ void __launch_bounds__(kGThreads, 1) k_ghost_gram_tc(const __grid_con
                     const uint32_t d_tmem = tmem + (phaseA ? 0u : 256u) + coff;
                     const int kl = phaseA ? kt : kt - nkA;
                     // K-major, 128B swizzle: 16 features = 32 bytes inside the swizzle row
-                    const uint64_t ad = tc::smem_desc(sa, 16, 1024, tc::SW_128B);
-                    const uint64_t bd = tc::smem_desc(sa + kGAStage + boff, 16, 1024, tc::SW_128B);
+                    const uint64_t ad = tc::smem_desc(sa + aoff, 16, 1024, tc::SW_128B);
+                    const uint64_t bd = tc::smem_desc(sa + boff, 16, 1024, tc::SW_128B);
 #pragma unroll
                     for (int kk = 0; kk < kGK / 16; ++kk)
                         tc::mma_bf16(d_tmem, tc::desc_advance(ad, kk * 32), tc::desc_advance(bd, kk * 32), idesc,
