@@ -428,17 +428,21 @@ def run_ours(args, w):
     for ly in w.layers:
         sizes += [w.B * ly.T * ly.d_in, w.B * ly.T * ly.d_out]
     arena = torch.empty(sum(seg(n) for n in sizes), dtype=torch.uint8, device=device)
-    views, off = [], 0
-    for n in sizes:
-        views.append(arena[off:off + n * esz].view(w.torch_dtype))
-        off += seg(n)
-    A_dev, E_dev = [], []
+
+    def carve(buf):
+        # the layers' A and E as views of one arena, in layer order
+        views, off = [], 0
+        for n in sizes:
+            views.append(buf[off:off + n * esz].view(w.torch_dtype))
+            off += seg(n)
+        return ([views[2 * i].view(w.B, ly.T, ly.d_in) for i, ly in enumerate(w.layers)],
+                [views[2 * i + 1].view(w.B, ly.T, ly.d_out) for i, ly in enumerate(w.layers)])
+
+    A_dev, E_dev = carve(arena)
     for i, ly in enumerate(w.layers):
         a, e = generate_layer(w, i, device)
-        A_dev.append(views[2 * i].view(a.shape))
-        E_dev.append(views[2 * i + 1].view(e.shape))
-        A_dev[-1].copy_(a)
-        E_dev[-1].copy_(e)
+        A_dev[i].copy_(a)
+        E_dev[i].copy_(e)
         del a, e
     T_list = [ly.T for ly in w.layers]
     stream = torch.cuda.current_stream(device)
@@ -599,7 +603,12 @@ def run_ours(args, w):
                   "read_floor_us": arena.numel() / (peaks["hbm_gbs"] * 1e9 * eff) * 1e6,
                   "ideal_read_us": arena.numel() / (peaks["hbm_gbs"] * 1e9) * 1e6}
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers: every step copies
+    # its inputs from pinned host memory and reads G back.  The inputs of step
+    # k + 1 are copied into a second device arena on a second stream while
+    # step k computes (as a data loader would prefetch the next batch); the
+    # same steps with the copies and the step one after the other on one
+    # stream are reported beside it, with the host link's own rate
     e2e = None
     if not args.no_e2e:
         arena_pin = torch.empty(arena.numel(), dtype=torch.uint8, pin_memory=True)
@@ -607,26 +616,65 @@ def run_ours(args, w):
         garena_pin = torch.empty(garena.numel(), dtype=torch.float32, pin_memory=True)
         h2d = arena.numel()
         d2h = garena.numel() * 4
-
-        def e2e_step():
-            arena.copy_(arena_pin, non_blocking=True)
-            step()
-            garena_pin.copy_(garena, non_blocking=True)
-
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
         ke = max(3, min(K, 10))
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(ke):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ems = max_over_ranks(e0.elapsed_time(e1), device)
+
+        def timed(fn):
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1)
+
+        link_ms = min(timed(lambda: arena.copy_(arena_pin, non_blocking=True)) for _ in range(3))
+
+        def serial(n):
+            for _ in range(n):
+                arena.copy_(arena_pin, non_blocking=True)
+                step()
+                garena_pin.copy_(garena, non_blocking=True)
+
+        arena2 = torch.empty_like(arena)
+        A2, E2 = carve(arena2)
+        preps = [prep, pg.prepare(A2, E2, T_list, outputs=(grads, clip, sq))]
+        arenas = [arena, arena2]
+        cstream = torch.cuda.Stream(device)
+        copied = [torch.cuda.Event(), torch.cuda.Event()]
+        freed = [torch.cuda.Event(), torch.cuda.Event()]
+
+        def pipelined(n):
+            cstream.wait_stream(stream)
+            with torch.cuda.stream(cstream):
+                arenas[0].copy_(arena_pin, non_blocking=True)
+                copied[0].record(cstream)
+            for k in range(n):
+                cur, nxt = k % 2, (k + 1) % 2
+                if k + 1 < n:
+                    with torch.cuda.stream(cstream):
+                        if k >= 1:
+                            cstream.wait_event(freed[nxt])     # step k - 1 is done with that arena
+                        arenas[nxt].copy_(arena_pin, non_blocking=True)
+                        copied[nxt].record(cstream)
+                stream.wait_event(copied[cur])
+                preps[cur].run(w.C, w.sigma, w.noise_seed, w.step)
+                freed[cur].record(stream)
+                garena_pin.copy_(garena, non_blocking=True)
+
+        serial(2)
+        pipelined(2)
+        ser_ms = max_over_ranks(timed(lambda: serial(ke)), device)
+        ems = max_over_ranks(timed(lambda: pipelined(ke)), device)
+        st = dp.dp_step_status(ctx)
+        if st != dp.DP_OK:
+            raise dp.DPError(st, "dp_step_status", dp.dp_last_error(ctx))
+        del arena2, A2, E2, preps
         e2e = {"value": job_throughput(world, w.B, ke, ems), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h}
+               "d2h_bytes_per_step": d2h, "steps": ke,
+               "copies": "next step's inputs copied on a second stream while the current step computes",
+               "serial_value": job_throughput(world, w.B, ke, ser_ms),
+               "h2d_link_gbs": h2d / (link_ms / 1e3) / 1e9}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
