@@ -50,6 +50,39 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     return t;
 }
 
+// Sum of squares of one row read as 16-byte vectors by a warp: lane l takes
+// vectors l, l + 32, ... in that order (eight loads in flight per lane).
+template <typename T>
+__device__ __forceinline__ float sumsq_vec(const uint4* __restrict__ p, int64_t n4, int lane) {
+    constexpr int PER = 16 / (int)sizeof(T);
+    float s = 0.f;
+    int64_t k = lane;
+    for (; k + 224 < n4; k += 256) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldg(p + k + 32 * u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const T* x = (const T*)&v[u];
+#pragma unroll
+            for (int q = 0; q < PER; ++q) { const float f = (float)x[q]; s = fmaf(f, f, s); }
+        }
+    }
+    for (; k < n4; k += 32) {
+        const uint4 v = __ldg(p + k);
+        const T* x = (const T*)&v;
+#pragma unroll
+        for (int q = 0; q < PER; ++q) { const float f = (float)x[q]; s = fmaf(f, f, s); }
+    }
+    return s;
+}
+
+// The T == 1 closed form of one layer's squared norm from the two row sums of
+// squares: ||a||^2 ||e||^2, plus ||e||^2 for a bias, as one fused multiply-add.
+__device__ __forceinline__ float t1_partial(float sa, float se, int has_bias) {
+    return fmaf(sa, se, has_bias ? se : 0.f);
+}
+
 // ---------------------------------------------------------------- Philox
 // Philox-4x32 with ten rounds (Salmon, Moraes, Dror, Shaw, SC'11): each round
 // multiplies counter words 0 and 2 by two fixed odd constants, keeps the low

@@ -142,6 +142,115 @@ __global__ void __launch_bounds__(kClipMaxThreads) k_clip(const ClipParams p, fl
     }
 }
 
+// Every layer of the step is a T == 1 bf16 layer: the norm kernel and the
+// clip kernel in one launch.  A block of eight warps serves R = max(1, 8 / n)
+// records: each warp takes (record, layer) items and forms the layer's partial
+// from the sums of squares of the a and e rows in the norm kernel's order
+// (vector l, l + 32, ... of each row for lane l), the partials meet in shared
+// memory, and a warp per record combines them with the butterfly the clip
+// kernel applies to one slot per lane -- so n2 and c are bitwise those of the
+// two-kernel path.  A warp whose row is a pre-scaled operand keeps that row's
+// vectors in registers and writes c_i times them once c_i is known (when every
+// such row fits kKeepUnits vectors per lane; otherwise the block re-reads them).
+constexpr int kFusedWarps = 8;
+
+__global__ void __launch_bounds__(32 * kFusedWarps, 4) k_norm_clip_t1(const ClipParams p, const T1Group g,
+                                                                   float* __restrict__ n2_out,
+                                                                   float* __restrict__ c_out,
+                                                                   float* __restrict__ n2_user,
+                                                                   float* __restrict__ c_user,
+                                                                   unsigned* __restrict__ status) {
+    using T = __nv_bfloat16;
+    __shared__ float part[kFusedWarps][32];
+    __shared__ float cs[kFusedWarps];
+    // A and E may come from the kernel just before this one on the stream
+    grid_dep_wait();
+    grid_dep_trigger();
+    if (p.status_next && blockIdx.x == 0 && threadIdx.x == 0) *p.status_next = 0u;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int R = g.n >= kFusedWarps ? 1 : kFusedWarps / g.n;
+    const int64_t rec0 = (int64_t)blockIdx.x * R;
+    // the row kept for pre-scaling by this warp's last item (at most one item
+    // per warp when g.keep_x: the host allows it only for g.n <= kFusedWarps)
+    uint4 keep[kKeepUnits];
+    int keep_r = -1;
+    uint4* keep_dst = nullptr;
+    int64_t keep_n4 = 0;
+    for (int item = warp; item < R * g.n; item += kFusedWarps) {
+        const int r = item / g.n, l = item - r * g.n;
+        const int64_t rec = rec0 + r;
+        if (rec >= p.B) continue;
+        const auto& ly = g.L[l];
+        const uint4* a = (const uint4*)ly.A + rec * (ly.d_in / 8);
+        const uint4* e = (const uint4*)ly.E + rec * (ly.d_out / 8);
+        float sa, se;
+        if (g.keep_x && ly.scale_job >= 0) {
+            const uint4* x = ly.x_is_a ? a : e;
+            const int64_t n4 = ly.x_is_a ? ly.d_in / 8 : ly.d_out / 8;
+#pragma unroll
+            for (int j = 0; j < kKeepUnits; ++j)
+                if (lane + 32 * j < n4) keep[j] = __ldg(x + lane + 32 * j);
+            const float so = warp_sum(sumsq_vec<T>(ly.x_is_a ? e : a, ly.x_is_a ? ly.d_out / 8 : ly.d_in / 8, lane));
+            float sx = 0.f;
+#pragma unroll
+            for (int j = 0; j < kKeepUnits; ++j) {
+                if (lane + 32 * j < n4) {
+                    const T* q = (const T*)&keep[j];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) { const float f = (float)q[u]; sx = fmaf(f, f, sx); }
+                }
+            }
+            sx = warp_sum(sx);
+            sa = ly.x_is_a ? sx : so;
+            se = ly.x_is_a ? so : sx;
+            keep_r = r;
+            keep_dst = p.scale[ly.scale_job].dst + rec * n4;
+            keep_n4 = n4;
+        } else {
+            sa = warp_sum(sumsq_vec<T>(a, ly.d_in / 8, lane));
+            se = warp_sum(sumsq_vec<T>(e, ly.d_out / 8, lane));
+        }
+        if (lane == 0) part[r][l] = t1_partial(sa, se, ly.has_bias);
+    }
+    __syncthreads();
+    if (warp < R && rec0 + warp < p.B) {
+        const int64_t rec = rec0 + warp;
+        const float s = warp_sum(lane < g.n ? part[warp][lane] : 0.f);
+        const bool finite = isfinite(s);
+        // C / n rounded toward zero keeps c * n <= C in float arithmetic
+        const float c = !finite ? 0.f : (sqrtf(s) <= p.C ? 1.0f : __fdiv_rz(p.C, sqrtf(s)));
+        if (lane == 0) {
+            if (!finite) atomicOr(status, 1u);
+            n2_out[rec] = s;
+            c_out[rec] = c;
+            if (n2_user) n2_user[rec] = s;
+            if (c_user) c_user[rec] = c;
+            cs[warp] = c;
+        }
+    }
+    if (p.nscale == 0) return;
+    __syncthreads();
+    if (g.keep_x) {
+        if (keep_r >= 0) {
+            const float c = cs[keep_r];
+#pragma unroll
+            for (int j = 0; j < kKeepUnits; ++j)
+                if (lane + 32 * j < keep_n4) keep_dst[lane + 32 * j] = scale_bf16x8(keep[j], c);
+        }
+        return;
+    }
+    int64_t units = 0;
+    for (int j = 0; j < p.nscale; ++j) units += p.scale[j].units;
+    const int nrec = p.B - rec0 < R ? (int)(p.B - rec0) : R;
+    for (int64_t x = threadIdx.x; x < (int64_t)nrec * units; x += blockDim.x) {
+        const int r = (int)(x / units);
+        const uint4* src;
+        uint4* dst;
+        scale_unit(p, x - (int64_t)r * units, rec0 + r, &src, &dst);
+        *dst = scale_bf16x8(__ldg(src), cs[r]);
+    }
+}
+
 // --------------------------------------------- stored-gradient weighted sum
 struct WsumParams {
     int n;
@@ -539,6 +648,16 @@ cudaError_t launch_clip(const ClipParams& p, float* n2, float* c, float* n2_user
         e = launch_dependent(k_clip<false>, dim3((unsigned)p.B), dim3(G), 0, s, p, n2, c, n2_user, c_user, status);
     }
     count_launch(KL_CLIP);
+    return e;
+}
+
+cudaError_t launch_norm_clip_t1(const ClipParams& p, const T1Group& g, float* n2, float* c, float* n2_user,
+                                float* c_user, unsigned* status, cudaStream_t s) {
+    const int R = g.n >= kFusedWarps ? 1 : kFusedWarps / g.n;   // records per block
+    const unsigned grid = (unsigned)((p.B + R - 1) / R);
+    const cudaError_t e = launch_dependent(k_norm_clip_t1, dim3(grid), dim3(32 * kFusedWarps), 0, s, p, g, n2, c,
+                                           n2_user, c_user, status);
+    count_launch(KL_NORM_CLIP_T1);
     return e;
 }
 

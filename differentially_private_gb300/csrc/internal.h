@@ -95,6 +95,27 @@ struct ClipParams {
     PrescaleJob scale[kMaxPrescale];
 };
 
+// Several T == 1 bf16 layers (rows of whole 16-byte vectors) in one launch,
+// one warp per record.
+struct T1Group {
+    int n;
+    int64_t B;
+    struct {
+        const void* A;
+        const void* E;
+        int64_t d_in, d_out;
+        int has_bias;
+        float* partial;
+        int scale_job;   // fused norm + clip kernel: index of the layer's pre-scale job, or -1
+        int x_is_a;      // that job's operand is A (else E)
+    } L[kMaxGroup];
+    int keep_x;          // fused kernel: every pre-scaled row fits kKeepUnits vectors per lane
+};
+// 16-byte vectors per lane of a pre-scaled row that the fused kernel keeps in registers
+constexpr int kKeepUnits = 4;
+// at most this many T == 1 layers take the fused norm + clip kernel (a lane per layer)
+constexpr int kMaxFusedT1 = 32;
+
 // one-thread kernel whose bounded wait on a barrier nobody completes gives up
 // after limit_ns and sets the timeout bit of *status (waitcheck.cu)
 cudaError_t launch_wait_expiry(unsigned* status, uint64_t limit_ns, cudaStream_t s);
@@ -114,7 +135,7 @@ cudaError_t ensure_smem_limit(const void* kernel, int bytes);
 // (dp_kernel_launches, dp_kernel_launch_counts)
 enum KernelId {
     KL_NORM_T1, KL_NORM_T1_GROUP, KL_NORM_GHOST_CC, KL_NORM_MAT_CC, KL_LAYER_SQNORM, KL_LAYER_SQNORM_STATUS,
-    KL_GHOST_GRAM_TC, KL_MAT_SKINNY_TC, KL_CLIP, KL_GRAD_WSUM, KL_GRAD_GEMM_SMALL, KL_GRAD_GEMM_CC, KL_BIAS_SUM,
+    KL_GHOST_GRAM_TC, KL_MAT_SKINNY_TC, KL_CLIP, KL_NORM_CLIP_T1, KL_GRAD_WSUM, KL_GRAD_GEMM_SMALL, KL_GRAD_GEMM_CC, KL_BIAS_SUM,
     KL_PRESCALE_ROWS, KL_CLIPPED_SUM_FOLD_PAIR_TC, KL_CLIPPED_SUM_TC, KL_SUM_LAYERS_PAIR_TC, KL_NOISE_SHARD,
     KL_BOX_MULLER, KL_PHILOX_NORMALS, KL_PACK_GROUPS, KL_INT8_QUANTIZE_WEIGHT, KL_INT8_ROWSCAN,
     KL_INT8_GEMM, KL_INT8_CODES, KL_INT8_GEMM_TC, KL_WAIT_EXPIRES, KL_COUNT
@@ -149,6 +170,10 @@ cudaError_t launch_layer_sqnorm_checked(const float* partial, int nslots, int64_
                                         const unsigned* status, cudaStream_t s);
 cudaError_t launch_clip(const ClipParams& p, float* n2, float* c, float* n2_user, float* c_user,
                         unsigned* status, cudaStream_t s);
+// every layer of the step T == 1: the layers' norms, the clip factors and the
+// pre-scaled copies in one launch, instead of the norm kernel and the clip kernel
+cudaError_t launch_norm_clip_t1(const ClipParams& p, const T1Group& g, float* n2, float* c, float* n2_user,
+                                float* c_user, unsigned* status, cudaStream_t s);
 cudaError_t launch_grad_wsum(const GradTask* tasks, int n, const float* c, const unsigned* status,
                              const StepScalars& sc, cudaStream_t s);
 cudaError_t launch_grad_gemm_cc(const GradTask& t, const float* c, const unsigned* status,

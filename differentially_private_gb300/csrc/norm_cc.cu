@@ -25,46 +25,8 @@ namespace {
 constexpr int kGT = 32;   // Gram / gradient tile edge
 
 // ------------------------------------------------------------------ T == 1
-// Sum of squares of one row read as 16-byte vectors by a warp: lane l takes
-// vectors l, l + 32, ... in that order (four loads in flight per lane).
-template <typename T>
-__device__ __forceinline__ float sumsq_vec(const uint4* __restrict__ p, int64_t n4, int lane) {
-    constexpr int PER = 16 / (int)sizeof(T);
-    float s = 0.f;
-    int64_t k = lane;
-    for (; k + 96 < n4; k += 128) {
-        uint4 v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = __ldg(p + k + 32 * u);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const T* x = (const T*)&v[u];
-#pragma unroll
-            for (int q = 0; q < PER; ++q) { const float f = (float)x[q]; s = fmaf(f, f, s); }
-        }
-    }
-    for (; k < n4; k += 32) {
-        const uint4 v = __ldg(p + k);
-        const T* x = (const T*)&v;
-#pragma unroll
-        for (int q = 0; q < PER; ++q) { const float f = (float)x[q]; s = fmaf(f, f, s); }
-    }
-    return s;
-}
-
 // Several T == 1 layers in one launch (bf16, rows of whole 16-byte vectors):
 // blockIdx.y selects the layer, one warp per record.
-struct T1Group {
-    int n;
-    int64_t B;
-    struct {
-        const void* A;
-        const void* E;
-        int64_t d_in, d_out;
-        int has_bias;
-        float* partial;
-    } L[kMaxGroup];
-};
 
 __global__ void __launch_bounds__(256) k_norm_t1_group(const T1Group g) {
     using T = __nv_bfloat16;
@@ -78,7 +40,7 @@ __global__ void __launch_bounds__(256) k_norm_t1_group(const T1Group g) {
     if (rec >= g.B) return;
     const float sa = warp_sum(sumsq_vec<T>((const uint4*)ly.A + rec * (ly.d_in / 8), ly.d_in / 8, lane));
     const float se = warp_sum(sumsq_vec<T>((const uint4*)ly.E + rec * (ly.d_out / 8), ly.d_out / 8, lane));
-    if (lane == 0) ly.partial[rec] = sa * se + (ly.has_bias ? se : 0.f);
+    if (lane == 0) ly.partial[rec] = t1_partial(sa, se, ly.has_bias);
 }
 
 template <int DT, bool VEC>
@@ -101,7 +63,7 @@ __global__ void __launch_bounds__(256) k_norm_t1(const void* __restrict__ Av, co
     }
     sa = warp_sum(sa);
     se = warp_sum(se);
-    if (lane == 0) partial[rec] = sa * se + (has_bias ? se : 0.f);
+    if (lane == 0) partial[rec] = t1_partial(sa, se, has_bias);
 }
 
 // ------------------------------------------------------------ ghost Gram
@@ -296,7 +258,10 @@ cudaError_t launch_norm_t1_group(const NormTask* tasks, int n, int64_t B, cudaSt
             g.L[i].d_out = t.d_out;
             g.L[i].has_bias = t.has_bias;
             g.L[i].partial = t.partial;
+            g.L[i].scale_job = -1;
+            g.L[i].x_is_a = 0;
         }
+        g.keep_x = 0;
         const dim3 grid((unsigned)((B * 32 + 255) / 256), (unsigned)g.n);
         const cudaError_t e = launch_dependent(k_norm_t1_group, grid, dim3(256), 0, s, g);
         count_launch(KL_NORM_T1_GROUP);

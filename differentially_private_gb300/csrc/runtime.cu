@@ -102,6 +102,11 @@ struct dp_ctx {
     size_t d_slots_cap = 0;
     std::vector<std::pair<const float*, int64_t>> slots_key;   // (partial, nslots) per layer d_slots was built from
     std::vector<SlotRef> h_slots;      // host copy of d_slots (the source of its last upload)
+    // every layer of the step T == 1 and accumulated in one batch call without
+    // per-layer outputs: their norms are deferred to the clip call, which runs
+    // norms, clip factors and pre-scaled copies in one kernel
+    bool t1_fused = false;
+    std::vector<NormTask> t1_tasks;    // in registration order
     std::string err;
 };
 
@@ -377,7 +382,7 @@ static std::atomic<int64_t> g_kernel_launches[KL_COUNT];
 // Names of the kernels, in KernelId order.
 static const char* const kKernelNames[KL_COUNT] = {
     "k_norm_t1", "k_norm_t1_group", "k_norm_ghost_cc", "k_norm_mat_cc", "k_layer_sqnorm",
-    "k_layer_sqnorm_status", "k_ghost_gram_tc", "k_mat_skinny_tc", "k_clip", "k_grad_wsum",
+    "k_layer_sqnorm_status", "k_ghost_gram_tc", "k_mat_skinny_tc", "k_clip", "k_norm_clip_t1", "k_grad_wsum",
     "k_grad_gemm_small", "k_grad_gemm_cc", "k_bias_sum", "k_prescale_rows", "k_clipped_sum_fold_pair_tc",
     "k_clipped_sum_tc", "k_sum_layers_pair_tc", "k_noise_shard", "k_box_muller", "k_philox_normals",
     "k_pack_groups", "k_int8_quantize_weight", "k_int8_rowscan", "k_int8_gemm",
@@ -669,6 +674,7 @@ dp_status dp_begin_step(dp_ctx* ctx, int64_t B) {
     }
     ctx->B = B;
     ctx->L = (double)B;
+    ctx->t1_fused = false;
     ctx->phase = OPEN;
     ctx->err.clear();
     return DP_OK;
@@ -719,6 +725,22 @@ dp_status dp_norm_accumulate_batch(dp_ctx* ctx, int n, const int* layer_ids, con
         dp_status st = prepare(ctx, layer_ids[i], A[i], E[i], T[i], plans[i]);
         if (st != DP_OK) return st;
     }
+    // every layer of the step T == 1, no per-layer outputs: the norms run inside
+    // the clip call's kernel (nothing is launched here)
+    bool fuse = n == (int)ctx->layers.size() && n <= kMaxFusedT1;
+    for (int i = 0; i < n && fuse; ++i)
+        fuse = plans[i].norm_kernel == NK_T1 && t1_groupable(make_norm_task(plans[i])) &&
+               !(sqnorm_out && sqnorm_out[i]);
+    if (fuse) {
+        ctx->t1_tasks.assign((size_t)n, NormTask{});
+        for (int i = 0; i < n; ++i) ctx->t1_tasks[(size_t)layer_ids[i]] = make_norm_task(plans[i]);
+        for (int i = 0; i < n; ++i) {
+            dp_status st = finish(ctx, layer_ids[i], plans[i], nullptr);
+            if (st != DP_OK) return st;
+        }
+        ctx->t1_fused = true;
+        return DP_OK;
+    }
     // one grouped launch for every skinny materialized layer, one launch each for the rest
     std::vector<NormTask> skinny, t1;
     for (int i = 0; i < n; ++i) {
@@ -747,6 +769,68 @@ dp_status dp_norm_accumulate_batch(dp_ctx* ctx, int n, const int* layer_ids, con
     return DP_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// The clip kernel's parameters besides the slot table: B, C, the next step's
+// status word (zeroed by the kernel: every kernel that could write it belongs
+// to an earlier, finished step) and the first kMaxPrescale pre-scaled operand
+// copies, which the clip kernel writes.
+ClipParams clip_params(dp_ctx* ctx, float C) {
+    ClipParams p;
+    p.B = ctx->B;
+    p.C = C;
+    p.slots = nullptr;
+    p.total_slots = 0;
+    p.status_next = ctx->status_words + (ctx->slot ^ 1);
+    p.nscale = 0;
+    for (Layer& ly : ctx->layers) {
+        ly.scaled_by_clip = ly.grad_kernel == GK_GEMM_TC && ly.prescale && p.nscale < kMaxPrescale;
+        if (!ly.scaled_by_clip) continue;
+        const int64_t d = ly.prescale_A ? ly.d_in : ly.d_out;
+        p.scale[p.nscale++] = PrescaleJob{static_cast<const uint4*>(ly.prescale_A ? ly.A : ly.E),
+                                          reinterpret_cast<uint4*>(ly.escaled), ly.T * d / 8};
+    }
+    return p;
+}
+
+// the deferred T == 1 norms, the clip factors and the pre-scaled copies in one launch
+dp_status clip_fused_t1(dp_ctx* ctx, float C, float* c_out, float* total_sqnorm_out) {
+    const ClipParams p = clip_params(ctx, C);
+    T1Group grp;
+    grp.n = (int)ctx->t1_tasks.size();
+    grp.B = ctx->B;
+    // a warp of the fused kernel keeps a pre-scaled row in registers when it
+    // has one item (at most eight layers) and every such row is short enough
+    grp.keep_x = grp.n <= 8 ? 1 : 0;
+    int job = 0;
+    for (int i = 0; i < grp.n; ++i) {
+        const NormTask& t = ctx->t1_tasks[(size_t)i];
+        const Layer& ly = ctx->layers[(size_t)i];
+        grp.L[i].A = t.A;
+        grp.L[i].E = t.E;
+        grp.L[i].d_in = t.d_in;
+        grp.L[i].d_out = t.d_out;
+        grp.L[i].has_bias = t.has_bias;
+        grp.L[i].partial = nullptr;
+        grp.L[i].scale_job = ly.scaled_by_clip ? job++ : -1;
+        grp.L[i].x_is_a = ly.prescale_A ? 1 : 0;
+        if (ly.scaled_by_clip && (ly.prescale_A ? t.d_in : t.d_out) / 8 > 32 * kKeepUnits) grp.keep_x = 0;
+    }
+    const cudaError_t e =
+        launch_norm_clip_t1(p, grp, ctx->n2, ctx->c, total_sqnorm_out, c_out, ctx->status, ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "norm and clip kernel launch");
+    ctx->clean[ctx->slot ^ 1] = true;
+    ctx->C = C;
+    ctx->phase = CLIPPED;
+    return DP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnorm_out) {
     NvtxRange nvtx_range("dp_clip_factors");
     if (!ctx) return DP_ERR_INVALID_ARG;
@@ -756,6 +840,7 @@ dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnor
         if (!ctx->layers[l].accumulated)
             return fail(ctx, DP_ERR_STATE, "layer %zu was not accumulated in this step", l);
     DeviceGuard g(ctx->device);
+    if (ctx->t1_fused) return clip_fused_t1(ctx, C, c_out, total_sqnorm_out);
     std::vector<std::pair<const float*, int64_t>> key(ctx->layers.size());
     int64_t total = 0;
     for (size_t l = 0; l < ctx->layers.size(); ++l) {
@@ -784,23 +869,9 @@ dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnor
                                               cudaMemcpyHostToDevice, ctx->stream);
         if (e != cudaSuccess) return cuda_fail(ctx, e, "slot table upload");
     }
-    ClipParams p;
-    p.B = ctx->B;
-    p.C = C;
+    ClipParams p = clip_params(ctx, C);
     p.slots = ctx->d_slots;
     p.total_slots = total;
-    // the clip kernel also zeroes the other status word for the next step
-    // (every kernel that could write it belongs to an earlier, finished step)
-    p.status_next = ctx->status_words + (ctx->slot ^ 1);
-    // the clip kernel also writes the first kMaxPrescale pre-scaled operand copies
-    p.nscale = 0;
-    for (Layer& ly : ctx->layers) {
-        ly.scaled_by_clip = ly.grad_kernel == GK_GEMM_TC && ly.prescale && p.nscale < kMaxPrescale;
-        if (!ly.scaled_by_clip) continue;
-        const int64_t d = ly.prescale_A ? ly.d_in : ly.d_out;
-        p.scale[p.nscale++] = PrescaleJob{static_cast<const uint4*>(ly.prescale_A ? ly.A : ly.E),
-                                          reinterpret_cast<uint4*>(ly.escaled), ly.T * d / 8};
-    }
     const cudaError_t e = launch_clip(p, ctx->n2, ctx->c, total_sqnorm_out, c_out, ctx->status, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "clip kernel launch");
     ctx->clean[ctx->slot ^ 1] = true;
