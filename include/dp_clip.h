@@ -172,6 +172,12 @@ dp_status dp_norm_accumulate(dp_ctx* ctx, int layer_id, const void* A, const voi
  * launch per kernel kind instead of one launch per layer.  Arrays are host
  * arrays of length n; sqnorm_out may be NULL (or hold NULL entries).  All
  * arguments are validated before anything is launched.
+ * When the call holds every registered layer, every one of them takes the
+ * T = 1 closed form in bf16 with rows of whole 16-byte vectors, there are at
+ * most 32 of them and no sqnorm_out entry is given, nothing is launched here:
+ * dp_clip_factors computes these norms, the clip factors and the pre-scaled
+ * operands in one kernel, with bitwise the results of the separate launches.
+ * A and E are borrowed until dp_clipped_noisy_grad in either case.
  */
 dp_status dp_norm_accumulate_batch(dp_ctx* ctx, int n, const int* layer_ids,
                                    const void* const* A, const void* const* E,
