@@ -157,3 +157,34 @@ def test_clipped_sum_follows_the_step_state_machine():
     assert ei.value.status == dp.DP_ERR_STATE
     assert dp.dp_step_status(pg.ctx) == dp.DP_OK
     pg.close()
+
+
+def test_sharded_step_over_nccl_with_one_rank():
+    """The sharded step's exchange through NCCL on the GPU with one rank: the
+    all-reduce, reduce-scatter and all-gather run on the library's device
+    buffers (more ranks need more GPUs).  G matches the single-GPU step, and
+    G(sigma) - G(0) is the float64 noise at every coordinate."""
+    import torch.distributed as dist
+    import differentially_private_gb300 as dp
+    from differentially_private_gb300.sharded import LibraryShardOps, sharded_step
+    if not dist.is_available() or not dist.is_nccl_available():
+        pytest.skip("torch.distributed has no NCCL")
+    if dist.is_initialized():
+        pytest.skip("a process group is already initialized")
+    dist.init_process_group("nccl", store=dist.HashStore(), rank=0, world_size=1)
+    try:
+        B, C, sigma, seed, step = 7, 1.0, 0.9, 21, 5
+        A, E = _inputs(B, 3)
+        pg = dp.PrivateGradient(LAYERS, dtype=torch.bfloat16)
+        full = pg.step(A, E, T_LIST, C=C, sigma=sigma, seed=seed, step=step)
+        G_full = torch.cat([g for g in full.grads])
+        ops = LibraryShardOps(pg)
+        G = sharded_step(ops, A, E, T_LIST, C, sigma, seed, step).clone()
+        G0 = sharded_step(ops, A, E, T_LIST, C, 0.0, seed, step).clone()
+        torch.cuda.synchronize()
+        assert rel_fro(to64(G), to64(G_full)) <= G_RTOL
+        want = sigma * C * noise_of(seed, step, 0, pg.P) / B
+        assert np.allclose(to64(G) - to64(G0), want, rtol=1e-4, atol=2e-6 * sigma * C / B)
+        pg.close()
+    finally:
+        dist.destroy_process_group()
