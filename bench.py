@@ -154,6 +154,19 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+PIN_CHUNK = 1 << 30
+
+
+def pinned_chunks(nbytes: int):
+    """Pinned host memory for nbytes as (offset, uint8 tensor) pieces of 1 GiB.
+    torch's pinned-memory allocator rounds one request up to a power of two
+    (16 GB for the 11.6 GB of inputs of the Llama-shaped layer, held by every
+    rank of a node at once); 1 GiB pieces waste less than one piece."""
+    import torch
+    return [(o, torch.empty(min(PIN_CHUNK, nbytes - o), dtype=torch.uint8, pin_memory=True))
+            for o in range(0, nbytes, PIN_CHUNK)]
+
+
 def max_over_ranks(x: float, device) -> float:
     """The largest x over the ranks of the default process group (x itself
     without one): the job is as slow as its slowest rank."""
@@ -611,8 +624,14 @@ def run_ours(args, w):
     # stream; the line reports the faster, both, and the host link's own rate
     e2e = None
     if not args.no_e2e:
-        arena_pin = torch.empty(arena.numel(), dtype=torch.uint8, pin_memory=True)
-        arena_pin.copy_(arena)
+        arena_pin = pinned_chunks(arena.numel())
+        for o, c in arena_pin:
+            c.copy_(arena[o:o + c.numel()])
+
+        def h2d_copy(dst):
+            for o, c in arena_pin:
+                dst[o:o + c.numel()].copy_(c, non_blocking=True)
+
         garena_pin = torch.empty(garena.numel(), dtype=torch.float32, pin_memory=True)
         h2d = arena.numel()
         d2h = garena.numel() * 4
@@ -628,7 +647,7 @@ def run_ours(args, w):
             torch.cuda.synchronize()
             return e0.elapsed_time(e1)
 
-        link_ms = min(timed(lambda: arena.copy_(arena_pin, non_blocking=True)) for _ in range(3))
+        link_ms = min(timed(lambda: h2d_copy(arena)) for _ in range(3))
 
         copy_ev = []
 
@@ -636,7 +655,7 @@ def run_ours(args, w):
             for _ in range(n):
                 ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 ev[0].record(stream)
-                arena.copy_(arena_pin, non_blocking=True)
+                h2d_copy(arena)
                 ev[1].record(stream)
                 copy_ev.append(ev)
                 step()
@@ -653,7 +672,7 @@ def run_ours(args, w):
         def pipelined(n):
             cstream.wait_stream(stream)
             with torch.cuda.stream(cstream):
-                arenas[0].copy_(arena_pin, non_blocking=True)
+                h2d_copy(arenas[0])
                 copied[0].record(cstream)
             for k in range(n):
                 cur, nxt = k % 2, (k + 1) % 2
@@ -661,7 +680,7 @@ def run_ours(args, w):
                     with torch.cuda.stream(cstream):
                         if k >= 1:
                             cstream.wait_event(freed[nxt])     # step k - 1 is done with that arena
-                        arenas[nxt].copy_(arena_pin, non_blocking=True)
+                        h2d_copy(arenas[nxt])
                         copied[nxt].record(cstream)
                 stream.wait_event(copied[cur])
                 preps[cur].run(w.C, w.sigma, w.noise_seed, w.step)
@@ -677,7 +696,7 @@ def run_ours(args, w):
         st = dp.dp_step_status(ctx)
         if st != dp.DP_OK:
             raise dp.DPError(st, "dp_step_status", dp.dp_last_error(ctx))
-        del arena2, A2, E2, preps
+        del arena2, A2, E2, preps, arena_pin
         pipe_value = job_throughput(world, w.B, ke, ems)
         ser_value = job_throughput(world, w.B, ke, ser_ms)
         # the faster of the two schedules (for a few KB of inputs the second
