@@ -62,7 +62,7 @@ __global__ void k_int8_quantize_weight(const __half* __restrict__ W, int64_t N, 
 // lanes of a word combine their bits by shuffles.
 __global__ void k_int8_rowscan(const __half* __restrict__ A, int64_t n, int64_t K, int64_t rows, int64_t words,
                                float tau, uint32_t* __restrict__ sets, uint32_t* __restrict__ uni,
-                               float* __restrict__ scales, unsigned* __restrict__ status) {
+                               float* __restrict__ scales, unsigned* __restrict__ status, int vec) {
     const int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (status && i == 0 && lane == 0) *status = 0u;   // the tensor-core product's wait status
@@ -70,7 +70,6 @@ __global__ void k_int8_rowscan(const __half* __restrict__ A, int64_t n, int64_t 
     const __half* a = A + i * K;
     uint32_t* set = sets + (i / rows) * words;
     const int64_t groups = (K + 7) / 8;
-    const bool vec = (K & 7) == 0;
     float m = 0.f;
     for (int64_t g0 = 0; g0 < groups; g0 += 32) {
         const int64_t g = g0 + lane;
@@ -273,7 +272,7 @@ __global__ void k_int8_codes(const __half* __restrict__ A, int64_t n, int64_t K,
                              const uint32_t* __restrict__ uni, const float* __restrict__ scales,
                              const int8_t* __restrict__ Wq, int64_t N, __nv_bfloat16* __restrict__ qa,
                              __nv_bfloat16* __restrict__ qw, int64_t nsets, int* __restrict__ lists,
-                             int list_blocks) {
+                             int list_blocks, int vec) {
     if ((int)blockIdx.x < list_blocks) {
         const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
         if (t < nsets) set_list(sets, words, K, t, lists);
@@ -289,12 +288,20 @@ __global__ void k_int8_codes(const __half* __restrict__ A, int64_t n, int64_t K,
             const uint32_t* set = record_owned ? sets + (r / rows) * words : uni;
             const float s = __ldg(scales + r);
             const uint32_t word = j0 < K ? __ldg(set + (j0 >> 5)) : 0u;
+            // the group's eight entries, one 16-byte load when the rows are whole aligned vectors
+            __align__(16) __half a8[8];
+            if (vec) {
+                *reinterpret_cast<uint4*>(a8) = __ldg(reinterpret_cast<const uint4*>(A + r * K + j0));
+            } else {
+#pragma unroll
+                for (int b = 0; b < 8; ++b) a8[b] = j0 + b < K ? A[r * K + j0 + b] : __float2half(0.f);
+            }
 #pragma unroll
             for (int b = 0; b < 8; ++b) {
                 const int64_t j = j0 + b;
                 int q = 0;
                 if (j < K && s > 0.f && !((word >> (j & 31)) & 1u))
-                    q = (int)rintf((127.0f * __half2float(A[r * K + j])) / s);
+                    q = (int)rintf((127.0f * __half2float(a8[b])) / s);
                 out[b] = __float2bfloat16_rn((float)q);
             }
             *reinterpret_cast<uint4*>(qa + r * Kp + j0) = *reinterpret_cast<const uint4*>(out);
@@ -620,8 +627,11 @@ extern "C" dp_status dp_int8_forward(const void* A, int64_t n, int64_t K, int64_
     if (cudaMemsetAsync(sets, 0, (size_t)(records + 1) * words * 4, s) != cudaSuccess) return DP_ERR_CUDA;
     const bool tensor_cores = K <= 4 * kQChunk;
     unsigned* status = reinterpret_cast<unsigned*>(ws + lay.status);
+    // rows of whole 16-byte vectors on 16-byte boundaries are read as such
+    const int vec = (K % 8 == 0 && (reinterpret_cast<uintptr_t>(A) & 15u) == 0) ? 1 : 0;
     k_int8_rowscan<<<(unsigned)((n + 7) / 8), 256, 0, s>>>(static_cast<const __half*>(A), n, K, rows_per_record, words,
-                                                           tau, sets, uni, scales, tensor_cores ? status : nullptr);
+                                                           tau, sets, uni, scales, tensor_cores ? status : nullptr,
+                                                           vec);
     count_launch(KL_INT8_ROWSCAN);
     if (!tensor_cores) {
         // beyond four exact chunks per tile: the integer product on the CUDA cores
@@ -655,7 +665,7 @@ extern "C" dp_status dp_int8_forward(const void* A, int64_t n, int64_t K, int64_
         const int64_t list_blocks = (records + 1 + 7) / 8;   // a warp per set, 8 warps per block
         k_int8_codes<<<(unsigned)(list_blocks + grid), 256, 0, s>>>(
             static_cast<const __half*>(A), n, K, lay.Kp, rows_per_record, words, record_owned ? 1 : 0, sets, uni,
-            scales, Wq, N, qa, qw, records + 1, lists, (int)list_blocks);
+            scales, Wq, N, qa, qw, records + 1, lists, (int)list_blocks, vec);
     }
     count_launch(KL_INT8_CODES);
     QGemmParams p;

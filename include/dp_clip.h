@@ -303,8 +303,9 @@ dp_status dp_pack_groups(const void* src, void* dst, int64_t B, int64_t T, int64
  * outputs; -1 for invalid sizes (n not a multiple of rows_per_record, n, K,
  * N or rows < 1).
  *
- * dp_int8_forward -- A: device half [n, K] row-major, rows r*rows_per_record
- * .. (r+1)*rows_per_record-1 owned by record r.  With O_r the columns where
+ * dp_int8_forward -- A: device half [n, K] row-major (any 2-byte alignment;
+ * rows that are whole 16-byte vectors on 16-byte boundaries are read as
+ * such), rows r*rows_per_record .. (r+1)*rows_per_record-1 owned by record r.  With O_r the columns where
  * some row of record r has |A| >= tau (tau > 0), U their union, s_i the
  * largest |A_ij| below tau in row i, and O = O_r of the row's record
  * (record_owned != 0) or U (record_owned == 0, batched LLM.int8):

@@ -58,6 +58,29 @@ def test_forward_bit_exact(record_owned, shape):
     assert np.array_equal(got, want.view(np.uint16)), int((got != want.view(np.uint16)).sum())
 
 
+@pytest.mark.parametrize("record_owned", [True, False])
+def test_activations_off_a_16_byte_boundary(record_owned):
+    """A view that starts one element into its buffer (K a multiple of 8): the
+    rows are read element by element and the output is the same bits as from
+    an aligned copy, and the oracle's."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(17)
+    records, rows, K, N = 3, 40, 256, 72
+    buf = torch.randn(records * rows * K + 1, device="cuda", generator=g).half()
+    buf[1 + rows * K + 9] = 7.5                       # an outlier in record 1
+    A = buf[1:].view(records * rows, K)
+    assert A.data_ptr() % 16 != 0
+    W = (torch.randn(N, K, device="cuda", generator=g) * 0.05).half()
+    lin = Int8Linear(W)
+    Y = lin(A, rows, tau=6.0, record_owned=record_owned)
+    Y2 = lin(A.clone(), rows, tau=6.0, record_owned=record_owned)
+    torch.cuda.synchronize()
+    assert torch.equal(Y, Y2)
+    want = oint8.forward(A.cpu().numpy(), rows, lin.Wq.cpu().numpy(), lin.sW.cpu().numpy(),
+                         lin.What.cpu().numpy(), 6.0, record_owned=record_owned)
+    assert np.array_equal(_bits(Y), want.view(np.uint16))
+
+
 def test_appendix_a_witness_on_the_gpu():
     gx = json.load(open(GOLDEN))
     W = torch.tensor(gx["weight"], dtype=torch.float16, device="cuda")
