@@ -696,7 +696,7 @@ dp_status dp_norm_accumulate(dp_ctx* ctx, int layer_id, const void* A, const voi
     if (!ctx) return DP_ERR_INVALID_ARG;
     dp_status st = check_accumulate(ctx, layer_id, A, E, T);
     if (st != DP_OK) return st;
-    if (sqnorm_out && !aligned16(sqnorm_out) && (reinterpret_cast<uintptr_t>(sqnorm_out) & 3u))
+    if (sqnorm_out && (reinterpret_cast<uintptr_t>(sqnorm_out) & 3u))
         return fail(ctx, DP_ERR_INVALID_ARG, "sqnorm_out must be 4-byte aligned");
     DeviceGuard g(ctx->device);
     Layer plan;
@@ -718,6 +718,8 @@ dp_status dp_norm_accumulate_batch(dp_ctx* ctx, int n, const int* layer_ids, con
         for (int j = 0; j < i; ++j)
             if (layer_ids[j] == layer_ids[i])
                 return fail(ctx, DP_ERR_STATE, "layer %d appears twice in one batch", layer_ids[i]);
+        if (sqnorm_out && sqnorm_out[i] && (reinterpret_cast<uintptr_t>(sqnorm_out[i]) & 3u))
+            return fail(ctx, DP_ERR_INVALID_ARG, "sqnorm_out[%d] must be 4-byte aligned", i);
     }
     DeviceGuard g(ctx->device);
     std::vector<Layer> plans((size_t)n);
@@ -836,6 +838,8 @@ dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnor
     if (!ctx) return DP_ERR_INVALID_ARG;
     if (ctx->phase != OPEN) return fail(ctx, DP_ERR_STATE, "dp_clip_factors needs an open, unclipped step");
     if (!std::isfinite(C) || !(C > 0.0f)) return fail(ctx, DP_ERR_INVALID_ARG, "clip bound C must be finite and > 0");
+    if ((reinterpret_cast<uintptr_t>(c_out) & 3u) || (reinterpret_cast<uintptr_t>(total_sqnorm_out) & 3u))
+        return fail(ctx, DP_ERR_INVALID_ARG, "c_out and total_sqnorm_out must be 4-byte aligned");
     for (size_t l = 0; l < ctx->layers.size(); ++l)
         if (!ctx->layers[l].accumulated)
             return fail(ctx, DP_ERR_STATE, "layer %zu was not accumulated in this step", l);

@@ -154,7 +154,8 @@ dp_status dp_set_normalizer(dp_ctx* ctx, double L);
  *                 for T = 1 the closed form ||a_i||^2 ||e_i||^2 (+ ||e_i||^2);
  *   materialize:  n2_i = ||E_i^T A_i||_F^2 (+ ||sum_t E_i[t]||^2), and the
  *                 per-example gradients are kept in context memory for the sum.
- * If sqnorm_out is not NULL it receives this layer's n2 (device float [B]).
+ * If sqnorm_out is not NULL it receives this layer's n2 (device float [B], 4-byte
+ * aligned: DP_ERR_INVALID_ARG otherwise).
  * The per-record result depends only on that record's rows and the shapes:
  * it is bitwise identical whatever B or the other records are (record
  * isolation: "Sensitivity Inflation ...", Proposition 2).
@@ -192,7 +193,8 @@ dp_status dp_norm_accumulate_batch(dp_ctx* ctx, int n, const int* layer_ids,
  * C must be finite and > 0 (DP_ERR_INVALID_ARG).  Every registered layer must
  * have been accumulated in this step (DP_ERR_STATE otherwise: a layer left out
  * would be released without noise).  c_out / total_sqnorm_out, if not NULL,
- * receive c and n2 (device float [B]).  A non-finite n2_i sets the device
+ * receive c and n2 (device float [B], 4-byte aligned: DP_ERR_INVALID_ARG
+ * otherwise).  A non-finite n2_i sets the device
  * status word; dp_clipped_noisy_grad then writes nothing and dp_step_status
  * reports DP_ERR_NONFINITE.
  */
