@@ -189,6 +189,13 @@ def test_call_order_and_argument_errors():
         with pytest.raises(dp.DPError) as e:
             dp.dp_norm_accumulate(ctx, 7, A1, E1, 3)
         assert e.value.status == dp.DP_ERR_INVALID_ARG
+        sq = torch.empty(4, device="cuda")
+        with pytest.raises(dp.DPError) as e:
+            dp.dp_norm_accumulate(ctx, l1, A1, E1, 3, sq.data_ptr() + 2)  # output off a 4-byte boundary
+        assert e.value.status == dp.DP_ERR_INVALID_ARG
+        with pytest.raises(dp.DPError) as e:
+            dp.dp_norm_accumulate_batch(ctx, [l1], [A1], [E1], [3], [sq.data_ptr() + 2])
+        assert e.value.status == dp.DP_ERR_INVALID_ARG
         with pytest.raises(dp.DPError) as e:
             dp.dp_norm_accumulate(ctx, l1, A1, E1, 0)
         assert e.value.status == dp.DP_ERR_SHAPE
@@ -200,6 +207,11 @@ def test_call_order_and_argument_errors():
         with pytest.raises(dp.DPError) as e:
             dp.dp_set_normalizer(ctx, 0.0)
         assert e.value.status == dp.DP_ERR_INVALID_ARG
+        out = torch.empty(8, device="cuda")
+        for c_out, n2_out in ((out.data_ptr() + 2, None), (None, out.data_ptr() + 1)):
+            with pytest.raises(dp.DPError) as e:
+                dp.dp_clip_factors(ctx, 1.0, c_out, n2_out)             # outputs off a 4-byte boundary
+            assert e.value.status == dp.DP_ERR_INVALID_ARG
         dp.dp_clip_factors(ctx, 1.0)
         for bad_sigma in (-0.1, float("nan")):
             with pytest.raises(dp.DPError) as e:
