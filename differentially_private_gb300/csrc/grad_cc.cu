@@ -91,6 +91,16 @@ __global__ void __launch_bounds__(kClipMaxThreads) k_clip(const ClipParams p, fl
         uint4* dst;
         if (rec < p.B && scale_unit(p, t + (int64_t)k * G, rec, &src, &dst)) pre[k] = __ldcs(src);
     }
+    // the slot table of the first round: written by the host before an earlier
+    // step when p.slots_ready, so it is read before the dependency wait
+    SlotRef ref0[kClipLoads];
+    if (p.slots_ready && rec < p.B) {
+#pragma unroll
+        for (int u = 0; u < kClipLoads; ++u) {
+            const int64_t j = t + (int64_t)u * G;
+            if (j < p.total_slots) ref0[u] = p.slots[j];
+        }
+    }
     grid_dep_wait();
     grid_dep_trigger();
     if (p.status_next && blockIdx.x == 0 && threadIdx.x == 0) *p.status_next = 0u;
@@ -103,7 +113,7 @@ __global__ void __launch_bounds__(kClipMaxThreads) k_clip(const ClipParams p, fl
                 const int64_t j = j0 + (int64_t)u * G;
                 v[u] = 0.f;
                 if (j < p.total_slots) {
-                    const SlotRef r = p.slots[j];
+                    const SlotRef r = p.slots_ready && j0 == t ? ref0[u] : p.slots[j];
                     v[u] = __ldcg(r.base + rec * r.stride);
                 }
             }

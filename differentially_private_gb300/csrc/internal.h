@@ -90,6 +90,7 @@ struct ClipParams {
     float C;
     const SlotRef* slots;      // device array: layers in registration order, each layer's slots in order
     int64_t total_slots;
+    int slots_ready;           // the table was uploaded before an earlier step (readable before the dependency wait)
     unsigned* status_next;     // status word of the next step, zeroed by the kernel (or nullptr)
     int nscale;                // pre-scaled operand copies made by the clip kernel
     PrescaleJob scale[kMaxPrescale];

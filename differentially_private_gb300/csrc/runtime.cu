@@ -785,6 +785,7 @@ ClipParams clip_params(dp_ctx* ctx, float C) {
     p.C = C;
     p.slots = nullptr;
     p.total_slots = 0;
+    p.slots_ready = 0;
     p.status_next = ctx->status_words + (ctx->slot ^ 1);
     p.nscale = 0;
     for (Layer& ly : ctx->layers) {
@@ -851,7 +852,8 @@ dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnor
         key[l] = {ctx->layers[l].partial, (int64_t)ctx->layers[l].nslots};
         total += ctx->layers[l].nslots;
     }
-    if (key != ctx->slots_key) {
+    const bool slots_ready = key == ctx->slots_key;
+    if (!slots_ready) {
         // the flat slot table changes only when the layer set or its scratch does
         if (ctx->d_slots_cap < (size_t)total) {
             cudaError_t e = cudaStreamSynchronize(ctx->stream);
@@ -876,6 +878,7 @@ dp_status dp_clip_factors(dp_ctx* ctx, float C, float* c_out, float* total_sqnor
     ClipParams p = clip_params(ctx, C);
     p.slots = ctx->d_slots;
     p.total_slots = total;
+    p.slots_ready = slots_ready ? 1 : 0;
     const cudaError_t e = launch_clip(p, ctx->n2, ctx->c, total_sqnorm_out, c_out, ctx->status, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "clip kernel launch");
     ctx->clean[ctx->slot ^ 1] = true;
