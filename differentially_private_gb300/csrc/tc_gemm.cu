@@ -128,7 +128,6 @@ __device__ __forceinline__ void noise8(uint64_t seed, uint64_t step, uint64_t kb
 }
 
 // S[4q .. 4q+3] += sigma C z at this thread's coordinates k0 + 4q .. k0 + 4q + 3
-constexpr int kNoiseChunks = kColsPerWarp / 4;
 template <int NC>
 __device__ __forceinline__ void add_noise_chunk_n(const SumParams& p, uint64_t k0, int q, float (&S)[NC]) {
     const uint64_t k = k0 + 4u * (uint64_t)q;
@@ -145,9 +144,6 @@ __device__ __forceinline__ void add_noise_chunk_n(const SumParams& p, uint64_t k
 #pragma unroll
             for (int j = 0; j < 4; ++j) S[4 * qq + j] = fmaf(p.scale, z[j], S[4 * qq + j]);
         }
-}
-__device__ __forceinline__ void add_noise_chunk(const SumParams& p, uint64_t k0, int q, float (&S)[kColsPerWarp]) {
-    add_noise_chunk_n<kColsPerWarp>(p, k0, q, S);
 }
 
 __global__ void __launch_bounds__(kFoldThreads, 1) k_clipped_sum_tc(const __grid_constant__ SumParams p) {
