@@ -648,18 +648,22 @@ def run_ours(args, w):
             return e0.elapsed_time(e1)
 
         link_ms = min(timed(lambda: h2d_copy(arena)) for _ in range(3))
+        d2h_link_ms = min(timed(lambda: garena_pin.copy_(garena, non_blocking=True)) for _ in range(3))
 
-        copy_ev = []
+        copy_ev, read_ev = [], []
 
         def serial(n):
             for _ in range(n):
-                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
                 ev[0].record(stream)
                 h2d_copy(arena)
                 ev[1].record(stream)
-                copy_ev.append(ev)
                 step()
+                ev[2].record(stream)
                 garena_pin.copy_(garena, non_blocking=True)
+                ev[3].record(stream)
+                copy_ev.append((ev[0], ev[1]))
+                read_ev.append((ev[2], ev[3]))
 
         arena2 = torch.empty_like(arena)
         A2, E2 = carve(arena2)
@@ -690,8 +694,10 @@ def run_ours(args, w):
         serial(2)
         pipelined(2)
         copy_ev.clear()
+        read_ev.clear()
         ser_ms = max_over_ranks(timed(lambda: serial(ke)), device)
         loop_copy_ms = statistics.median(a.elapsed_time(b) for a, b in copy_ev)
+        loop_read_ms = statistics.median(a.elapsed_time(b) for a, b in read_ev)
         ems = max_over_ranks(timed(lambda: pipelined(ke)), device)
         st = dp.dp_step_status(ctx)
         if st != dp.DP_OK:
@@ -707,7 +713,9 @@ def run_ours(args, w):
                           if pipe_value >= ser_value else "copy, step and read-back one after the other on one stream"),
                "pipelined_value": pipe_value, "serial_value": ser_value,
                "h2d_link_gbs": h2d / (link_ms / 1e3) / 1e9,
-               "h2d_gbs_in_serial_loop": h2d / (loop_copy_ms / 1e3) / 1e9}
+               "h2d_gbs_in_serial_loop": h2d / (loop_copy_ms / 1e3) / 1e9,
+               "d2h_link_gbs": d2h / (d2h_link_ms / 1e3) / 1e9,
+               "d2h_gbs_in_serial_loop": d2h / (loop_read_ms / 1e3) / 1e9}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
